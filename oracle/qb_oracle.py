@@ -1,0 +1,471 @@
+"""Plain CPU oracle of the Stable LatentMoE forward with Quantile Balancing.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may use it.  It shares no code with the CUDA path; its inputs come
+from ``qb_inputs`` (seeded draws, no method arithmetic).
+
+Sources, cited by page title and section:
+
+* [K3-width]  "Kimi K3 模型结构（5）：宽度维度，Stable LatentMoE" (xhh.club):
+  sections 内容提要 (summary), 延伸解读 (extended reading; sub-sections
+  "Why a half-width latent space", "What each part of the Stable trio solves",
+  "Quantile Balancing vs DeepSeek-V3 routing", "Parameter scale and
+  deployment") and its Q&A (questions on SiTU-GLU, Quantile Balancing,
+  routing, RMSNorm and the shared expert).
+* [K3-explainer]  "KIMI K3" LatentMoE explainer (dimsnsums.com), section
+  "Why does the router need three moves?".
+* [Concept-wiki]  "Stable LatentMoE" concept page (codewithdark), sections
+  "Overview" and "Key Components".
+
+Precision contract.  Routing is exact fp32 (IEEE round-to-nearest-even, one
+rounding per operation, no fused multiply-add): numpy's elementwise float32
+ufuncs satisfy this, and no reduction here uses numpy's pairwise ``sum``.  The
+dense layer is fp64, rounded to the storage type (bf16 or fp32) at the points
+where the GPU stores a tensor.
+
+Every function below is pinned by tests that do not restate it (closed forms,
+brute force, invariants, hand-worked fixtures in ``tests/golden``).  The one
+exception is recorded here: agreement with the real K3 model is **parity
+unpinned** (the pages give no weights, outputs or worked numbers).
+"""
+from __future__ import annotations
+
+import itertools
+from typing import Callable, Optional
+
+import numpy as np
+
+F32 = np.float32
+
+# ---------------------------------------------------------------------------
+# Router score
+# ---------------------------------------------------------------------------
+
+# Constants of the fp32 score recipe (see sigmoid_score).
+_LOG2E = F32(1.4426950408889634)          # 1/ln 2
+_LN2_HI = F32(0.693145751953125)          # ln 2 rounded to 15 significant bits
+_LN2_LO = F32(1.4286068203094173e-06)     # ln 2 - _LN2_HI
+_TAYLOR = [F32(1.0 / 5040.0), F32(1.0 / 720.0), F32(1.0 / 120.0), F32(1.0 / 24.0),
+           F32(1.0 / 6.0), F32(0.5), F32(1.0), F32(1.0)]
+_CLAMP = F32(80.0)
+
+
+def sigmoid_score(logits: np.ndarray) -> np.ndarray:
+    """Router score s = sigmoid(logit) as an exactly specified fp32 result.
+
+    [K3-width] Q&A on routing: the router applies a sigmoid to its full-width
+    logits.  The pages fix no precision, and the score decides the routing
+    integers, so the score is pinned to one fp32 recipe that any IEEE machine
+    reproduces bit for bit (every step one correctly rounded fp32 op):
+
+        x' = clamp(x, -80, 80);  y = -x'
+        j  = rint(y * log2e)                      (ties to even)
+        r  = (y - j*LN2_HI) - j*LN2_LO            (Cody-Waite reduction, |r| <= 0.35)
+        p  = Taylor series of e^r to degree 7, Horner form
+        e  = p * 2^j                              (exact power-of-two scaling)
+        s  = 1 / (1 + e)
+
+    The degree-7 remainder is below 0.05 ulp; the result is within 2 ulp of
+    the correctly rounded sigmoid (pinned by the tests).  Logits beyond +-80
+    are clamped, which only moves scores below 2e-35.
+    """
+    x = np.asarray(logits, dtype=F32)
+    y = -np.clip(x, -_CLAMP, _CLAMP)
+    j = np.rint(y * _LOG2E)
+    r = (y - j * _LN2_HI) - j * _LN2_LO
+    p = _TAYLOR[0]
+    for c in _TAYLOR[1:]:
+        p = p * r + c
+    two_j = ((j.astype(np.int32) + 127) << 23).view(F32)
+    e = p * two_j
+    return (F32(1.0) / (F32(1.0) + e)).astype(F32)
+
+
+def router_logits(x: np.ndarray, w_router: np.ndarray, offset: Optional[np.ndarray]) -> np.ndarray:
+    """logits = x . W_r^T + o in fp64, rounded once to fp32.
+
+    [K3-width] Q&A on routing: scores are computed on the full-width input
+    (no latent compression before the router).  o is a per-expert router
+    offset (part of the router's parameters; used by the workloads to skew
+    the load)."""
+    z = np.asarray(x, np.float64) @ np.asarray(w_router, np.float64).T
+    if offset is not None:
+        z = z + np.asarray(offset, np.float64)[None, :]
+    return z.astype(F32)
+
+
+# ---------------------------------------------------------------------------
+# Quantile Balancing
+# ---------------------------------------------------------------------------
+
+def qb_targets(T: int, n: int, k: int) -> np.ndarray:
+    """Per-expert target loads r_j with sum r_j = T*k.
+
+    [K3-width] Q&A on Quantile Balancing: every expert should receive exactly
+    the target load m*k/n (m = tokens).  That is not an integer in general;
+    the reading taken is the array-split rounding: floor(T*k/n) for every
+    expert plus one for the first (T*k mod n) experts."""
+    base, extra = divmod(T * k, n)
+    r = np.full(n, base, dtype=np.int64)
+    r[:extra] += 1
+    return r
+
+
+def biased(s: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """v = fl32(s + b): the quantity top-k selection ranks ([K3-width] Q&A on
+    routing: the bias e_score_correction_bias is added to the score for
+    selection)."""
+    return (np.asarray(s, F32) + np.asarray(b, F32)[None, :]).astype(F32)
+
+
+def rank_experts(v: np.ndarray) -> np.ndarray:
+    """Per token, expert indices ordered by (v descending, index ascending).
+
+    A stable sort of -v keeps equal values in index order, which is the tie
+    rule (lower expert index wins)."""
+    return np.argsort(-v, axis=1, kind="stable")
+
+
+def qb_margins(s: np.ndarray, b: np.ndarray, k: int) -> np.ndarray:
+    """Margins m[t, j] = s[t, j] - tau[t, j] (fp32), -0 canonicalised to +0.
+
+    [K3-width] Q&A on Quantile Balancing: the bias comes from a quantile of
+    "the margin"; 延伸解读 "QB vs DeepSeek-V3": QB is coordinate descent on the
+    dual of the balanced assignment problem.  In the coordinate step for
+    expert j (all other biases fixed), token t admits j iff
+    s[t, j] + b_j beats tau[t, j], the token's k-th best biased score among
+    the *other* experts.  So m[t, j] is the raw score's lead over that cut.
+
+    tau by definition is the k-th largest of {v[t, l] : l != j}.  With the
+    token's ranking by v, that value is the (k+1)-th ranked v when j is in
+    the token's top k, and the k-th ranked v otherwise (removing j from the
+    list moves later ranks up by one only when j is ranked before them).
+    """
+    s = np.asarray(s, F32)
+    T, n = s.shape
+    v = biased(s, b)
+    order = rank_experts(v)
+    rows = np.arange(T)
+    v_k = v[rows, order[:, k - 1]]
+    v_k1 = v[rows, order[:, k]]
+    in_top = np.zeros((T, n), dtype=bool)
+    in_top[rows[:, None], order[:, :k]] = True
+    tau = np.where(in_top, v_k1[:, None], v_k[:, None]).astype(F32)
+    m = (s - tau).astype(F32)
+    m[m == 0] = F32(0.0)
+    return m
+
+
+def qb_coordinate_bias(margins_j: np.ndarray, r_j: int) -> np.float32:
+    """Exact coordinate minimiser for one expert: b'_j = -q_j.
+
+    [K3-width] Q&A on Quantile Balancing: the bias is the (1 - k/n) quantile
+    of the margin (with a sign: admission needs m + b > 0), so that exactly
+    the target load is admitted.  Sorting the T margins descending as
+    M_1 >= ... >= M_T, any q in [M_{r+1}, M_r) admits exactly r tokens; the
+    midpoint is taken:
+        q = fl(fl(M_r + M_{r+1}) * 0.5)      for 1 <= r <= T-1
+        q = fl(M_1 + 1)                      for r = 0   (admit nobody)
+        q = fl(M_T - 1)                      for r >= T  (admit everybody)
+    """
+    M = np.sort(np.asarray(margins_j, F32))[::-1]
+    T = M.shape[0]
+    if r_j <= 0:
+        q = M[0] + F32(1.0)
+    elif r_j >= T:
+        q = M[T - 1] - F32(1.0)
+    else:
+        q = (M[r_j - 1] + M[r_j]) * F32(0.5)
+    return F32(-q)
+
+
+def common_offset(b_raw: np.ndarray) -> np.ndarray:
+    """Subtract the common offset: b = fl(b' - c), c = fl(tree_sum(b') / n).
+
+    [K3-width] Q&A on Quantile Balancing: the bias is the margin quantile
+    "minus a common offset".  Selection is invariant to a common shift (the
+    dual is unchanged when every bias moves together), so the reading taken
+    is the zero-mean normalisation.  The sum is a fixed pairwise tree: pad
+    to P = 2^ceil(log2 n) with +0, then a_i <- a_{2i} + a_{2i+1} level by
+    level, so the fp32 result is unique."""
+    b_raw = np.asarray(b_raw, F32)
+    n = b_raw.shape[0]
+    P = 1 << max(0, (n - 1).bit_length())
+    a = np.zeros(P, dtype=F32)
+    a[:n] = b_raw
+    while a.shape[0] > 1:
+        a = (a[0::2] + a[1::2]).astype(F32)
+    c = F32(a[0] / F32(n))
+    return (b_raw - c).astype(F32)
+
+
+def qb_sweep_jacobi(s: np.ndarray, b: np.ndarray, k: int) -> np.ndarray:
+    """One QB sweep in which every expert's coordinate step uses the same b.
+
+    [K3-width] 延伸解读 "QB vs DeepSeek-V3" (coordinate descent on the dual,
+    jumping to the exact coordinate minimiser, no step size) and Q&A on
+    Quantile Balancing (quantiles may be formed from histograms so that the
+    exchange is cheap; one step reaches balance).  Forming all experts'
+    quantiles from one set of biases in one pass is what makes a single
+    histogram exchange possible, so the parallel (Jacobi) sweep is the
+    reading taken for the hot path."""
+    s = np.asarray(s, F32)
+    T, n = s.shape
+    r = qb_targets(T, n, k)
+    m = qb_margins(s, b, k)
+    b_raw = np.array([qb_coordinate_bias(m[:, j], int(r[j])) for j in range(n)], dtype=F32)
+    return common_offset(b_raw)
+
+
+def qb_sweep_gauss_seidel(s: np.ndarray, b: np.ndarray, k: int) -> np.ndarray:
+    """One cyclic coordinate-descent sweep (experts 0..n-1, each step sees the
+    latest biases), then the common offset.  The literal form of
+    [K3-width] 延伸解读 "QB vs DeepSeek-V3"; used by the oracle's invariant
+    tests.  tau is computed here directly from its definition (k-th largest
+    biased score among the other experts)."""
+    s = np.asarray(s, F32)
+    T, n = s.shape
+    r = qb_targets(T, n, k)
+    b = np.array(b, dtype=F32, copy=True)
+    for j in range(n):
+        v = biased(s, b)
+        v[:, j] = -np.inf
+        tau = -np.sort(-v, axis=1)[:, k - 1]
+        m = (s[:, j] - tau).astype(F32)
+        m[m == 0] = F32(0.0)
+        b[j] = qb_coordinate_bias(m, int(r[j]))
+    return common_offset(b)
+
+
+def route_topk(s: np.ndarray, b: np.ndarray, k: int):
+    """Biased top-k selection with raw-score mixture weights.
+
+    [K3-width] Q&A on routing: the top-k experts are chosen on score + bias,
+    and the mixture weights are the original scores renormalised over the
+    chosen experts (the bias only affects selection).  [K3-explainer]: the
+    bias decides admission while the router scores still set the weights.
+
+    idx[t] lists the chosen experts in rank order (v descending, lower index
+    first on ties).  The normaliser is summed in rank order in fp32 and each
+    weight is one IEEE division.  No routed scaling factor is applied (the
+    pages give none).  loads[j] counts the routes to expert j."""
+    s = np.asarray(s, F32)
+    T, n = s.shape
+    order = rank_experts(biased(s, b))
+    idx = order[:, :k].astype(np.int32)
+    sel = s[np.arange(T)[:, None], idx]
+    total = sel[:, 0].copy()
+    for i in range(1, k):
+        total = (total + sel[:, i]).astype(F32)
+    w = (sel / total[:, None]).astype(F32)
+    loads = np.bincount(idx.ravel(), minlength=n).astype(np.int32)
+    return idx, w, loads
+
+
+def moe_route_qb(logits: np.ndarray, bias_in: Optional[np.ndarray], k: int,
+                 qb_sweeps: int = 1, mode: str = "jacobi"):
+    """The router: scores, QB biases, biased top-k, weights and loads.
+
+    qb_sweeps = 0 keeps the bias frozen ([K3-width] Q&A on routing: the bias
+    is frozen at inference).  Otherwise the sweeps start from bias_in and the
+    final bias routes the same batch ([K3-width] 延伸解读 "Stable trio": the
+    load reaches its target exactly)."""
+    s = sigmoid_score(logits)
+    T, n = s.shape
+    b = np.zeros(n, F32) if bias_in is None else np.array(bias_in, dtype=F32, copy=True)
+    sweep = qb_sweep_jacobi if mode == "jacobi" else qb_sweep_gauss_seidel
+    for _ in range(qb_sweeps):
+        b = sweep(s, b, k)
+    idx, w, loads = route_topk(s, b, k)
+    return s, b, idx, w, loads
+
+
+def dual_objective(s: np.ndarray, b: np.ndarray, k: int, r: np.ndarray) -> float:
+    """D(b) = sum_t topk_sum(s_t + b) - sum_j r_j b_j (fp64): the dual of the
+    balanced assignment LP (max sum of s over assignments with k experts per
+    token and r_j tokens per expert) named in [K3-width] 延伸解读 "QB vs
+    DeepSeek-V3"."""
+    v = np.asarray(s, np.float64) + np.asarray(b, np.float64)[None, :]
+    top = -np.sort(-v, axis=1)[:, :k]
+    return float(top.sum() - np.dot(np.asarray(r, np.float64), np.asarray(b, np.float64)))
+
+
+def brute_force_assignment(s: np.ndarray, k: int, r: np.ndarray):
+    """Best total score over every assignment with k distinct experts per token
+    and exactly r_j tokens per expert (exhaustive search; tiny inputs only)."""
+    s = np.asarray(s, np.float64)
+    T, n = s.shape
+    subsets = list(itertools.combinations(range(n), k))
+    best = [-np.inf, None]
+    load = np.zeros(n, dtype=np.int64)
+    r = np.asarray(r, np.int64)
+    choice = [None] * T
+
+    def rec(t, acc):
+        if t == T:
+            if np.array_equal(load, r) and acc > best[0]:
+                best[0], best[1] = acc, list(choice)
+            return
+        for sub in subsets:
+            if any(load[j] >= r[j] for j in sub):
+                continue
+            for j in sub:
+                load[j] += 1
+            choice[t] = sub
+            rec(t + 1, acc + sum(s[t, j] for j in sub))
+            for j in sub:
+                load[j] -= 1
+
+    rec(0, 0.0)
+    return best[0], best[1]
+
+
+# ---------------------------------------------------------------------------
+# Dense layer (fp64, rounded at storage points)
+# ---------------------------------------------------------------------------
+
+def round_to(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Round fp64 values to the storage type and return them as fp64.
+    bf16 goes through fp32 (round to nearest even at both steps)."""
+    a32 = np.asarray(a, np.float64).astype(F32)
+    if dtype == "f32":
+        return a32.astype(np.float64)
+    u = a32.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return ((u.astype(np.uint32) << 16).view(F32)).astype(np.float64)
+
+
+def situ_glu(g: np.ndarray, u: np.ndarray, beta1: float = 4.0, beta2: float = 25.0) -> np.ndarray:
+    """SiTU-GLU: a = b1*tanh(g/b1), b = b2*tanh(u/b2), out = a*sigmoid(a)*b.
+
+    [K3-width] Q&A on SiTU-GLU: SwiGLU with a softcap beta*tanh(x/beta) on the
+    gate branch (beta1 = 4) and the up branch (beta2 = 25); 延伸解读 "Stable
+    trio": the caps bound the output (beta1*beta2 = 100).  [K3-explainer]:
+    small inputs behave like SwiGLU (hidden_act: situ)."""
+    g = np.asarray(g, np.float64)
+    u = np.asarray(u, np.float64)
+    a = beta1 * np.tanh(g / beta1)
+    bb = beta2 * np.tanh(u / beta2)
+    return a * (1.0 / (1.0 + np.exp(-a))) * bb
+
+
+def rmsnorm(y: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """z = y / sqrt(mean(y^2) + eps) * gamma over the latent axis.
+
+    [K3-width] Q&A on RMSNorm: placed after the latent aggregation and before
+    the up-projection, making the routed branch insensitive to scale.  The
+    pages are silent on a gain; an elementwise gain gamma is taken."""
+    y = np.asarray(y, np.float64)
+    rms = np.sqrt(np.mean(y * y, axis=-1, keepdims=True) + eps)
+    return y / rms * np.asarray(gamma, np.float64)
+
+
+def shared_mlp(x: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_out: np.ndarray,
+               dtype: str) -> np.ndarray:
+    """Merged shared expert: act = SiTU-GLU(x W_g^T, x W_u^T) stored, then
+    act W_o^T (fp64, not rounded: its sum with the routed branch is).
+
+    [K3-width] Q&A on the shared expert: the two shared experts are one MLP
+    of intermediate 6144 (3072 each) at full width, added straight to the
+    routed output.  [K3-explainer]: hidden_act situ is the model's activation,
+    taken here for the shared MLP too."""
+    x = np.asarray(x, np.float64)
+    act = round_to(situ_glu(x @ np.asarray(w_gate, np.float64).T,
+                            x @ np.asarray(w_up, np.float64).T), dtype)
+    return act @ np.asarray(w_out, np.float64).T
+
+
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def mxfp4_decode(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """MXFP4 -> fp64: E2M1 code value times 2^(E8M0 - 127), per 32 along K.
+
+    [K3-width] 延伸解读 "Parameter scale and deployment": at deployment only
+    the routed experts' weights are MXFP4.  Codes follow the OCP Microscaling
+    spec: bit 3 is the sign, bits 0-2 index {0, .5, 1, 1.5, 2, 3, 4, 6}.  An
+    E8M0 byte of 255 (NaN) is not a valid weight scale."""
+    packed = np.asarray(packed, np.uint8)
+    lo = packed & 0x0F
+    hi = packed >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+    mag = E2M1_VALUES[codes & 7]
+    val = np.where(codes & 8, -mag, mag)
+    sc = np.asarray(scales, np.int64)
+    if np.any(sc == 255):
+        raise ValueError("E8M0 scale 255 (NaN) is not a valid weight scale")
+    mult = np.ldexp(1.0, sc - 127)
+    return val * np.repeat(mult, 32, axis=-1)
+
+
+class LayerWeights:
+    """fp64 views of a workload's weights, drawn on demand (experts one by one)."""
+
+    def __init__(self, inputs):
+        self.inp = inputs
+        self.s = inputs.shape
+        self._dense = {}
+
+    def dense(self, name) -> np.ndarray:
+        if name not in self._dense:
+            self._dense[name] = self.inp.values(name).astype(np.float64)
+        return self._dense[name]
+
+    def expert(self, name, e: int) -> np.ndarray:
+        if self.s.wfmt == "mxfp4":
+            packed, scales = self.inp.expert_mxfp4(name, e)
+            return mxfp4_decode(packed, scales)
+        raw = self.inp.expert_raw(name, e)
+        from qb_inputs import bf16_bits_to_f32
+        vals = bf16_bits_to_f32(raw) if raw.dtype == np.uint16 else raw
+        return vals.astype(np.float64)
+
+
+def layer_forward(inputs, tokens: Optional[np.ndarray] = None, logits: Optional[np.ndarray] = None,
+                  bias_in: Optional[np.ndarray] = None, qb_sweeps: Optional[int] = None,
+                  mode: str = "jacobi", rms_eps: float = 1e-6,
+                  beta1: float = 4.0, beta2: float = 25.0, weights: Optional[LayerWeights] = None):
+    """Stable LatentMoE forward for the tokens in ``tokens`` (default: all).
+
+    Routing always covers all T tokens (QB's quantiles are over the batch);
+    the dense part runs for the requested tokens only.  Steps and sources:
+
+    1. scores, QB biases, top-k, weights, loads (moe_route_qb).  ``logits``
+       may be given (fp32 [T, n]); otherwise router_logits(x, W_r, o).
+    2. h = round(x W_down^T): [K3-width] 延伸解读 "half-width latent": the
+       input is compressed 7168 -> 3584 before the experts.
+    3. per route (t, i), e = idx[t, i]: act = round(SiTU-GLU(h W_g[e]^T,
+       h W_u[e]^T)); e_ti = round(act W_o[e]^T): per-expert GLU in latent space.
+    4. y = sum_i w[t, i] e_ti;  z = round(RMSNorm(y)):  [K3-width] Q&A on RMSNorm.
+    5. out = round(z W_up^T + act_s W_so^T): up-projection back to d plus the
+       merged shared expert ([K3-width] Q&A on the shared expert).
+    """
+    s = inputs.shape
+    W = weights or LayerWeights(inputs)
+    X = W.dense("x")
+    if logits is None:
+        logits = router_logits(X, W.dense("w_router"), W.dense("router_offset"))
+    sweeps = s.qb_sweeps if qb_sweeps is None else qb_sweeps
+    scores, bias, idx, w, loads = moe_route_qb(logits, bias_in, s.k, sweeps, mode)
+
+    tok = np.arange(s.T) if tokens is None else np.asarray(tokens)
+    Xs = X[tok]
+    h = round_to(Xs @ W.dense("w_down").T, s.dtype)
+    sub_idx = idx[tok]
+    E = np.zeros((len(tok), s.k, s.latent), dtype=np.float64)
+    for e in np.unique(sub_idx):
+        rows, cols = np.nonzero(sub_idx == e)
+        wg, wu, wo = W.expert("w_gate", e), W.expert("w_up", e), W.expert("w_out", e)
+        hr = h[rows]
+        act = round_to(situ_glu(hr @ wg.T, hr @ wu.T, beta1, beta2), s.dtype)
+        E[rows, cols] = round_to(act @ wo.T, s.dtype)
+    y = np.einsum("tk,tkl->tl", w[tok].astype(np.float64), E)
+    z = round_to(rmsnorm(y, W.dense("gamma"), rms_eps), s.dtype)
+    acc = z @ W.dense("w_proj_up").T
+    if s.m_s:
+        acc = acc + shared_mlp(Xs, W.dense("w_shared_gate"), W.dense("w_shared_up"),
+                               W.dense("w_shared_out"), s.dtype)
+    out = round_to(acc, s.dtype)
+    return dict(scores=scores, bias=bias, idx=idx, w=w, loads=loads, logits=logits,
+                tokens=tok, h=h, z=z, out=out)
