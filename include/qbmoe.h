@@ -1,0 +1,222 @@
+/*
+ * qbmoe — Stable LatentMoE forward with Quantile Balancing on one GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  "Device" pointers are CUDA device
+ * (or managed) memory on the current device; "host" pointers are ordinary
+ * host memory.  Every call that takes a stream is asynchronous and
+ * stream-ordered on it (NULL = the legacy default stream); nothing here
+ * synchronises the host except qbmoe_status and the functions documented as
+ * synchronous.  A negative return value means nothing was launched and no
+ * output was touched.
+ *
+ * Sources, by page title and section:
+ *   [K3-width]  "Kimi K3 模型结构（5）：宽度维度，Stable LatentMoE" (xhh.club),
+ *               its 延伸解读 (extended reading) sections and its Q&A.
+ *   [K3-explainer]  "KIMI K3" LatentMoE explainer (dimsnsums.com),
+ *               "Why does the router need three moves?".
+ */
+#ifndef QBMOE_H
+#define QBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Compatible with cudaStream_t. */
+typedef struct CUstream_st* qbmoe_stream_t;
+
+typedef enum {
+    QBMOE_OK = 0,
+    QBMOE_EINVAL = -1,     /* bad size, null or misaligned pointer, unsupported option */
+    QBMOE_ENOMEM = -2,     /* device allocation failed (qbmoe_create only) */
+    QBMOE_ECUDA = -3,      /* a CUDA runtime/driver call or a launch failed */
+    QBMOE_EARCH = -4,      /* current device is not compute capability 10.3 */
+    QBMOE_EWORKSPACE = -5, /* caller workspace too small / ctx built for fewer tokens */
+    QBMOE_ETIMEOUT = -6,   /* a kernel's bounded wait expired (reported by qbmoe_status) */
+    QBMOE_EDEVICE = -7     /* a kernel's own check failed (reported by qbmoe_status) */
+} qbmoe_status_t;
+
+/* Storage types. */
+enum { QBMOE_F32 = 0, QBMOE_BF16 = 1 };
+/* Routed-expert weight formats. */
+enum { QBMOE_W_F32 = 0, QBMOE_W_BF16 = 1, QBMOE_W_MXFP4 = 2 };
+
+/* Limits of this build. */
+#define QBMOE_MAX_EXPERTS 1024
+#define QBMOE_MAX_TOPK 32
+
+/*
+ * Scores.  s = sigmoid(logit) is an exactly specified fp32 result: clamp the
+ * logit to [-80, 80], y = -x, j = rint(y*0x1.715476p+0),
+ * r = (y - j*0x1.62e4p-1) - j*0x1.7f7d1cp-20, p = degree-7 Taylor series of
+ * e^r in Horner form (coefficients 1/5040, 1/720, 1/120, 1/24, 1/6 rounded to
+ * fp32, then 1/2, 1, 1), e = p*2^j, s = 1/(1+e); every step one IEEE fp32
+ * operation, no fused multiply-add.  ([K3-width] Q&A on routing: sigmoid
+ * router on the full-width input.)
+ */
+
+/*
+ * ---------------------------------------------------------------------------
+ * moe_route_qb — router scores, Quantile Balancing, biased top-k.
+ *
+ * [K3-width] Q&A on Quantile Balancing: each expert's bias is the (1 - k/n)
+ * quantile over tokens of its margin, minus a common offset, so that every
+ * expert admits its target load T*k/n; 延伸解读 "QB vs DeepSeek-V3": one
+ * exact coordinate-descent step on the balanced-assignment dual.  Q&A on
+ * routing: top-k on score + bias, mixture weights = raw scores renormalised
+ * over the chosen k, bias frozen at inference (qb_sweeps = 0).
+ *
+ * Per sweep (Jacobi: every expert from the same bias b):
+ *   v = fl(s + b); per token the experts ranked by (v desc, index asc);
+ *   tau[t][j] = the (k+1)-th ranked v if j is in the token's top k, else the
+ *   k-th; m[t][j] = fl(s - tau) (-0 -> +0);
+ *   r_j = floor(T*k/n) + (j < T*k mod n);  M = m[.][j] sorted descending;
+ *   q_j = fl(fl(M_r + M_{r+1}) * 0.5)  (r=0: fl(M_1 + 1); r>=T: fl(M_T - 1));
+ *   b'_j = -q_j;  c = fl(S / n), S = pairwise tree sum of b' padded with +0
+ *   to 2^ceil(log2 n); b = fl(b' - c).
+ * Final: idx[t] = top k of fl(s + b) in rank order; w[t][i] =
+ * fl(s[idx_i] / sum), sum accumulated in rank order in fp32;
+ * loads[j] = number of routes to j.
+ *
+ * T >= 1, 2 <= n <= QBMOE_MAX_EXPERTS, 1 <= k < n, k <= QBMOE_MAX_TOPK,
+ * qb_sweeps >= 0.
+ * logits   [T, n] fp32 device, row-major, pre-sigmoid.
+ * bias_in  [n] fp32 device (NULL = zeros).  bias_out [n] fp32 device; may
+ *          equal bias_in.
+ * scores   [T, n] fp32 device out.  topk_idx [T, k] int32, topk_w [T, k]
+ *          fp32, loads [n] int32 device out.
+ * workspace: device, >= qbmoe_route_workspace_bytes(T, n, k) bytes, 256-byte
+ *          aligned; owned by the caller; contents are scratch.
+ * All device pointers 16-byte aligned.  Results are bit-reproducible.
+ * Returns QBMOE_OK after enqueueing, or a negative code (nothing launched).
+ */
+size_t qbmoe_route_workspace_bytes(int T, int n, int k);
+int moe_route_qb(int T, int n, int k, int qb_sweeps,
+                 const float* logits, const float* bias_in, float* bias_out,
+                 float* scores, int32_t* topk_idx, float* topk_w, int32_t* loads,
+                 void* workspace, size_t workspace_bytes, qbmoe_stream_t stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * Layer context.
+ */
+typedef struct {
+    int d;              /* model width */
+    int latent;         /* latent width ([K3-width] 延伸解读: 7168 -> 3584) */
+    int n_experts;      /* routed experts */
+    int top_k;          /* experts per token */
+    int expert_inter;   /* routed expert GLU intermediate */
+    int shared_inter;   /* merged shared-expert intermediate; 0 = no shared expert */
+    float situ_beta1;   /* gate softcap, 4 on the pages */
+    float situ_beta2;   /* up softcap, 25 on the pages */
+    float rms_eps;      /* RMSNorm epsilon */
+    int act_dtype;      /* QBMOE_F32 | QBMOE_BF16: activations and dense weights */
+    int expert_wfmt;    /* QBMOE_W_F32 | QBMOE_W_BF16 | QBMOE_W_MXFP4 */
+    int qb_sweeps;      /* 0 = frozen bias (inference); 1 = one QB step */
+} qbmoe_config;
+
+/*
+ * Weights: device pointers in canonical K-major layouts ("[rows, K]", K
+ * contiguous), typed by act_dtype unless stated.  The caller owns them and
+ * must keep them alive and unchanged while the context uses them (the
+ * context keeps pointers, not copies).
+ *   w_router [n, d]; router_offset [n] fp32 or NULL (per-expert logit offset)
+ *   w_down [latent, d]
+ *   w_gate, w_up [n, m, latent]; w_out [n, latent, m]    (expert_wfmt)
+ *     MXFP4: values packed two per byte (element 2i in the low nibble) as
+ *     [rows, K/2] u8, scales E8M0 [rows, K/32] u8 in s_gate/s_up/s_out.
+ *   rms_gamma [latent] fp32
+ *   w_proj_up [d, latent]
+ *   w_shared_gate, w_shared_up [m_s, d]; w_shared_out [d, m_s]  (m_s > 0)
+ */
+typedef struct {
+    const void* w_router;
+    const float* router_offset;
+    const void* w_down;
+    const void* w_gate;
+    const void* w_up;
+    const void* w_out;
+    const uint8_t* s_gate;
+    const uint8_t* s_up;
+    const uint8_t* s_out;
+    const float* rms_gamma;
+    const void* w_proj_up;
+    const void* w_shared_gate;
+    const void* w_shared_up;
+    const void* w_shared_out;
+} qbmoe_weights;
+
+typedef struct qbmoe_ctx qbmoe_ctx;
+
+/* Validate cfg, allocate the context's device workspace for up to max_tokens
+ * tokens on the current device (synchronous).  *out = NULL on failure. */
+int qbmoe_create(qbmoe_ctx** out, const qbmoe_config* cfg, int max_tokens);
+/* Bytes of device workspace qbmoe_create allocates for these sizes. */
+size_t qbmoe_layer_workspace_bytes(const qbmoe_config* cfg, int max_tokens);
+/* Record the weight pointers (host call, no device work, no copies). */
+int qbmoe_set_weights(qbmoe_ctx* ctx, const qbmoe_weights* w);
+/* Free the context's workspace (synchronous). NULL is a no-op. */
+int qbmoe_destroy(qbmoe_ctx* ctx);
+
+/*
+ * moe_latent_forward — one Stable LatentMoE layer forward for T tokens.
+ *
+ *   scores = sigmoid(x W_r^T + o) (or of logits_in when given)   [K3-width] Q&A routing
+ *   b, idx, w, loads as moe_route_qb
+ *   h   = round(x W_down^T)                                       [K3-width] 延伸解读 latent
+ *   act = round(SiTU-GLU(h W_g[e]^T, h W_u[e]^T)) per route       [K3-width] Q&A SiTU-GLU
+ *         SiTU-GLU(g, u) = a*sigmoid(a)*b, a = b1*tanh(g/b1), b = b2*tanh(u/b2)
+ *   e   = round(act W_o[e]^T)
+ *   z   = round(RMSNorm(sum_i w_i e_i) * gamma)                   [K3-width] Q&A RMSNorm
+ *   out = round(z W_proj_up^T + act_s W_shared_out^T),
+ *         act_s = round(SiTU-GLU(x W_shared_gate^T, x W_shared_up^T))   Q&A shared expert
+ * ("round" = to act_dtype; accumulation is fp32.)
+ *
+ * x [T, d] act_dtype device; out [T, d] act_dtype device.
+ * logits_in: NULL, or [T, n] fp32 device router logits used instead of the
+ *   router GEMM (x W_r^T + o is then not computed).
+ * bias_in [n] fp32 device or NULL (zeros); bias_out [n] fp32 device (may
+ *   alias bias_in) or NULL.
+ * scores_opt [T, n] fp32, idx_opt [T, k] int32, w_opt [T, k] fp32,
+ *   loads_opt [n] int32: device outputs, each NULL if not wanted.
+ * 1 <= T <= max_tokens.  No allocation, no host synchronisation.
+ */
+int moe_latent_forward(qbmoe_ctx* ctx, int T, const void* x, const float* logits_in,
+                       const float* bias_in, float* bias_out, void* out,
+                       float* scores_opt, int32_t* idx_opt, float* w_opt, int32_t* loads_opt,
+                       qbmoe_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return and clear the context's device status
+ * word: QBMOE_OK, QBMOE_ETIMEOUT (a bounded wait expired; the kernel
+ * returned early and its outputs are undefined) or QBMOE_EDEVICE.
+ * ctx may be NULL (then only the stream's CUDA error state is checked).
+ */
+int qbmoe_status(qbmoe_ctx* ctx, qbmoe_stream_t stream);
+
+/*
+ * Stage timing.  When enabled, moe_latent_forward records CUDA events around
+ * each stage on its stream; qbmoe_stage_times (synchronous) writes the
+ * milliseconds of the last forward's stages into ms[0..max-1] and their names
+ * (static strings) into names, returning the number of stages.
+ */
+int qbmoe_set_timing(qbmoe_ctx* ctx, int enable);
+int qbmoe_stage_times(qbmoe_ctx* ctx, float* ms, const char** names, int max);
+
+/* Number of kernels the last moe_latent_forward / moe_route_qb call launched. */
+int qbmoe_last_launch_count(qbmoe_ctx* ctx);
+int qbmoe_route_last_launch_count(void);
+
+/* Test hook: cap on bounded device waits (iterations; <= 0 restores the
+ * default).  Applies to launches made after the call. */
+int qbmoe_set_wait_limit(qbmoe_ctx* ctx, long long iterations);
+
+const char* qbmoe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QBMOE_H */

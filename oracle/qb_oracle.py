@@ -42,12 +42,17 @@ F32 = np.float32
 # Router score
 # ---------------------------------------------------------------------------
 
-# Constants of the fp32 score recipe (see sigmoid_score).
-_LOG2E = F32(1.4426950408889634)          # 1/ln 2
-_LN2_HI = F32(0.693145751953125)          # ln 2 rounded to 15 significant bits
-_LN2_LO = F32(1.4286068203094173e-06)     # ln 2 - _LN2_HI
-_TAYLOR = [F32(1.0 / 5040.0), F32(1.0 / 720.0), F32(1.0 / 120.0), F32(1.0 / 24.0),
-           F32(1.0 / 6.0), F32(0.5), F32(1.0), F32(1.0)]
+# Constants of the fp32 score recipe (see sigmoid_score), as exact fp32 values.
+_LOG2E = F32(float.fromhex("0x1.715476p+0"))      # 1/ln 2 rounded to fp32
+_LN2_HI = F32(float.fromhex("0x1.62e4p-1"))       # ln 2 to 15 significant bits
+_LN2_LO = F32(float.fromhex("0x1.7f7d1cp-20"))    # ln 2 - _LN2_HI, rounded to fp32
+_TAYLOR = [F32(float.fromhex(h)) for h in (
+    "0x1.a01a02p-13",   # 1/5040
+    "0x1.6c16c2p-10",   # 1/720
+    "0x1.111112p-7",    # 1/120
+    "0x1.555556p-5",    # 1/24
+    "0x1.555556p-3",    # 1/6
+    "0x1p-1", "0x1p+0", "0x1p+0")]
 _CLAMP = F32(80.0)
 
 

@@ -1,0 +1,405 @@
+// C ABI of the layer: context, workspace and the forward orchestration.
+//
+// [K3-width] = "Kimi K3 模型结构（5）：宽度维度，Stable LatentMoE" (xhh.club).
+// The stages follow the pages' layer: full-width sigmoid router (Q&A on
+// routing), QB bias (Q&A on Quantile Balancing), latent down-projection
+// (延伸解读 "why a half-width latent space"), per-expert SiTU-GLU in latent
+// space (Q&A on SiTU-GLU), weighted combine + RMSNorm (Q&A on RMSNorm),
+// up-projection plus the merged full-width shared expert (Q&A on the shared
+// expert).
+#include "common.cuh"
+#include "dispatch.cuh"
+#include "gemm_tc.cuh"
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+int qbmoe_check_device_arch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QBMOE_ECUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return QBMOE_ECUDA;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return QBMOE_ECUDA;
+    return (major == 10 && minor == 3) ? QBMOE_OK : QBMOE_EARCH;
+}
+
+namespace {
+
+constexpr int kMaxStages = 16;
+
+struct Stage {
+    const char* name;
+};
+
+}  // namespace
+
+struct qbmoe_ctx {
+    qbmoe_config cfg{};
+    int max_tokens = 0;
+    int device = 0;
+    qbmoe_weights w{};
+    bool have_weights = false;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    // workspace views
+    float* scores = nullptr;
+    qbh::RouteBuffers rb{};
+    int32_t* idx = nullptr;
+    float* wts = nullptr;
+    int32_t* loads = nullptr;
+    int* offsets = nullptr;
+    int* tile_off_simt = nullptr;
+    int* tile_off_tc = nullptr;
+    int* perm = nullptr;
+    int* route_pos = nullptr;
+    void* h = nullptr;
+    void* act = nullptr;
+    void* e = nullptr;
+    void* zcat = nullptr;
+    int* status = nullptr;
+    long long wait_limit = 0;
+    // timing
+    bool timing = false;
+    cudaEvent_t ev[kMaxStages + 1] = {};
+    const char* stage_names[kMaxStages] = {};
+    int n_stages = 0;
+    int launches = 0;
+    qbh::TcPlan* tc = nullptr;
+};
+
+namespace {
+
+size_t elt(int dtype) { return dtype == QBMOE_BF16 ? 2 : 4; }
+
+size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = qbh::align_up(off + bytes, 256);
+        return base ? base + o : nullptr;
+    };
+    const int n = c.n_experts, k = c.top_k;
+    const size_t routes = (size_t)T * k;
+    const size_t a = elt(c.act_dtype);
+    char* p_scores = take((size_t)T * n * 4);
+    const size_t rbytes = qbh::route_ws_layout(T, n, k, nullptr, nullptr);
+    char* p_route = take(rbytes);
+    char* p_idx = take(routes * 4);
+    char* p_w = take(routes * 4);
+    char* p_loads = take((size_t)n * 4);
+    char* p_off = take((size_t)(n + 1) * 4);
+    char* p_toff = take((size_t)(n + 1) * 4);
+    char* p_toff2 = take((size_t)(n + 1) * 4);
+    char* p_perm = take(routes * 4);
+    char* p_rpos = take(routes * 4);
+    char* p_h = take((size_t)T * c.latent * a);
+    char* p_act = take(routes * c.expert_inter * a);
+    char* p_e = take(routes * c.latent * a);
+    char* p_z = take((size_t)T * (c.latent + c.shared_inter) * a);
+    char* p_status = take(256);
+    if (x && base) {
+        x->scores = (float*)p_scores;
+        qbh::route_ws_layout(T, n, k, &x->rb, p_route);
+        x->idx = (int32_t*)p_idx;
+        x->wts = (float*)p_w;
+        x->loads = (int32_t*)p_loads;
+        x->offsets = (int*)p_off;
+        x->tile_off_simt = (int*)p_toff;
+        x->tile_off_tc = (int*)p_toff2;
+        x->perm = (int*)p_perm;
+        x->route_pos = (int*)p_rpos;
+        x->h = p_h;
+        x->act = p_act;
+        x->e = p_e;
+        x->zcat = p_z;
+        x->status = (int*)p_status;
+    }
+    return off;
+}
+
+int validate(const qbmoe_config* c, int max_tokens) {
+    if (!c) return QBMOE_EINVAL;
+    if (c->d < 1 || c->latent < 1 || c->expert_inter < 1 || c->shared_inter < 0) return QBMOE_EINVAL;
+    if (c->n_experts < 2 || c->n_experts > QBMOE_MAX_EXPERTS) return QBMOE_EINVAL;
+    if (c->top_k < 1 || c->top_k >= c->n_experts || c->top_k > QBMOE_MAX_TOPK) return QBMOE_EINVAL;
+    if (c->qb_sweeps < 0 || max_tokens < 1) return QBMOE_EINVAL;
+    if (c->act_dtype != QBMOE_F32 && c->act_dtype != QBMOE_BF16) return QBMOE_EINVAL;
+    if (c->act_dtype == QBMOE_F32 && c->expert_wfmt != QBMOE_W_F32) return QBMOE_EINVAL;
+    if (c->act_dtype == QBMOE_BF16 && c->expert_wfmt != QBMOE_W_BF16 && c->expert_wfmt != QBMOE_W_MXFP4)
+        return QBMOE_EINVAL;
+    if (c->expert_wfmt == QBMOE_W_MXFP4 && (c->latent % 32 || c->expert_inter % 32)) return QBMOE_EINVAL;
+    if (c->latent > 32 * 256) return QBMOE_EINVAL;
+    if (!(c->situ_beta1 > 0.0f) || !(c->situ_beta2 > 0.0f) || !(c->rms_eps >= 0.0f)) return QBMOE_EINVAL;
+    // 16-byte rows of every activation matrix (vector and TMA access)
+    const int a = c->act_dtype == QBMOE_BF16 ? 8 : 4;
+    if (c->d % a || c->latent % a || c->expert_inter % a || c->shared_inter % a) return QBMOE_EINVAL;
+    if ((long long)max_tokens * c->top_k > (1LL << 30)) return QBMOE_EINVAL;
+    return QBMOE_OK;
+}
+
+struct StageClock {
+    qbmoe_ctx* c;
+    cudaStream_t s;
+    int i = 0;
+    void mark(const char* name) {
+        if (!c->timing || i >= kMaxStages) return;
+        cudaEventRecord(c->ev[i], s);
+        c->stage_names[i] = name;
+        ++i;
+    }
+    void end() {
+        if (!c->timing || i == 0 || i > kMaxStages) return;
+        cudaEventRecord(c->ev[i], s);
+        c->n_stages = i;
+    }
+};
+
+}  // namespace
+
+extern "C" size_t qbmoe_layer_workspace_bytes(const qbmoe_config* cfg, int max_tokens) {
+    if (validate(cfg, max_tokens)) return 0;
+    return layout(*cfg, max_tokens, nullptr, nullptr);
+}
+
+extern "C" int qbmoe_create(qbmoe_ctx** out, const qbmoe_config* cfg, int max_tokens) {
+    if (!out) return QBMOE_EINVAL;
+    *out = nullptr;
+    int rc = validate(cfg, max_tokens);
+    if (rc) return rc;
+    if ((rc = qbmoe_check_device_arch())) return rc;
+    qbmoe_ctx* c = new (std::nothrow) qbmoe_ctx();
+    if (!c) return QBMOE_ENOMEM;
+    c->cfg = *cfg;
+    c->max_tokens = max_tokens;
+    cudaGetDevice(&c->device);
+    c->ws_bytes = layout(*cfg, max_tokens, nullptr, nullptr);
+    if (cudaMalloc(&c->ws, c->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return QBMOE_ENOMEM;
+    }
+    layout(*cfg, max_tokens, c, static_cast<char*>(c->ws));
+    if (cudaMemset(c->status, 0, 4) != cudaSuccess) {
+        cudaFree(c->ws);
+        delete c;
+        return QBMOE_ECUDA;
+    }
+    for (int i = 0; i <= kMaxStages; ++i) cudaEventCreate(&c->ev[i]);
+    c->tc = qbh::tc_plan_create(c->cfg);
+    *out = c;
+    return QBMOE_OK;
+}
+
+extern "C" int qbmoe_destroy(qbmoe_ctx* c) {
+    if (!c) return QBMOE_OK;
+    cudaDeviceSynchronize();
+    for (int i = 0; i <= kMaxStages; ++i)
+        if (c->ev[i]) cudaEventDestroy(c->ev[i]);
+    qbh::tc_plan_destroy(c->tc);
+    cudaFree(c->ws);
+    delete c;
+    return QBMOE_OK;
+}
+
+extern "C" int qbmoe_set_weights(qbmoe_ctx* c, const qbmoe_weights* w) {
+    if (!c || !w) return QBMOE_EINVAL;
+    const qbmoe_config& g = c->cfg;
+    if (!w->w_router || !w->w_down || !w->w_gate || !w->w_up || !w->w_out || !w->rms_gamma || !w->w_proj_up)
+        return QBMOE_EINVAL;
+    if (g.shared_inter > 0 && (!w->w_shared_gate || !w->w_shared_up || !w->w_shared_out)) return QBMOE_EINVAL;
+    if (g.expert_wfmt == QBMOE_W_MXFP4 && (!w->s_gate || !w->s_up || !w->s_out)) return QBMOE_EINVAL;
+    const void* ptrs[] = {w->w_router, w->router_offset, w->w_down, w->w_gate, w->w_up, w->w_out,
+                          w->rms_gamma, w->w_proj_up, w->w_shared_gate, w->w_shared_up, w->w_shared_out};
+    for (const void* p : ptrs)
+        if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
+    c->w = *w;
+    c->have_weights = true;
+    int rc = qbh::tc_plan_set_weights(c->tc, c->cfg, *w);
+    return rc;
+}
+
+extern "C" int qbmoe_set_timing(qbmoe_ctx* c, int enable) {
+    if (!c) return QBMOE_EINVAL;
+    c->timing = enable != 0;
+    return QBMOE_OK;
+}
+
+extern "C" int qbmoe_stage_times(qbmoe_ctx* c, float* ms, const char** names, int max) {
+    if (!c || !ms) return QBMOE_EINVAL;
+    if (!c->timing || c->n_stages == 0) return 0;
+    if (cudaEventSynchronize(c->ev[c->n_stages]) != cudaSuccess) return QBMOE_ECUDA;
+    const int n = c->n_stages < max ? c->n_stages : max;
+    for (int i = 0; i < n; ++i) {
+        float t = 0.0f;
+        cudaEventElapsedTime(&t, c->ev[i], c->ev[i + 1]);
+        ms[i] = t;
+        if (names) names[i] = c->stage_names[i];
+    }
+    return n;
+}
+
+extern "C" int qbmoe_last_launch_count(qbmoe_ctx* c) { return c ? c->launches : 0; }
+
+extern "C" int qbmoe_set_wait_limit(qbmoe_ctx* c, long long iterations) {
+    if (!c) return QBMOE_EINVAL;
+    c->wait_limit = iterations > 0 ? iterations : 0;
+    return QBMOE_OK;
+}
+
+extern "C" int qbmoe_status(qbmoe_ctx* c, qbmoe_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QBMOE_ECUDA;
+    if (cudaGetLastError() != cudaSuccess) return QBMOE_ECUDA;
+    if (!c) return QBMOE_OK;
+    int v = 0;
+    if (cudaMemcpy(&v, c->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return QBMOE_ECUDA;
+    if (v != 0 && cudaMemset(c->status, 0, 4) != cudaSuccess) return QBMOE_ECUDA;
+    return v;
+}
+
+extern "C" const char* qbmoe_strerror(int code) {
+    switch (code) {
+        case QBMOE_OK: return "ok";
+        case QBMOE_EINVAL: return "invalid argument";
+        case QBMOE_ENOMEM: return "device allocation failed";
+        case QBMOE_ECUDA: return "CUDA error";
+        case QBMOE_EARCH: return "device is not sm_103 (GB300)";
+        case QBMOE_EWORKSPACE: return "workspace too small";
+        case QBMOE_ETIMEOUT: return "bounded device wait expired";
+        case QBMOE_EDEVICE: return "device-side check failed";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const float* logits_in, const float* bias_in,
+                                  float* bias_out, void* out, float* scores_opt, int32_t* idx_opt, float* w_opt,
+                                  int32_t* loads_opt, qbmoe_stream_t stream) {
+    if (!c || !c->have_weights || !x || !out) return QBMOE_EINVAL;
+    if (T < 1) return QBMOE_EINVAL;
+    if (T > c->max_tokens) return QBMOE_EWORKSPACE;
+    const void* ptrs[] = {x, logits_in, bias_in, bias_out, out, scores_opt, idx_opt, w_opt, loads_opt};
+    for (const void* p : ptrs)
+        if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device) return QBMOE_EINVAL;
+
+    const qbmoe_config& g = c->cfg;
+    const int n = g.n_experts, k = g.top_k, L = g.latent, m = g.expert_inter, ms = g.shared_inter, d = g.d;
+    const int ad = g.act_dtype;
+    const int dense_wf = ad == QBMOE_BF16 ? QBMOE_W_BF16 : QBMOE_W_F32;
+    const long long ldz = (long long)L + ms;
+    const size_t a = elt(ad);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int nl = 0, rc = 0;
+    StageClock clk{c, s};
+    const bool use_tc = qbh::tc_enabled(c->tc);
+
+    // 1. router scores
+    clk.mark("router");
+    if (logits_in) {
+        rc = qbh::launch_scores(logits_in, c->scores, (long long)T * n, s, &nl);
+    } else if (use_tc) {
+        rc = qbh::tc_router(c->tc, T, x, c->scores, s, &nl);
+    } else {
+        qbh::GemmArgs ga;
+        ga.A = x; ga.lda = d; ga.rows = T; ga.K1 = d; ga.W1 = c->w.w_router; ga.F = n;
+        ga.out = c->scores; ga.ldo = n; ga.col_bias = c->w.router_offset;
+        rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_ROUTER, ga, s, &nl);
+    }
+    if (rc) return rc;
+
+    // 2-3. QB sweeps and biased top-k
+    clk.mark("qb_topk");
+    rc = qbh::launch_qb_and_topk(T, n, k, g.qb_sweeps, c->scores, bias_in, bias_out, c->idx, c->wts,
+                                 c->rb.blk_cnt, c->rb, s, &nl);
+    if (rc) return rc;
+
+    // 4. dispatch: loads, offsets, stable permutation
+    clk.mark("dispatch");
+    const int tpw = qbh::route_tokens_per_warp(T);
+    if ((rc = qbh::launch_loads_from_counts(T, n, tpw, c->rb.blk_cnt, c->loads, s, &nl))) return rc;
+    const int tile_rows = use_tc ? qbh::tc_token_tile(c->tc, T) : qbh::kSimtBM;
+    if ((rc = qbh::launch_expert_offsets(n, c->loads, c->offsets, tile_rows, c->tile_off_simt, s, &nl))) return rc;
+    if ((rc = qbh::launch_scatter(T, n, k, tpw, c->idx, c->rb.blk_cnt, c->offsets, c->perm, c->route_pos, s, &nl)))
+        return rc;
+
+    const size_t routes = (size_t)T * k;
+    const int max_tiles = (int)((routes + tile_rows - 1) / tile_rows) + n;
+    if (use_tc) {
+        clk.mark("xside_gemm");
+        rc = qbh::tc_xside(c->tc, T, x, c->h, c->zcat, ldz, s, &nl);
+        if (rc) return rc;
+        clk.mark("expert_gate_up");
+        rc = qbh::tc_expert_gate_up(c->tc, T, c->h, c->perm, c->offsets, c->tile_off_simt, max_tiles, c->act, s, &nl);
+        if (rc) return rc;
+        clk.mark("expert_down");
+        rc = qbh::tc_expert_down(c->tc, T, c->act, c->offsets, c->tile_off_simt, max_tiles, c->e, s, &nl);
+        if (rc) return rc;
+    } else {
+        // 5. latent down-projection h = x W_down^T
+        clk.mark("down_proj");
+        {
+            qbh::GemmArgs ga;
+            ga.A = x; ga.lda = d; ga.rows = T; ga.K1 = d; ga.W1 = c->w.w_down; ga.F = L;
+            ga.out = c->h; ga.ldo = L;
+            if ((rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_STORE, ga, s, &nl))) return rc;
+        }
+        // 5b. shared expert gate/up at full width -> act_s (right half of zcat)
+        if (ms > 0) {
+            clk.mark("shared_gate_up");
+            qbh::GemmArgs ga;
+            ga.A = x; ga.lda = d; ga.rows = T; ga.K1 = d; ga.W1 = c->w.w_shared_gate; ga.Wu = c->w.w_shared_up;
+            ga.F = ms; ga.out = static_cast<char*>(c->zcat) + (size_t)L * a; ga.ldo = ldz;
+            ga.beta1 = g.situ_beta1; ga.beta2 = g.situ_beta2;
+            if ((rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_SITU, ga, s, &nl))) return rc;
+        }
+        // 6. expert gate/up with SiTU-GLU, rows gathered through perm
+        clk.mark("expert_gate_up");
+        {
+            qbh::GemmArgs ga;
+            ga.A = c->h; ga.lda = L; ga.a_rows = c->perm; ga.K1 = L; ga.W1 = c->w.w_gate; ga.S1 = c->w.s_gate;
+            ga.Wu = c->w.w_up; ga.Su = c->w.s_up; ga.F = m; ga.seg_off = c->offsets; ga.tile_off = c->tile_off_simt;
+            ga.n_groups = n; ga.max_tiles = max_tiles; ga.out = c->act; ga.ldo = m;
+            ga.beta1 = g.situ_beta1; ga.beta2 = g.situ_beta2;
+            if ((rc = qbh::launch_gemm_simt(ad, g.expert_wfmt, qbh::EPI_SITU, ga, s, &nl))) return rc;
+        }
+        // 7. expert down e = act W_o^T
+        clk.mark("expert_down");
+        {
+            qbh::GemmArgs ga;
+            ga.A = c->act; ga.lda = m; ga.K1 = m; ga.W1 = c->w.w_out; ga.S1 = c->w.s_out; ga.F = L;
+            ga.seg_off = c->offsets; ga.tile_off = c->tile_off_simt; ga.n_groups = n; ga.max_tiles = max_tiles;
+            ga.out = c->e; ga.ldo = L;
+            if ((rc = qbh::launch_gemm_simt(ad, g.expert_wfmt, qbh::EPI_STORE, ga, s, &nl))) return rc;
+        }
+    }
+    // 8. combine + RMSNorm -> z (left part of zcat)
+    clk.mark("combine_rmsnorm");
+    rc = qbh::launch_combine_rmsnorm(ad, T, k, L, c->e, c->wts, c->route_pos, c->w.rms_gamma, g.rms_eps, c->zcat,
+                                     ldz, s, &nl);
+    if (rc) return rc;
+    // 9. out = [z | act_s] [W_proj_up | W_shared_out]^T
+    clk.mark("up_proj_shared");
+    if (use_tc) {
+        rc = qbh::tc_up_shared(c->tc, T, c->zcat, ldz, out, s, &nl);
+    } else {
+        qbh::GemmArgs ga;
+        ga.A = c->zcat; ga.lda = ldz; ga.rows = T; ga.K1 = L; ga.W1 = c->w.w_proj_up; ga.K2 = ms;
+        ga.W2 = c->w.w_shared_out; ga.F = d; ga.out = out; ga.ldo = d;
+        rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_STORE, ga, s, &nl);
+    }
+    if (rc) return rc;
+    clk.end();
+    // optional outputs
+    auto cp = [&](void* dst, const void* src, size_t bytes) {
+        if (!dst) return true;
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+    };
+    if (!cp(scores_opt, c->scores, (size_t)T * n * 4) || !cp(idx_opt, c->idx, routes * 4) ||
+        !cp(w_opt, c->wts, routes * 4) || !cp(loads_opt, c->loads, (size_t)n * 4))
+        return QBMOE_ECUDA;
+    c->launches = nl;
+    return QBMOE_OK;
+}

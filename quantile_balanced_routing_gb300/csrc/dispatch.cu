@@ -1,0 +1,152 @@
+// Token dispatch (expert offsets, stable permutation) and the fused
+// combine + RMSNorm of the routed branch.
+//
+// [K3-width] = "Kimi K3 模型结构（5）：宽度维度，Stable LatentMoE" (xhh.club).
+//   Q&A on RMSNorm: RMSNorm sits after the latent aggregation of the k expert
+//   outputs and before the up-projection.
+#include "common.cuh"
+#include "dispatch.cuh"
+
+#include <algorithm>
+
+namespace {
+
+using namespace qb;
+
+// One CTA (<= 1024 threads, one per expert): offsets = exclusive scan of
+// loads; tile_off = exclusive scan of ceil(load / tile_rows).
+__global__ void __launch_bounds__(1024)
+k_expert_offsets(int n, const int32_t* __restrict__ loads, int* __restrict__ offsets,
+                 int tile_rows, int* __restrict__ tile_off) {
+    __shared__ int wsum[2][32];
+    const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
+    const int v = j < n ? loads[j] : 0;
+    const int tv = j < n ? (v + tile_rows - 1) / tile_rows : 0;
+    int a = v, b = tv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int oa = __shfl_up_sync(0xffffffffu, a, off);
+        const int ob = __shfl_up_sync(0xffffffffu, b, off);
+        if (lane >= off) { a += oa; b += ob; }
+    }
+    if (lane == 31) { wsum[0][warp] = a; wsum[1][warp] = b; }
+    __syncthreads();
+    int pa = 0, pb = 0;
+    for (int w = 0; w < warp; ++w) { pa += wsum[0][w]; pb += wsum[1][w]; }
+    a += pa;
+    b += pb;
+    if (j < n) {
+        offsets[j] = a - v;
+        tile_off[j] = b - tv;
+    }
+    if (j == n - 1) {
+        offsets[n] = a;
+        tile_off[n] = b;
+    }
+}
+
+// Stable scatter: route (t, i) of expert e goes to
+//   pos = offsets[e] + blk_base[blk][e] + #(tokens of this block before t routed to e).
+// One thread per token of the block (block = 8 * tpw <= 64 tokens).
+__global__ void k_scatter(int T, int n, int k, int tpw, const int32_t* __restrict__ idx,
+                          const int* __restrict__ blk_base, const int* __restrict__ offsets,
+                          int* __restrict__ perm, int* __restrict__ route_pos) {
+    extern __shared__ unsigned long long masks[];   // [n]
+    const int blk_tokens = 8 * tpw;
+    const int tl = threadIdx.x;
+    const int t = blockIdx.x * blk_tokens + tl;
+    for (int j = tl; j < n; j += blockDim.x) masks[j] = 0ull;
+    __syncthreads();
+    if (t < T)
+        for (int i = 0; i < k; ++i) atomicOr(&masks[idx[(size_t)t * k + i]], 1ull << tl);
+    __syncthreads();
+    if (t >= T) return;
+    const int* base = blk_base + (size_t)blockIdx.x * n;
+    const unsigned long long below = (tl == 0) ? 0ull : ((1ull << tl) - 1ull);
+    for (int i = 0; i < k; ++i) {
+        const int e = idx[(size_t)t * k + i];
+        const int pos = offsets[e] + base[e] + __popcll(masks[e] & below);
+        perm[pos] = t;
+        route_pos[(size_t)t * k + i] = pos;
+    }
+}
+
+// y = sum_i w[t,i] * e[route_pos[t,i]] (fp32); z = y / sqrt(mean(y^2) + eps) * gamma.
+template <typename TA>
+__global__ void __launch_bounds__(256)
+k_combine_rmsnorm(int T, int k, int latent, const TA* __restrict__ e, const float* __restrict__ w,
+                  const int* __restrict__ route_pos, const float* __restrict__ gamma, float eps,
+                  TA* __restrict__ z, long long ldz) {
+    constexpr int kMaxPer = 32;
+    __shared__ float red[8];
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x;
+    float y[kMaxPer];
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q) y[q] = 0.0f;
+    for (int i = 0; i < k; ++i) {
+        const float wi = w[(size_t)t * k + i];
+        const TA* row = e + (size_t)route_pos[(size_t)t * k + i] * latent;
+#pragma unroll
+        for (int q = 0; q < kMaxPer; ++q) {
+            const int c = tid + q * 256;
+            if (c < latent) y[q] = fmaf(wi, to_f32(row[c]), y[q]);
+        }
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q) {
+        const int c = tid + q * 256;
+        if (c < latent) ss = fmaf(y[q], y[q], ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int q = 0; q < 8; ++q) tot += red[q];
+    const float inv = 1.0f / sqrtf(tot / (float)latent + eps);
+    TA* zr = z + (size_t)t * ldz;
+#pragma unroll
+    for (int q = 0; q < kMaxPer; ++q) {
+        const int c = tid + q * 256;
+        if (c < latent) zr[c] = from_f32<TA>(y[q] * inv * gamma[c]);
+    }
+}
+
+}  // namespace
+
+namespace qbh {
+
+int launch_expert_offsets(int n, const int32_t* loads, int* offsets, int tile_rows, int* tile_off,
+                          cudaStream_t s, int* nl) {
+    k_expert_offsets<<<1, 1024, 0, s>>>(n, loads, offsets, tile_rows, tile_off);
+    if (nl) ++*nl;
+    return cuda_err(cudaGetLastError());
+}
+
+int launch_scatter(int T, int n, int k, int tpw, const int32_t* idx, const int* blk_base, const int* offsets,
+                   int* perm, int* route_pos, cudaStream_t s, int* nl) {
+    const int bt = 8 * tpw;
+    const int nblk = (T + bt - 1) / bt;
+    k_scatter<<<nblk, bt, (size_t)n * sizeof(unsigned long long), s>>>(T, n, k, tpw, idx, blk_base, offsets,
+                                                                        perm, route_pos);
+    if (nl) ++*nl;
+    return cuda_err(cudaGetLastError());
+}
+
+int launch_combine_rmsnorm(int act_dtype, int T, int k, int latent, const void* e, const float* w,
+                           const int* route_pos, const float* gamma, float eps, void* z, long long ldz,
+                           cudaStream_t s, int* nl) {
+    if (latent > 32 * 256) return QBMOE_EINVAL;
+    if (act_dtype == QBMOE_BF16)
+        k_combine_rmsnorm<__nv_bfloat16><<<T, 256, 0, s>>>(T, k, latent, (const __nv_bfloat16*)e, w, route_pos,
+                                                            gamma, eps, (__nv_bfloat16*)z, ldz);
+    else
+        k_combine_rmsnorm<float><<<T, 256, 0, s>>>(T, k, latent, (const float*)e, w, route_pos, gamma, eps,
+                                                    (float*)z, ldz);
+    if (nl) ++*nl;
+    return cuda_err(cudaGetLastError());
+}
+
+}  // namespace qbh

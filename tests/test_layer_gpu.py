@@ -1,0 +1,90 @@
+"""GPU parity of moe_latent_forward (through the C ABI) against the CPU oracle."""
+import numpy as np
+import pytest
+
+import qb_inputs as QI
+from layer_check import compare_fed, compare_own_router, upload_and_run
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+SMALL_BF16 = QI.LayerShape("small_bf16", T=300, d=512, latent=256, n=64, k=8, m=128, m_s=256,
+                           dtype="bf16", wfmt="bf16", offset_var=1.0)
+SMALL_MXFP4 = SMALL_BF16.with_(name="small_mxfp4", wfmt="mxfp4")
+RAGGED_F32 = QI.LayerShape("ragged_f32", T=77, d=96, latent=64, n=10, k=3, m=40, m_s=48,
+                           dtype="f32", wfmt="f32", offset_var=1.0)
+FROZEN_BF16 = SMALL_BF16.with_(name="frozen_bf16", T=129, qb_sweeps=0)
+ONE_TOKEN = SMALL_BF16.with_(name="one_token", T=1)
+
+
+@pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16, SMALL_MXFP4, FROZEN_BF16, ONE_TOKEN],
+                         ids=lambda s: s.name)
+def test_layer_fed_logits(shape):
+    compare_fed(shape)
+
+
+@pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16], ids=lambda s: s.name)
+def test_layer_own_router(shape):
+    compare_own_router(shape, min_agree=0.95)
+
+
+def test_layer_reuses_context_and_bias_chains():
+    """Two forwards in a row through one context; the second starts from the
+    first's QB bias (the caller carries it between batches)."""
+    from qb_inputs.device import layer_for, upload
+    from oracle import qb_oracle as O
+    shape = SMALL_BF16.with_(T=200)
+    inp = QI.LayerInputs(shape)
+    d = upload(inp, "cuda:0", drop_host=False)
+    lay = layer_for(shape)
+    lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
+    W = O.LayerWeights(inp)
+    logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
+    lg = torch.from_numpy(logits).cuda()
+    b = torch.zeros(shape.n, dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(2):
+        out, r = lay.forward(d["x"], logits_in=lg, bias_in=b, bias_out=b, want_routing=True)
+        outs.append((out.float().cpu().numpy(), r["idx"].cpu().numpy()))
+    assert lay.status() == 0
+    b_ref = O.moe_route_qb(logits, None, shape.k, 1)[1]
+    b_ref2 = O.moe_route_qb(logits, b_ref, shape.k, 1)[1]
+    assert np.array_equal(b.cpu().numpy().view(np.uint32), b_ref2.view(np.uint32))
+    lay.close()
+
+
+def test_layer_launch_count_and_timing():
+    from qb_inputs.device import layer_for, upload
+    shape = QI.TINY_F32
+    inp = QI.LayerInputs(shape)
+    d = upload(inp, "cuda:0", drop_host=False)
+    lay = layer_for(shape)
+    lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
+    lay.set_timing(True)
+    lay.forward(d["x"])
+    assert lay.status() == 0
+    st = lay.stage_times()
+    assert len(st) >= 5 and all(ms >= 0 for _, ms in st)
+    assert lay.last_launch_count() >= 8
+    lay.close()
+
+
+def test_forward_rejects_too_many_tokens():
+    import quantile_balanced_routing_gb300 as Q
+    from qb_inputs.device import layer_for, upload
+    shape = QI.TINY_F32
+    d = upload(QI.LayerInputs(shape), "cuda:0")
+    lay = layer_for(shape, max_tokens=32)
+    lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
+    with pytest.raises(Q.QbmoeError) as e:
+        lay.forward(d["x"])
+    assert e.value.code == Q.QBMOE_EWORKSPACE
+    lay.close()
+
+
+@pytest.mark.slow
+def test_decode_workload_sampled_tokens():
+    shape = QI.DECODE
+    rng = np.random.default_rng(0)
+    tokens = np.sort(rng.choice(shape.T, 6, replace=False))
+    compare_fed(shape, tokens=tokens)
