@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Benchmark of the Stable LatentMoE layer forward (QB routing) on GB300.
+
+One step = one moe_latent_forward over one batch of the workload (router,
+Quantile Balancing, top-k, dispatch, latent down-projection, grouped SiTU-GLU
+experts, combine + RMSNorm, up-projection + merged shared expert).  Prints one
+JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode|prefill|prefill_mxfp4]
+
+Multi-GPU (torchrun): every rank runs an independent replica on its own batch
+(the path has no data exchange on one replica); value = all ranks' tokens /
+max-over-ranks time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import qb_inputs as QI  # noqa: E402
+
+WORKLOADS = {"decode": QI.DECODE, "prefill": QI.PREFILL, "prefill_mxfp4": QI.PREFILL_MXFP4}
+METRIC = "MoE-layer fwd routed tokens/s on 1 GB300; % of HBM / tensor-core roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def weight_bytes_per_elt(shape):
+    return (0.5 + 1.0 / 32.0) if shape.wfmt == "mxfp4" else (4 if shape.wfmt == "f32" else 2)
+
+
+def stage_work(shape, T):
+    """Algorithmic (bytes, flops) per launch of each stage: what the method
+    must move and compute once, ignoring re-reads."""
+    a = 4 if shape.dtype == "f32" else 2
+    wb = weight_bytes_per_elt(shape)
+    n, k, d, L, m, ms = shape.n, shape.k, shape.d, shape.latent, shape.m, shape.m_s
+    R = T * k
+    # grouped expert work touches every expert that receives a token; with QB
+    # every expert does when T*k >= n
+    used = min(n, R)
+    w = {
+        "router": (n * d * a + T * d * a + T * n * 4, 2 * T * n * d),
+        "expert_gate_up": (used * 2 * m * L * wb + T * L * a + R * m * a, 2 * R * L * 2 * m),
+        "expert_down": (used * L * m * wb + R * m * a + R * L * a, 2 * R * m * L),
+        "xside_gemm": ((L + 2 * ms) * d * a + T * d * a + T * (L + ms) * a, 2 * T * d * (L + 2 * ms)),
+        "down_proj": (L * d * a + T * d * a + T * L * a, 2 * T * d * L),
+        "shared_gate_up": (2 * ms * d * a + T * d * a + T * ms * a, 2 * T * d * 2 * ms),
+        "combine_rmsnorm": (R * L * a + T * L * a + R * 8, 4 * R * L),
+        "up_proj_shared": (d * (L + ms) * a + T * (L + ms) * a + T * d * a, 2 * T * d * (L + ms)),
+    }
+    return w
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(shape, n_tok, seed=0):
+    """Time the oracle on: full routing of the batch + the dense layer for
+    n_tok sampled tokens.  Weight draws happen before the clock starts.
+    Returns (seconds for routing, seconds for the dense part, tokens)."""
+    from oracle import qb_oracle as O
+    inp = QI.LayerInputs(shape)
+    rng = np.random.default_rng(seed)
+    tokens = np.sort(rng.choice(shape.T, n_tok, replace=False))
+
+    class Cached(O.LayerWeights):
+        def __init__(self, inputs):
+            super().__init__(inputs)
+            self.cache = {}
+
+        def expert(self, name, e):
+            return self.cache[(name, int(e))].astype(np.float64)
+
+    W = Cached(inp)
+    for nm in ("x", "w_router", "router_offset", "w_down", "gamma", "w_proj_up", "w_shared_gate",
+               "w_shared_up", "w_shared_out"):
+        if nm in inp.specs:
+            W.dense(nm)
+    t0 = time.perf_counter()
+    logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
+    route = O.moe_route_qb(logits, None, shape.k, shape.qb_sweeps)
+    t_route = time.perf_counter() - t0
+    for e in np.unique(route[2][tokens]):
+        for nm in ("w_gate", "w_up", "w_out"):
+            W.cache[(nm, int(e))] = O.LayerWeights.expert(W, nm, e).astype(np.float32)
+    t1 = time.perf_counter()
+    O.layer_forward(inp, tokens=tokens, logits=logits, weights=W)
+    t_layer = time.perf_counter() - t1
+    # layer_forward re-runs the routing over all T tokens; count it once
+    t_dense = max(t_layer - t_route, 1e-9)
+    return t_route, t_dense, n_tok
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(shape, n_tok):
+    t_route, t_dense, S = oracle_sample(shape, n_tok)
+    est = t_route + t_dense * shape.T / S
+    return {"value": shape.T / est, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": (f"numpy oracle: router GEMM (fp64) + QB routing of all {shape.T} tokens "
+                       f"({t_route:.2f} s) and the dense layer for {S} sampled tokens ({t_dense:.2f} s), "
+                       f"scaled to {shape.T} tokens; BLAS threads = cores, elementwise numpy single-threaded")}
+
+
+# ---------------------------------------------------------------------------
+
+def run_reference(args, shape, world, rank):
+    if rank != 0:
+        return
+    n_tok = max(1, int(os.environ.get("QB_ORACLE_TOKENS", "2")))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t_route, t_dense, S = oracle_sample(shape, n_tok, seed=i)
+        if i >= args.warmup:
+            times.append(t_route + t_dense * shape.T / S)
+    sec = statistics.mean(times)
+    val = shape.T / sec
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "routed tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": config_of(shape, args),
+            "cpu_baseline": {"value": val, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": (f"each step: full routing of {shape.T} tokens + dense layer of {n_tok} "
+                                        f"sampled tokens, scaled to {shape.T} tokens")},
+            "e2e": {"value": val, "unit": "routed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(shape, args):
+    return {"workload": shape.name, "T": shape.T, "d": shape.d, "latent": shape.latent, "n_experts": shape.n,
+            "top_k": shape.k, "expert_inter": shape.m, "shared_inter": shape.m_s, "expert_weights": shape.wfmt,
+            "qb_sweeps": shape.qb_sweeps, "seed": shape.seed,
+            "l2": "inputs larger than L2 (all weights are streamed every step)",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+def run_ours(args, shape, world, rank, local):
+    import torch
+    from qb_inputs.device import layer_for, upload
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = QI.LayerInputs(shape.with_(seed=shape.seed + rank))
+    d = upload(inp, dev)
+    lay = layer_for(shape)
+    lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
+    x = d["x"]
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    lay.set_timing(max(args.steps, 1))
+    for _ in range(args.warmup):
+        lay.forward(x, out=out)
+    rc = lay.status()
+    if rc:
+        raise RuntimeError(f"device status {rc} after warm-up")
+    lay.set_timing(max(args.steps, 1))
+    launches_per_step = lay.last_launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            lay.forward(x, out=out)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end) / max(args.steps, 1)
+    rc = lay.status()
+    if rc:
+        raise RuntimeError(f"device status {rc} in the timed region")
+    stages = lay.stage_times()
+    ms_max = max_over_ranks(ms, world)
+
+    # end to end: pinned host input -> device, forward, device -> host output
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        lay.forward(x_dev, out=out)
+        out_host.copy_(out, non_blocking=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        lay.forward(x_dev, out=out)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / max(args.steps, 1), world)
+    lay.close()
+
+    if rank != 0:
+        return
+    pk, src = peaks()
+    work = stage_work(shape, shape.T)
+    dom_name, dom_ms = max(stages, key=lambda s: s[1]) if stages else ("expert_gate_up", float("nan"))
+    b, f = work.get(dom_name, (0, 0))
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if f / max(b, 1) >= ridge:
+        achieved = f / (dom_ms * 1e-3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}
+    else:
+        achieved = b / (dom_ms * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
+    roof.update({"traffic": None, "kernel": dom_name, "ms_per_launch": dom_ms,
+                 "algorithmic_bytes": b, "algorithmic_flops": f, "peak_source": src})
+    n_cpu_tok = int(os.environ.get("QB_ORACLE_TOKENS", "4"))
+    cpu = cpu_baseline(shape, n_cpu_tok) if world == 1 and not args.no_cpu else None
+    tok = shape.T * world
+    line = {
+        "metric": METRIC, "value": tok / (ms_max * 1e-3), "unit": "routed tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if shape.wfmt == "bf16" else ("bf16+mxfp4" if shape.wfmt == "mxfp4" else "f32"),
+        "data": "synthetic (seeded, random-init weights)", "config": config_of(shape, args),
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": tok / (ms_e2e * 1e-3), "unit": "routed tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size()},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "stages_ms": {nm: round(t, 4) for nm, t in stages},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    shape = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, shape, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, shape, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -198,12 +198,14 @@ int moe_latent_forward(qbmoe_ctx* ctx, int T, const void* x, const float* logits
 int qbmoe_status(qbmoe_ctx* ctx, qbmoe_stream_t stream);
 
 /*
- * Stage timing.  When enabled, moe_latent_forward records CUDA events around
- * each stage on its stream; qbmoe_stage_times (synchronous) writes the
- * milliseconds of the last forward's stages into ms[0..max-1] and their names
- * (static strings) into names, returning the number of stages.
+ * Stage timing.  qbmoe_set_timing(ctx, slots) (synchronous) keeps CUDA events
+ * around each stage of the next `slots` forwards (a ring; 0 = off, at most
+ * 4096) on the forward's stream, without synchronising.  qbmoe_stage_times
+ * (synchronous) writes each stage's mean milliseconds over the recorded
+ * forwards still in the ring into ms[0..max-1] and the stages' names (static
+ * strings) into names (may be NULL); returns the number of stages, 0 if none.
  */
-int qbmoe_set_timing(qbmoe_ctx* ctx, int enable);
+int qbmoe_set_timing(qbmoe_ctx* ctx, int slots);
 int qbmoe_stage_times(qbmoe_ctx* ctx, float* ms, const char** names, int max);
 
 /* Number of kernels the last moe_latent_forward / moe_route_qb call launched. */

@@ -194,8 +194,8 @@ class LayerInputs:
     def expert_raw(self, name, e: int):
         """Storage form of expert e's slice of an expert tensor."""
         shape, sigma, fmt = self.specs[name]
-        per = shape[1] * shape[2]
-        return self._draw(name, shape[1:], sigma, fmt, offset=e * per)
+        per = int(shape[1]) * int(shape[2])
+        return self._draw(name, shape[1:], sigma, fmt, offset=int(e) * per)
 
     def mxfp4(self, name):
         """(packed, scales) of an expert tensor quantised to MXFP4."""

@@ -229,8 +229,11 @@ class LatentMoE:
     def status(self, stream=None) -> int:
         return self.lib.qbmoe_status(self.ctx, _stream_ptr(stream))
 
-    def set_timing(self, on: bool):
-        self.lib.qbmoe_set_timing(self.ctx, int(on))
+    def set_timing(self, slots: int):
+        """Record per-stage events for the next `slots` forwards (0 = off)."""
+        rc = self.lib.qbmoe_set_timing(self.ctx, int(slots))
+        if rc:
+            raise QbmoeError(rc, "qbmoe_set_timing")
 
     def stage_times(self):
         ms = (ctypes.c_float * 16)()

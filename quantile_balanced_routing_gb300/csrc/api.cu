@@ -60,11 +60,12 @@ struct qbmoe_ctx {
     void* zcat = nullptr;
     int* status = nullptr;
     long long wait_limit = 0;
-    // timing
-    bool timing = false;
-    cudaEvent_t ev[kMaxStages + 1] = {};
+    // timing: a ring of `slots` forwards, each with kMaxStages + 1 events
+    int slots = 0;
+    std::vector<cudaEvent_t> ev;
     const char* stage_names[kMaxStages] = {};
     int n_stages = 0;
+    long long recorded = 0;
     int launches = 0;
     qbh::TcPlan* tc = nullptr;
 };
@@ -143,16 +144,18 @@ struct StageClock {
     qbmoe_ctx* c;
     cudaStream_t s;
     int i = 0;
+    cudaEvent_t* slot() { return c->ev.data() + (size_t)(c->recorded % c->slots) * (kMaxStages + 1); }
     void mark(const char* name) {
-        if (!c->timing || i >= kMaxStages) return;
-        cudaEventRecord(c->ev[i], s);
+        if (!c->slots || i >= kMaxStages) return;
+        cudaEventRecord(slot()[i], s);
         c->stage_names[i] = name;
         ++i;
     }
     void end() {
-        if (!c->timing || i == 0 || i > kMaxStages) return;
-        cudaEventRecord(c->ev[i], s);
+        if (!c->slots || i == 0) return;
+        cudaEventRecord(slot()[i], s);
         c->n_stages = i;
+        ++c->recorded;
     }
 };
 
@@ -186,7 +189,6 @@ extern "C" int qbmoe_create(qbmoe_ctx** out, const qbmoe_config* cfg, int max_to
         delete c;
         return QBMOE_ECUDA;
     }
-    for (int i = 0; i <= kMaxStages; ++i) cudaEventCreate(&c->ev[i]);
     c->tc = qbh::tc_plan_create(c->cfg);
     *out = c;
     return QBMOE_OK;
@@ -195,8 +197,7 @@ extern "C" int qbmoe_create(qbmoe_ctx** out, const qbmoe_config* cfg, int max_to
 extern "C" int qbmoe_destroy(qbmoe_ctx* c) {
     if (!c) return QBMOE_OK;
     cudaDeviceSynchronize();
-    for (int i = 0; i <= kMaxStages; ++i)
-        if (c->ev[i]) cudaEventDestroy(c->ev[i]);
+    for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
     qbh::tc_plan_destroy(c->tc);
     cudaFree(c->ws);
     delete c;
@@ -220,23 +221,36 @@ extern "C" int qbmoe_set_weights(qbmoe_ctx* c, const qbmoe_weights* w) {
     return rc;
 }
 
-extern "C" int qbmoe_set_timing(qbmoe_ctx* c, int enable) {
-    if (!c) return QBMOE_EINVAL;
-    c->timing = enable != 0;
+extern "C" int qbmoe_set_timing(qbmoe_ctx* c, int slots) {
+    if (!c || slots < 0 || slots > 4096) return QBMOE_EINVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QBMOE_ECUDA;
+    for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
+    c->ev.assign((size_t)slots * (kMaxStages + 1), nullptr);
+    for (auto& e : c->ev)
+        if (cudaEventCreate(&e) != cudaSuccess) return QBMOE_ECUDA;
+    c->slots = slots;
+    c->recorded = 0;
+    c->n_stages = 0;
     return QBMOE_OK;
 }
 
 extern "C" int qbmoe_stage_times(qbmoe_ctx* c, float* ms, const char** names, int max) {
     if (!c || !ms) return QBMOE_EINVAL;
-    if (!c->timing || c->n_stages == 0) return 0;
-    if (cudaEventSynchronize(c->ev[c->n_stages]) != cudaSuccess) return QBMOE_ECUDA;
+    if (!c->slots || c->recorded == 0) return 0;
+    const long long have = c->recorded < c->slots ? c->recorded : c->slots;
     const int n = c->n_stages < max ? c->n_stages : max;
-    for (int i = 0; i < n; ++i) {
-        float t = 0.0f;
-        cudaEventElapsedTime(&t, c->ev[i], c->ev[i + 1]);
-        ms[i] = t;
-        if (names) names[i] = c->stage_names[i];
+    for (int i = 0; i < n; ++i) ms[i] = 0.0f;
+    for (long long q = c->recorded - have; q < c->recorded; ++q) {
+        cudaEvent_t* e = c->ev.data() + (size_t)(q % c->slots) * (kMaxStages + 1);
+        if (cudaEventSynchronize(e[c->n_stages]) != cudaSuccess) return QBMOE_ECUDA;
+        for (int i = 0; i < n; ++i) {
+            float t = 0.0f;
+            if (cudaEventElapsedTime(&t, e[i], e[i + 1]) != cudaSuccess) return QBMOE_ECUDA;
+            ms[i] += t / (float)have;
+        }
     }
+    if (names)
+        for (int i = 0; i < n; ++i) names[i] = c->stage_names[i];
     return n;
 }
 

@@ -60,7 +60,7 @@ def test_layer_launch_count_and_timing():
     d = upload(inp, "cuda:0", drop_host=False)
     lay = layer_for(shape)
     lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
-    lay.set_timing(True)
+    lay.set_timing(4)
     lay.forward(d["x"])
     assert lay.status() == 0
     st = lay.stage_times()

@@ -509,3 +509,18 @@ def test_planted_mistakes_are_caught(i, monkeypatch):
     for pin in pins:
         with pytest.raises(AssertionError):
             pin()
+
+
+def test_expert_slices_match_the_whole_tensor_at_large_indices():
+    """Expert e's slice drawn alone equals rows e of the whole tensor (the
+    offset arithmetic must not overflow 32 bits for 896 experts x 3.7M)."""
+    import qb_inputs as QI
+    shape = QI.DECODE
+    inp = QI.LayerInputs(shape)
+    per = shape.m * shape.latent
+    e = np.int32(895)
+    sl = inp.expert_raw("w_gate", e)
+    first = QI.normal_bf16(shape.seed, QI.TID["w_gate"], (4,), float(np.float32(1 / np.sqrt(shape.latent))),
+                           offset=895 * per)
+    assert np.array_equal(sl.ravel()[:4], first)
+    assert 895 * per > 2 ** 31
