@@ -212,9 +212,23 @@ int qbmoe_stage_times(qbmoe_ctx* ctx, float* ms, const char** names, int max);
 int qbmoe_last_launch_count(qbmoe_ctx* ctx);
 int qbmoe_route_last_launch_count(void);
 
-/* Test hook: cap on bounded device waits (iterations; <= 0 restores the
- * default).  Applies to launches made after the call. */
+/* Test hook: cap on bounded device waits, in polls of at most 20 us each
+ * (<= 0 restores the default of 2^17).  Applies to launches made after the
+ * call. */
 int qbmoe_set_wait_limit(qbmoe_ctx* ctx, long long iterations);
+
+/* Test hook: while enabled, the tensor-core GEMM kernels withhold their first
+ * accumulator hand-off, so the epilogue's bounded wait expires and the next
+ * qbmoe_status reports QBMOE_ETIMEOUT (outputs undefined).  The kernels then
+ * drain their own copies and MMAs, free TMEM and return; the context stays
+ * usable.  No effect when the layer runs on CUDA cores. */
+int qbmoe_debug_stall(qbmoe_ctx* ctx, int enable);
+
+/* 1 when the context's bf16 GEMMs run on the tcgen05 tensor-core kernels, 0
+ * when they run on the CUDA-core kernels (fp32 layers, shapes the tensor-core
+ * tiling does not cover, or QBMOE_DISABLE_TC=1 in the environment at
+ * qbmoe_create). */
+int qbmoe_uses_tensor_cores(qbmoe_ctx* ctx);
 
 const char* qbmoe_strerror(int code);
 

@@ -87,6 +87,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qbmoe_route_last_launch_count.restype = i
     lib.qbmoe_set_wait_limit.argtypes = [vp, ctypes.c_longlong]
     lib.qbmoe_set_wait_limit.restype = i
+    lib.qbmoe_debug_stall.argtypes = [vp, i]
+    lib.qbmoe_debug_stall.restype = i
+    lib.qbmoe_uses_tensor_cores.argtypes = [vp]
+    lib.qbmoe_uses_tensor_cores.restype = i
     lib.qbmoe_strerror.argtypes = [i]
     lib.qbmoe_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -246,3 +250,10 @@ class LatentMoE:
 
     def set_wait_limit(self, iterations: int):
         return self.lib.qbmoe_set_wait_limit(self.ctx, iterations)
+
+    def debug_stall(self, on: bool):
+        return self.lib.qbmoe_debug_stall(self.ctx, int(on))
+
+    @property
+    def uses_tensor_cores(self) -> bool:
+        return bool(self.lib.qbmoe_uses_tensor_cores(self.ctx))

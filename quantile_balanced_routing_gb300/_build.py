@@ -66,7 +66,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"]
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode:
             sys.stderr.write(p.stdout + p.stderr)

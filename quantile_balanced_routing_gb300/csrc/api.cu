@@ -55,6 +55,7 @@ struct qbmoe_ctx {
     int* perm = nullptr;
     int* route_pos = nullptr;
     void* h = nullptr;
+    void* h_perm = nullptr;
     void* act = nullptr;
     void* e = nullptr;
     void* zcat = nullptr;
@@ -96,6 +97,7 @@ size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
     char* p_perm = take(routes * 4);
     char* p_rpos = take(routes * 4);
     char* p_h = take((size_t)T * c.latent * a);
+    char* p_hp = take(routes * c.latent * a);
     char* p_act = take(routes * c.expert_inter * a);
     char* p_e = take(routes * c.latent * a);
     char* p_z = take((size_t)T * (c.latent + c.shared_inter) * a);
@@ -112,6 +114,7 @@ size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
         x->perm = (int*)p_perm;
         x->route_pos = (int*)p_rpos;
         x->h = p_h;
+        x->h_perm = p_hp;
         x->act = p_act;
         x->e = p_e;
         x->zcat = p_z;
@@ -259,8 +262,17 @@ extern "C" int qbmoe_last_launch_count(qbmoe_ctx* c) { return c ? c->launches : 
 extern "C" int qbmoe_set_wait_limit(qbmoe_ctx* c, long long iterations) {
     if (!c) return QBMOE_EINVAL;
     c->wait_limit = iterations > 0 ? iterations : 0;
+    qbh::tc_set_wait_limit(c->tc, c->wait_limit);
     return QBMOE_OK;
 }
+
+extern "C" int qbmoe_debug_stall(qbmoe_ctx* c, int enable) {
+    if (!c) return QBMOE_EINVAL;
+    qbh::tc_set_stall(c->tc, enable != 0);
+    return QBMOE_OK;
+}
+
+extern "C" int qbmoe_uses_tensor_cores(qbmoe_ctx* c) { return c && qbh::tc_enabled(c->tc) ? 1 : 0; }
 
 extern "C" int qbmoe_status(qbmoe_ctx* c, qbmoe_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -310,17 +322,21 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     StageClock clk{c, s};
     const bool use_tc = qbh::tc_enabled(c->tc);
 
-    // 1. router scores
-    clk.mark("router");
-    if (logits_in) {
-        rc = qbh::launch_scores(logits_in, c->scores, (long long)T * n, s, &nl);
-    } else if (use_tc) {
-        rc = qbh::tc_router(c->tc, T, x, c->scores, s, &nl);
+    // 1. router scores (tensor-core path: fused with the other x-side GEMMs)
+    if (use_tc) {
+        clk.mark("xside_gemm");
+        if (logits_in) rc = qbh::launch_scores(logits_in, c->scores, (long long)T * n, s, &nl);
+        if (!rc) rc = qbh::tc_xside(c->tc, T, x, logits_in == nullptr, c->scores, c->h, c->zcat, ldz, c->status, s, &nl);
     } else {
-        qbh::GemmArgs ga;
-        ga.A = x; ga.lda = d; ga.rows = T; ga.K1 = d; ga.W1 = c->w.w_router; ga.F = n;
-        ga.out = c->scores; ga.ldo = n; ga.col_bias = c->w.router_offset;
-        rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_ROUTER, ga, s, &nl);
+        clk.mark("router");
+        if (logits_in) {
+            rc = qbh::launch_scores(logits_in, c->scores, (long long)T * n, s, &nl);
+        } else {
+            qbh::GemmArgs ga;
+            ga.A = x; ga.lda = d; ga.rows = T; ga.K1 = d; ga.W1 = c->w.w_router; ga.F = n;
+            ga.out = c->scores; ga.ldo = n; ga.col_bias = c->w.router_offset;
+            rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_ROUTER, ga, s, &nl);
+        }
     }
     if (rc) return rc;
 
@@ -342,14 +358,12 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     const size_t routes = (size_t)T * k;
     const int max_tiles = (int)((routes + tile_rows - 1) / tile_rows) + n;
     if (use_tc) {
-        clk.mark("xside_gemm");
-        rc = qbh::tc_xside(c->tc, T, x, c->h, c->zcat, ldz, s, &nl);
-        if (rc) return rc;
+        if ((rc = qbh::tc_gather(c->h, L, c->perm, (int)routes, c->h_perm, s, &nl))) return rc;
         clk.mark("expert_gate_up");
-        rc = qbh::tc_expert_gate_up(c->tc, T, c->h, c->perm, c->offsets, c->tile_off_simt, max_tiles, c->act, s, &nl);
+        rc = qbh::tc_expert_gate_up(c->tc, T, c->h_perm, c->offsets, c->tile_off_simt, c->act, c->status, s, &nl);
         if (rc) return rc;
         clk.mark("expert_down");
-        rc = qbh::tc_expert_down(c->tc, T, c->act, c->offsets, c->tile_off_simt, max_tiles, c->e, s, &nl);
+        rc = qbh::tc_expert_down(c->tc, T, c->act, c->offsets, c->tile_off_simt, c->e, c->status, s, &nl);
         if (rc) return rc;
     } else {
         // 5. latent down-projection h = x W_down^T
@@ -397,7 +411,7 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     // 9. out = [z | act_s] [W_proj_up | W_shared_out]^T
     clk.mark("up_proj_shared");
     if (use_tc) {
-        rc = qbh::tc_up_shared(c->tc, T, c->zcat, ldz, out, s, &nl);
+        rc = qbh::tc_up_shared(c->tc, T, c->zcat, ldz, out, c->status, s, &nl);
     } else {
         qbh::GemmArgs ga;
         ga.A = c->zcat; ga.lda = ldz; ga.rows = T; ga.K1 = L; ga.W1 = c->w.w_proj_up; ga.K2 = ms;

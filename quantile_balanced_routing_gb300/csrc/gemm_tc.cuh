@@ -14,12 +14,19 @@ bool tc_enabled(const TcPlan* p);
 // token rows per grouped tile for T tokens (the tile_off granularity)
 int tc_token_tile(const TcPlan* p, int T);
 
-int tc_router(TcPlan* p, int T, const void* x, float* scores, cudaStream_t s, int* nl);
-int tc_xside(TcPlan* p, int T, const void* x, void* h, void* zcat, long long ldz, cudaStream_t s, int* nl);
-int tc_expert_gate_up(TcPlan* p, int T, const void* h, const int* perm, const int* offsets, const int* tile_off,
-                      int max_tiles, void* act, cudaStream_t s, int* nl);
-int tc_expert_down(TcPlan* p, int T, const void* act, const int* offsets, const int* tile_off, int max_tiles,
-                   void* e, cudaStream_t s, int* nl);
-int tc_up_shared(TcPlan* p, int T, const void* zcat, long long ldz, void* out, cudaStream_t s, int* nl);
+void tc_set_wait_limit(TcPlan* p, long long iterations);
+void tc_set_stall(TcPlan* p, int on);
+
+// Router (optional) + latent down-projection + shared gate/up in one launch.
+int tc_xside(TcPlan* p, int T, const void* x, bool with_router, float* scores, void* h, void* zcat, long long ldz,
+             int* status, cudaStream_t s, int* nl);
+// dst[r] = src[rows[r]] for r < n_rows (bf16 rows of `cols` elements).
+int tc_gather(const void* src, int cols, const int* rows, int n_rows, void* dst, cudaStream_t s, int* nl);
+int tc_expert_gate_up(TcPlan* p, int T, const void* h_perm, const int* offsets, const int* tile_off, void* act,
+                      int* status, cudaStream_t s, int* nl);
+int tc_expert_down(TcPlan* p, int T, const void* act, const int* offsets, const int* tile_off, void* e,
+                   int* status, cudaStream_t s, int* nl);
+int tc_up_shared(TcPlan* p, int T, const void* zcat, long long ldz, void* out, int* status, cudaStream_t s,
+                 int* nl);
 
 }  // namespace qbh

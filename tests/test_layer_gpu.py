@@ -15,15 +15,70 @@ RAGGED_F32 = QI.LayerShape("ragged_f32", T=77, d=96, latent=64, n=10, k=3, m=40,
                            dtype="f32", wfmt="f32", offset_var=1.0)
 FROZEN_BF16 = SMALL_BF16.with_(name="frozen_bf16", T=129, qb_sweeps=0)
 ONE_TOKEN = SMALL_BF16.with_(name="one_token", T=1)
+# tensor-core tilings: ~8 tokens per expert (16-token tiles), ~525 per expert
+# (256-token tiles plus ragged tails), dense GEMMs with 256-token tiles and tails
+TC_DECODE_LIKE = SMALL_BF16.with_(name="tc_decode_like", T=64)
+TC_PREFILL_LIKE = QI.LayerShape("tc_prefill_like", T=2100, d=512, latent=256, n=32, k=8, m=128, m_s=512,
+                                dtype="bf16", wfmt="bf16", offset_var=2.0)
 
 
-@pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16, SMALL_MXFP4, FROZEN_BF16, ONE_TOKEN],
-                         ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16, SMALL_MXFP4, FROZEN_BF16, ONE_TOKEN,
+                                   TC_DECODE_LIKE, TC_PREFILL_LIKE], ids=lambda s: s.name)
 def test_layer_fed_logits(shape):
     compare_fed(shape)
 
 
-@pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16], ids=lambda s: s.name)
+def test_bf16_layers_run_on_tensor_cores(monkeypatch):
+    from qb_inputs.device import layer_for
+    lay = layer_for(SMALL_BF16)
+    assert lay.uses_tensor_cores
+    lay.close()
+    lay = layer_for(QI.TINY_F32)
+    assert not lay.uses_tensor_cores
+    lay.close()
+    monkeypatch.setenv("QBMOE_DISABLE_TC", "1")
+    lay = layer_for(SMALL_BF16)
+    assert not lay.uses_tensor_cores
+    lay.close()
+
+
+@pytest.mark.parametrize("shape", [SMALL_BF16, TC_PREFILL_LIKE], ids=lambda s: s.name)
+def test_layer_cuda_core_path_matches_oracle(shape, monkeypatch):
+    """The CUDA-core GEMMs (used for fp32 and untiled shapes) on bf16 shapes."""
+    monkeypatch.setenv("QBMOE_DISABLE_TC", "1")
+    compare_fed(shape)
+
+
+def test_bounded_wait_expires_and_context_stays_usable():
+    """A tensor-core kernel whose accumulator hand-off never arrives gives up
+    after its bounded wait, reports QBMOE_ETIMEOUT, and the context runs the
+    next forward correctly."""
+    import quantile_balanced_routing_gb300 as Q
+    from qb_inputs.device import layer_for, upload
+    from oracle import qb_oracle as O
+    from layer_check import row_rel_err, to_f64
+    shape = TC_DECODE_LIKE
+    inp = QI.LayerInputs(shape)
+    d = upload(inp, "cuda:0", drop_host=False)
+    lay = layer_for(shape)
+    assert lay.uses_tensor_cores
+    lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
+    lay.set_wait_limit(200)
+    lay.debug_stall(True)
+    lay.forward(d["x"])
+    assert lay.status() == Q.QBMOE_ETIMEOUT
+    lay.debug_stall(False)
+    lay.set_wait_limit(0)
+    W = O.LayerWeights(inp)
+    logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
+    out = lay.forward(d["x"], logits_in=torch.from_numpy(logits).cuda())
+    assert lay.status() == 0
+    ref = O.layer_forward(inp, logits=logits, weights=W)
+    assert row_rel_err(to_f64(out), ref["out"]).max() <= 2e-2
+    lay.close()
+
+
+@pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16, TC_PREFILL_LIKE], ids=lambda s: s.name)
 def test_layer_own_router(shape):
     compare_own_router(shape, min_agree=0.95)
 
