@@ -347,9 +347,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling only: scale the workload down to this many experts, keeping tokens per expert")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     shape = WORKLOADS[args.workload]
+    if args.experts:
+        shape = shape.with_(name=f"{shape.name}_scaled_n{args.experts}", n=args.experts,
+                            T=max(1, shape.T * args.experts // shape.n))
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, shape, int(os.environ.get("WORLD_SIZE", "1")), rank)
