@@ -100,6 +100,34 @@ int moe_route_qb(int T, int n, int k, int qb_sweeps,
                  void* workspace, size_t workspace_bytes, qbmoe_stream_t stream);
 
 /*
+ * moe_route_qb_noalloc — moe_route_qb for callers that cannot allocate.
+ *
+ * The pages have no counterpart: this is a deployment variant of the router
+ * above with identical results, for callers that cannot hand it a workspace
+ * because they may not allocate device memory where they route (inside a
+ * CUDA graph capture, on a serving path whose memory is planned up front, in
+ * a plug-in that only receives its inputs and outputs).  Arguments are those
+ * of moe_route_qb without the workspace.  The scratch lives in one fixed
+ * device array of qbmoe_route_noalloc_max_bytes() bytes (32 MiB) that every
+ * GPU which loads the library keeps until the process exits; sizes whose
+ * scratch (qbmoe_route_workspace_bytes(T, n, k)) exceeds it are refused with
+ * QBMOE_EWORKSPACE before anything is launched.  The call makes no cudaMalloc
+ * or cudaFree and calls no allocating library routine.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls share the one array, so calls that may overlap on the
+ * GPU (different streams, or different host threads on one device) race and
+ * must be serialised by the caller.  Nothing needs to start at zero: every
+ * scratch region is written before it is read.
+ */
+size_t qbmoe_route_noalloc_max_bytes(void);
+int moe_route_qb_noalloc(int T, int n, int k, int qb_sweeps,
+                         const float* logits, const float* bias_in, float* bias_out,
+                         float* scores, int32_t* topk_idx, float* topk_w, int32_t* loads,
+                         qbmoe_stream_t stream);
+
+/*
  * ---------------------------------------------------------------------------
  * Layer context.
  */

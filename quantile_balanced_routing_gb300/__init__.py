@@ -65,6 +65,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qbmoe_route_workspace_bytes.restype = sz
     lib.moe_route_qb.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.moe_route_qb.restype = i
+    lib.moe_route_qb_noalloc.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.moe_route_qb_noalloc.restype = i
+    lib.qbmoe_route_noalloc_max_bytes.argtypes = []
+    lib.qbmoe_route_noalloc_max_bytes.restype = sz
     lib.qbmoe_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(QbmoeConfig), i]
     lib.qbmoe_create.restype = i
     lib.qbmoe_layer_workspace_bytes.argtypes = [ctypes.POINTER(QbmoeConfig), i]
@@ -131,6 +135,12 @@ def moe_route_qb(T, n, k, qb_sweeps, logits, bias_in, bias_out, scores, topk_idx
                  workspace, workspace_bytes, stream) -> int:
     return load_library().moe_route_qb(T, n, k, qb_sweeps, logits, bias_in, bias_out, scores, topk_idx,
                                        topk_w, loads, workspace, workspace_bytes, stream)
+
+
+def moe_route_qb_noalloc(T, n, k, qb_sweeps, logits, bias_in, bias_out, scores, topk_idx, topk_w, loads,
+                         stream) -> int:
+    return load_library().moe_route_qb_noalloc(T, n, k, qb_sweeps, logits, bias_in, bias_out, scores, topk_idx,
+                                               topk_w, loads, stream)
 
 
 def moe_latent_forward(ctx, T, x, logits_in, bias_in, bias_out, out, scores, idx, w, loads, stream) -> int:
