@@ -134,7 +134,7 @@ int validate(const qbmoe_config* c, int max_tokens) {
     if (c->act_dtype == QBMOE_BF16 && c->expert_wfmt != QBMOE_W_BF16 && c->expert_wfmt != QBMOE_W_MXFP4)
         return QBMOE_EINVAL;
     if (c->expert_wfmt == QBMOE_W_MXFP4 && (c->latent % 32 || c->expert_inter % 32)) return QBMOE_EINVAL;
-    if (c->latent > 32 * 256) return QBMOE_EINVAL;
+    if (c->latent > 128 * 8 * 4) return QBMOE_EINVAL;   // combine kernel: 128 threads x 8 vectors
     if (!(c->situ_beta1 > 0.0f) || !(c->situ_beta2 > 0.0f) || !(c->rms_eps >= 0.0f)) return QBMOE_EINVAL;
     // 16-byte rows of every activation matrix (vector and TMA access)
     const int a = c->act_dtype == QBMOE_BF16 ? 8 : 4;

@@ -72,45 +72,70 @@ __global__ void k_scatter(int T, int n, int k, int tpw, const int32_t* __restric
 }
 
 // y = sum_i w[t,i] * e[route_pos[t,i]] (fp32); z = y / sqrt(mean(y^2) + eps) * gamma.
+// One CTA of 128 threads per token; 16-byte vector loads and stores.
+constexpr int kCombThreads = 128;
+constexpr int kCombMaxVec = 8;   // vectors per thread: latent <= 128 * 8 * (16 / sizeof(TA))
+
 template <typename TA>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombThreads)
 k_combine_rmsnorm(int T, int k, int latent, const TA* __restrict__ e, const float* __restrict__ w,
                   const int* __restrict__ route_pos, const float* __restrict__ gamma, float eps,
                   TA* __restrict__ z, long long ldz) {
-    constexpr int kMaxPer = 32;
-    __shared__ float red[8];
+    constexpr int V = 16 / sizeof(TA);             // elements per vector
+    __shared__ float red[kCombThreads / 32];
     const int t = blockIdx.x;
     const int tid = threadIdx.x;
-    float y[kMaxPer];
+    const int nvec = latent / V;
+    float y[kCombMaxVec][V];
 #pragma unroll
-    for (int q = 0; q < kMaxPer; ++q) y[q] = 0.0f;
+    for (int q = 0; q < kCombMaxVec; ++q)
+#pragma unroll
+        for (int u = 0; u < V; ++u) y[q][u] = 0.0f;
     for (int i = 0; i < k; ++i) {
         const float wi = w[(size_t)t * k + i];
-        const TA* row = e + (size_t)route_pos[(size_t)t * k + i] * latent;
+        const uint4* row = reinterpret_cast<const uint4*>(e + (size_t)route_pos[(size_t)t * k + i] * latent);
 #pragma unroll
-        for (int q = 0; q < kMaxPer; ++q) {
-            const int c = tid + q * 256;
-            if (c < latent) y[q] = fmaf(wi, to_f32(row[c]), y[q]);
+        for (int q = 0; q < kCombMaxVec; ++q) {
+            const int c = tid + q * kCombThreads;
+            if (c < nvec) {
+                const uint4 raw = __ldg(row + c);
+                const TA* vals = reinterpret_cast<const TA*>(&raw);
+#pragma unroll
+                for (int u = 0; u < V; ++u) y[q][u] = fmaf(wi, to_f32(vals[u]), y[q][u]);
+            }
         }
     }
     float ss = 0.0f;
 #pragma unroll
-    for (int q = 0; q < kMaxPer; ++q) {
-        const int c = tid + q * 256;
-        if (c < latent) ss = fmaf(y[q], y[q], ss);
-    }
+    for (int q = 0; q < kCombMaxVec; ++q)
+        if (tid + q * kCombThreads < nvec)
+#pragma unroll
+            for (int u = 0; u < V; ++u) ss = fmaf(y[q][u], y[q][u], ss);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     if ((tid & 31) == 0) red[tid >> 5] = ss;
     __syncthreads();
     float tot = 0.0f;
-    for (int q = 0; q < 8; ++q) tot += red[q];
-    const float inv = 1.0f / sqrtf(tot / (float)latent + eps);
-    TA* zr = z + (size_t)t * ldz;
 #pragma unroll
-    for (int q = 0; q < kMaxPer; ++q) {
-        const int c = tid + q * 256;
-        if (c < latent) zr[c] = from_f32<TA>(y[q] * inv * gamma[c]);
+    for (int q = 0; q < kCombThreads / 32; ++q) tot += red[q];
+    const float inv = 1.0f / sqrtf(tot / (float)latent + eps);
+    uint4* zr = reinterpret_cast<uint4*>(z + (size_t)t * ldz);
+    const float4* g4 = reinterpret_cast<const float4*>(gamma);
+#pragma unroll
+    for (int q = 0; q < kCombMaxVec; ++q) {
+        const int c = tid + q * kCombThreads;
+        if (c < nvec) {
+            __align__(16) TA o[V];
+#pragma unroll
+            for (int u = 0; u < V; u += 4) {
+                const float4 g = __ldg(g4 + (c * V + u) / 4);
+                o[u + 0] = from_f32<TA>(y[q][u + 0] * inv * g.x);
+                o[u + 1] = from_f32<TA>(y[q][u + 1] * inv * g.y);
+                o[u + 2] = from_f32<TA>(y[q][u + 2] * inv * g.z);
+                o[u + 3] = from_f32<TA>(y[q][u + 3] * inv * g.w);
+            }
+            zr[c] = *reinterpret_cast<const uint4*>(o);
+        }
     }
 }
 
@@ -138,13 +163,14 @@ int launch_scatter(int T, int n, int k, int tpw, const int32_t* idx, const int* 
 int launch_combine_rmsnorm(int act_dtype, int T, int k, int latent, const void* e, const float* w,
                            const int* route_pos, const float* gamma, float eps, void* z, long long ldz,
                            cudaStream_t s, int* nl) {
-    if (latent > 32 * 256) return QBMOE_EINVAL;
+    const int V = act_dtype == QBMOE_BF16 ? 8 : 4;
+    if (latent % V || latent / V > kCombThreads * kCombMaxVec || !aligned16(gamma)) return QBMOE_EINVAL;
     if (act_dtype == QBMOE_BF16)
-        k_combine_rmsnorm<__nv_bfloat16><<<T, 256, 0, s>>>(T, k, latent, (const __nv_bfloat16*)e, w, route_pos,
-                                                            gamma, eps, (__nv_bfloat16*)z, ldz);
+        k_combine_rmsnorm<__nv_bfloat16><<<T, kCombThreads, 0, s>>>(T, k, latent, (const __nv_bfloat16*)e, w,
+                                                                     route_pos, gamma, eps, (__nv_bfloat16*)z, ldz);
     else
-        k_combine_rmsnorm<float><<<T, 256, 0, s>>>(T, k, latent, (const float*)e, w, route_pos, gamma, eps,
-                                                    (float*)z, ldz);
+        k_combine_rmsnorm<float><<<T, kCombThreads, 0, s>>>(T, k, latent, (const float*)e, w, route_pos, gamma, eps,
+                                                             (float*)z, ldz);
     if (nl) ++*nl;
     return cuda_err(cudaGetLastError());
 }

@@ -42,7 +42,8 @@ namespace {
 
 using namespace qb;
 
-constexpr int kThreads = 192;
+constexpr int kProdAWarp = 0, kProdBWarp = 1, kMmaWarp = 2, kEpiFirstWarp = 3;
+constexpr int kThreads = (kEpiFirstWarp + 4) * 32;   // 224
 constexpr int kBK = 64;                        // K elements per block (128 bytes of bf16)
 constexpr int kATileBytes = 128 * kBK * 2;     // 16 KB
 constexpr int kMaxSub = 3;
@@ -66,8 +67,7 @@ struct SubGemm {
 struct TcParams {
     CUtensorMap a0[kMaxSub];
     CUtensorMap a1[kMaxSub];
-    CUtensorMap b;      // activations, box {64, BN}
-    CUtensorMap b16;    // activations, box {64, 16}
+    CUtensorMap bx[5];  // activations, boxes {64, 16 << i} rows, i = 0..4 (16..256)
     SubGemm sub[kMaxSub];
     int n_sub;
     int m_total;
@@ -87,8 +87,11 @@ struct TileInfo {
     int sub, mt, g, row0, nrows;
 };
 
+// Tile -> (sub-GEMM, m-tile, expert, token rows).  Grouped launches read the
+// expert offsets from the CTA's shared-memory copy (s_toff, s_seg).
 template <int BN>
-__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_tiles_dense, TileInfo& ti) {
+__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_tiles_dense, const int* s_toff,
+                                            const int* s_seg, TileInfo& ti) {
     int m;
     if (p.n_groups > 0) {
         const int ntg = tile / p.m_total;
@@ -96,12 +99,17 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_t
         int lo = 0, hi = p.n_groups - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(p.tile_off + mid) <= ntg) lo = mid; else hi = mid - 1;
+            if (s_toff[mid] <= ntg) lo = mid; else hi = mid - 1;
         }
         ti.g = lo;
-        const int nt = ntg - __ldg(p.tile_off + lo);
-        ti.row0 = __ldg(p.seg_off + lo) + nt * BN;
-        ti.nrows = min(BN, __ldg(p.seg_off + lo + 1) - ti.row0);
+        // The expert's rows are split into equal tiles (multiples of 16 rows),
+        // so the tiles that share a weight tile run at the same pace.
+        const int nt = ntg - s_toff[lo];
+        const int ntiles = s_toff[lo + 1] - s_toff[lo];
+        const int seg0 = s_seg[lo], seg1 = s_seg[lo + 1];
+        const int per = (((seg1 - seg0 + ntiles - 1) / ntiles) + 15) & ~15;
+        ti.row0 = seg0 + nt * per;
+        ti.nrows = min(per, seg1 - ti.row0);
     } else {
         const int G = p.raster_g;
         const int per = G * n_tiles_dense;
@@ -120,29 +128,44 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_t
     ti.mt = m - p.sub[s].m_begin;
 }
 
-template <int BN, int STAGES>
+template <int BN, int SA, int SB>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
     constexpr int kBBytes = BN * kBK * 2;
-    constexpr int kStage = kATileBytes + kBBytes;
-    constexpr uint32_t kCols = (2 * BN <= 32) ? 32 : 2 * BN;   // power of two for BN in {16, 64, 256}
+    constexpr uint32_t kCols = (2 * BN <= 32) ? 32 : (2 * BN <= 128 ? 128 : 512);   // two accumulators, power of two
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStage);
-    uint64_t* empty = full + STAGES;
-    uint64_t* accf = empty + STAGES;
+    uint8_t* a_ring = smem;                                  // SA x 16 KB weight tiles
+    uint8_t* b_ring = smem + SA * kATileBytes;               // SB x BN*128 B token tiles
+    uint64_t* fullA = reinterpret_cast<uint64_t*>(b_ring + SB * kBBytes);
+    uint64_t* emptyA = fullA + SA;
+    uint64_t* fullB = emptyA + SA;
+    uint64_t* emptyB = fullB + SB;
+    uint64_t* accf = emptyB + SB;
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* st = reinterpret_cast<float*>(tmem_slot + 4);   // [128][kStLd]
+    int* s_toff = reinterpret_cast<int*>(st + 128 * kStLd);   // [n_groups + 1] (grouped only)
+    int* s_seg = s_toff + (QBMOE_MAX_EXPERTS + 1);            // [n_groups + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long lim = p.wait_limit > 0 ? p.wait_limit : kDefaultWait;
+    if (p.n_groups > 0) {
+        for (int i = threadIdx.x; i <= p.n_groups; i += blockDim.x) {
+            s_toff[i] = __ldg(p.tile_off + i);
+            s_seg[i] = __ldg(p.seg_off + i);
+        }
+    }
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
+        for (int s = 0; s < SA; ++s) {
+            tc::mbar_init(&fullA[s], 1);
+            tc::mbar_init(&emptyA[s], 1);
+        }
+        for (int s = 0; s < SB; ++s) {
+            tc::mbar_init(&fullB[s], 1);
+            tc::mbar_init(&emptyB[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&accf[a], 1);
@@ -152,10 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::fence_proxy_async_smem();
-        tc::prefetch_tmap(&p.b);
-        tc::prefetch_tmap(&p.b16);
+        for (int i = 0; i < 5; ++i) tc::prefetch_tmap(&p.bx[i]);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(tmem_slot, kCols);
         tc::tmem_relinquish();
     }
@@ -165,68 +187,82 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     const uint32_t tbase = *tmem_slot;
 
     const int n_tiles_dense = p.n_groups > 0 ? 0 : (p.rows + BN - 1) / BN;
-    const int n_tiles = p.n_groups > 0 ? __ldg(p.tile_off + p.n_groups) * p.m_total : n_tiles_dense * p.m_total;
+    const int n_tiles = p.n_groups > 0 ? s_toff[p.n_groups] * p.m_total : n_tiles_dense * p.m_total;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == kProdAWarp || warp == kProdBWarp) {
+        // ------------------------------------------------- producers (one lane each)
+        // Warp kProdAWarp streams the weight tiles through the deep A ring,
+        // warp kProdBWarp the token tiles through the B ring, so the weight
+        // stream can run SA blocks ahead whatever the token-tile size.
+        const bool is_a = warp == kProdAWarp;
+        const int S = is_a ? SA : SB;
+        uint64_t* fullx = is_a ? fullA : fullB;
+        uint64_t* emptyx = is_a ? emptyA : emptyB;
         uint32_t issued = 0, last_par = 0;
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
                 TileInfo ti;
-                decode_tile<BN>(p, tile, n_tiles_dense, ti);
+                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
                 const SubGemm& sg = p.sub[ti.sub];
                 const int n_eff = (ti.nrows + 15) & ~15;
-                const uint32_t bytes = kATileBytes + n_eff * kBK * 2;
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait(&empty[s], ph ^ 1u, lim)) {
+                    if (!tc::mbar_wait(&emptyx[s], ph ^ 1u, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         break;
                     }
-                    uint8_t* A = smem + s * kStage;
-                    uint8_t* B = A + kATileBytes;
-                    tc::mbar_expect_tx(&full[s], bytes);
-                    if (sg.epi == SUB_SITU) {
-                        const int y = ti.g * sg.F + ti.mt * 64;
-                        tc::tma_load_2d(A, &p.a0[ti.sub], &full[s], kb * kBK, y);
-                        tc::tma_load_2d(A + kATileBytes / 2, &p.a1[ti.sub], &full[s], kb * kBK, y);
+                    if (is_a) {
+                        uint8_t* A = a_ring + s * kATileBytes;
+                        tc::mbar_expect_tx(&fullx[s], kATileBytes);
+                        if (sg.epi == SUB_SITU) {
+                            const int y = ti.g * sg.F + ti.mt * 64;
+                            tc::tma_load_2d(A, &p.a0[ti.sub], &fullx[s], kb * kBK, y);
+                            tc::tma_load_2d(A + kATileBytes / 2, &p.a1[ti.sub], &fullx[s], kb * kBK, y);
+                        } else {
+                            const int y = ti.g * sg.F + ti.mt * 128;
+                            if (kb < sg.k_split)
+                                tc::tma_load_2d(A, &p.a0[ti.sub], &fullx[s], kb * kBK, y);
+                            else
+                                tc::tma_load_2d(A, &p.a1[ti.sub], &fullx[s], (kb - sg.k_split) * kBK, y);
+                        }
                     } else {
-                        const int y = ti.g * sg.F + ti.mt * 128;
-                        if (kb < sg.k_split)
-                            tc::tma_load_2d(A, &p.a0[ti.sub], &full[s], kb * kBK, y);
-                        else
-                            tc::tma_load_2d(A, &p.a1[ti.sub], &full[s], (kb - sg.k_split) * kBK, y);
-                    }
-                    if (n_eff == BN) {
-                        tc::tma_load_2d(B, &p.b, &full[s], kb * kBK, ti.row0);
-                    } else {
-                        for (int c = 0; c < n_eff / 16; ++c)
-                            tc::tma_load_2d(B + c * 16 * kBK * 2, &p.b16, &full[s], kb * kBK, ti.row0 + c * 16);
+                        uint8_t* B = b_ring + s * kBBytes;
+                        tc::mbar_expect_tx(&fullx[s], n_eff * kBK * 2);
+                        // n_eff rows as a sum of power-of-two boxes (largest first): <= 5 TMA issues
+                        int r = 0;
+#pragma unroll
+                        for (int i = 4; i >= 0; --i) {
+                            const int h = 16 << i;
+                            if (h <= BN && (n_eff - r) >= h) {
+                                tc::tma_load_2d(B + r * kBK * 2, &p.bx[i], &fullx[s], kb * kBK, ti.row0 + r);
+                                r += h;
+                            }
+                        }
                     }
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
-                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
         }
         __syncthreads();
         // drain: every TMA this thread issued has landed before SMEM is released
         if (lane == 0 && *abort_flag) {
-            for (int s = 0; s < STAGES; ++s)
-                if ((issued >> s) & 1u) tc::mbar_wait(&full[s], (last_par >> s) & 1u, kDefaultWait);
+            for (int s = 0; s < S; ++s)
+                if ((issued >> s) & 1u) tc::mbar_wait(&fullx[s], (last_par >> s) & 1u, kDefaultWait);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
+            int sa = 0, sb = 0;
+            uint32_t pha = 0, phb = 0;
             int ab = 0;
             uint32_t aph = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
                 TileInfo ti;
-                decode_tile<BN>(p, tile, n_tiles_dense, ti);
+                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
                 const uint32_t n_eff = (ti.nrows + 15) & ~15;
                 const uint32_t idesc = tc::idesc_bf16_m128(n_eff);
                 if (!tc::mbar_wait(&acce[ab], aph ^ 1u, lim)) {
@@ -238,21 +274,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
                 const uint32_t d = tbase + ab * BN;
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait(&full[s], ph, lim)) {
+                    if (!tc::mbar_wait(&fullA[sa], pha, lim) || !tc::mbar_wait(&fullB[sb], phb, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint32_t a_addr = tc::smem_u32(smem + s * kStage);
-                    const uint32_t b_addr = a_addr + kATileBytes;
+                    const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
+                    const uint32_t b_addr = tc::smem_u32(b_ring + sb * kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         tc::tc_mma_bf16(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32), idesc,
                                         (kb | kk) != 0);
-                    tc::tc_commit(&empty[s]);
-                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                    tc::tc_commit(&emptyA[sa]);
+                    tc::tc_commit(&emptyB[sb]);
+                    if (++sa == SA) { sa = 0; pha ^= 1u; }
+                    if (++sb == SB) { sb = 0; phb ^= 1u; }
                 }
                 if (!ok) break;
                 if (!(p.stall_first_tile && tile == (int)blockIdx.x)) tc::tc_commit(&accf[ab]);
@@ -268,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;               // TMEM lane quarter of this warp
-        const int et = threadIdx.x - 64;      // 0..127
+        const int et = threadIdx.x - kEpiFirstWarp * 32;   // 0..127
         int ab = 0;
         uint32_t aph = 0;
         volatile int* ok_slot = abort_flag + 1;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
             TileInfo ti;
-            decode_tile<BN>(p, tile, n_tiles_dense, ti);
+            decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
             const SubGemm& sg = p.sub[ti.sub];
             const int n_eff = (ti.nrows + 15) & ~15;
             // one thread waits; the verdict is shared so the 128 threads stay uniform
@@ -362,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         __syncthreads();
     }
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tbase, kCols);
     }
@@ -381,13 +419,18 @@ __global__ void k_gather_rows(const uint4* __restrict__ src, int vec_per_row, co
     }
 }
 
-template <int BN>
-constexpr int stages_for() {
-    return BN == 16 ? 11 : (BN == 64 ? 8 : 4);
-}
+// Ring depths (weight tiles A, token tiles B), chosen by measurement on
+// GB300: the token ring must cover its own load latency, the weight ring the
+// DRAM latency of the streamed weights.
+template <int BN> struct Rings;
+template <> struct Rings<16> { static constexpr int SA = 11, SB = 11; };
+template <> struct Rings<64> { static constexpr int SA = 9, SB = 7; };
+template <> struct Rings<160> { static constexpr int SA = 6, SB = 5; };
+template <> struct Rings<256> { static constexpr int SA = 5, SB = 4; };
 template <int BN>
 constexpr size_t smem_for() {
-    return 1024 + (size_t)stages_for<BN>() * (kATileBytes + BN * kBK * 2) + 256 + 128 * kStLd * 4;
+    return 1024 + (size_t)Rings<BN>::SA * kATileBytes + (size_t)Rings<BN>::SB * BN * kBK * 2 + 512 + 128 * kStLd * 4 +
+           2 * (QBMOE_MAX_EXPERTS + 1) * 4;
 }
 
 }  // namespace
@@ -435,11 +478,20 @@ bool make_map(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long 
     return r == CUDA_SUCCESS;
 }
 
+// Token-tile maps with box heights 16, 32, 64, 128, 256 (those above BN unused).
+bool make_token_maps(TcPlan* P, TcParams& prm, const void* x, long long rows, long long K, long long ld, int BN) {
+    for (int i = 0; i < 5; ++i) {
+        const int h = std::min(16 << i, BN);
+        if (!make_map(P, &prm.bx[i], x, rows, K, ld, h)) return false;
+    }
+    return true;
+}
+
 template <int BN>
 int launch_bn(TcParams& prm, int grid, cudaStream_t s) {
-    constexpr int S = stages_for<BN>();
     constexpr size_t smem = smem_for<BN>();
-    auto kern = k_tc_gemm<BN, S>;
+    static_assert(smem <= 232448, "shared memory per CTA");
+    auto kern = k_tc_gemm<BN, Rings<BN>::SA, Rings<BN>::SB>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -454,6 +506,7 @@ int launch_any(int BN, TcParams& prm, int grid, cudaStream_t s) {
     switch (BN) {
         case 16: return launch_bn<16>(prm, grid, s);
         case 64: return launch_bn<64>(prm, grid, s);
+        case 160: return launch_bn<160>(prm, grid, s);
         case 256: return launch_bn<256>(prm, grid, s);
         default: return QBMOE_EINVAL;
     }
@@ -473,7 +526,7 @@ int launch_dense(TcPlan* P, TcParams& prm, int T, const void* x, long long ldx, 
                  int* nl) {
     int BN = 256;
     if ((long long)prm.m_total * ((T + 255) / 256) < 64) BN = T <= 16 ? 16 : 64;
-    if (!make_map(P, &prm.b, x, T, K, ldx, BN) || !make_map(P, &prm.b16, x, T, K, ldx, 16)) return QBMOE_ECUDA;
+    if (!make_token_maps(P, prm, x, T, K, ldx, BN)) return QBMOE_ECUDA;
     prm.rows = T;
     prm.nkb = (int)((K + kBK - 1) / kBK);
     prm.n_groups = 0;
@@ -521,8 +574,10 @@ void tc_set_stall(TcPlan* p, int on) {
 }
 
 int tc_token_tile(const TcPlan* P, int T) {
+    // Token rows per grouped tile: each expert's rows are split into equal
+    // tiles of at most this many rows (e.g. 293 -> 160 + 133).
     const long long avg = (long long)T * P->cfg.top_k / P->cfg.n_experts;
-    return avg <= 16 ? 16 : (avg <= 64 ? 64 : 256);
+    return avg <= 16 ? 16 : (avg <= 64 ? 64 : 160);
 }
 
 int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, void* h, void* zcat, long long ldz,
@@ -577,8 +632,7 @@ int tc_gather(const void* src, int cols, const int* perm, int n_rows, void* dst,
 
 static int launch_grouped(TcPlan* P, TcParams& prm, const void* act, long long routes, long long K,
                           const int* offsets, const int* tile_off, int BN, cudaStream_t s, int* nl) {
-    if (!make_map(P, &prm.b, act, routes, K, K, BN) || !make_map(P, &prm.b16, act, routes, K, K, 16))
-        return QBMOE_ECUDA;
+    if (!make_token_maps(P, prm, act, routes, K, K, BN)) return QBMOE_ECUDA;
     prm.nkb = (int)((K + kBK - 1) / kBK);
     prm.n_groups = P->cfg.n_experts;
     prm.seg_off = offsets;
