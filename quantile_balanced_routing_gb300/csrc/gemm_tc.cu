@@ -42,13 +42,18 @@ namespace {
 
 using namespace qb;
 
-constexpr int kProdAWarp = 0, kProdBWarp = 1, kMmaWarp = 2, kEpiFirstWarp = 3;
-constexpr int kThreads = (kEpiFirstWarp + 4) * 32;   // 224
+constexpr int kProdAWarp = 0, kProdBWarp = 1, kMmaWarp = 2, kEpiFirstWarp = 3, kConvFirstWarp = 7;
+constexpr int kThreads = (kEpiFirstWarp + 4) * 32;     // 224
+constexpr int kThreadsMx = (kConvFirstWarp + 4) * 32;  // 352: four MXFP4 converter warps added
 constexpr int kBK = 64;                        // K elements per block (128 bytes of bf16)
 constexpr int kATileBytes = 128 * kBK * 2;     // 16 KB
+constexpr int kPackBytes = 128 * kBK / 2;              // packed E2M1 bytes of one 128 x 64 weight block
+constexpr int kScaleGroup = 8;                         // K blocks per E8M0 scale load (16 scale bytes per row)
+constexpr int kScaleBytes = 128 * 2 * kScaleGroup;     // 2 KB
 constexpr int kMaxSub = 3;
 constexpr int kStLd = 17;                      // epilogue staging row stride (floats)
 constexpr long long kDefaultWait = 1LL << 17;  // polls (<= 20 us each) before a wait expires
+constexpr long long kDrainWait = 1LL << 12;    // polls per stage when draining after an expiry
 
 enum { SUB_STORE = 0, SUB_ROUTER = 1, SUB_SITU = 2 };
 
@@ -67,7 +72,8 @@ struct SubGemm {
 struct TcParams {
     CUtensorMap a0[kMaxSub];
     CUtensorMap a1[kMaxSub];
-    CUtensorMap bx[5];  // activations, boxes {64, 16 << i} rows, i = 0..4 (16..256)
+    CUtensorMap bx[6];  // activations, boxes {64, 8 << i} rows, i = 0..5 (8..256)
+    CUtensorMap sc0, sc1;   // MXFP4 weights: E8M0 scales of a0 / a1 (box {16, rows})
     SubGemm sub[kMaxSub];
     int n_sub;
     int m_total;
@@ -128,19 +134,99 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_t
     ti.mt = m - p.sub[s].m_begin;
 }
 
-template <int BN, int SA, int SB>
-__global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
+// Epilogue of one accumulator tile by the 128 epilogue threads: TMEM lane
+// quarter q of this warp, 16-column chunks staged through SMEM, epilogue
+// math, 16-byte global stores.  f_base is the output feature of TMEM lane 0;
+// tacc the accumulator's TMEM column base.
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo& ti, const SubGemm& sg, int f_base,
+                                              uint32_t tacc, int q, int lane, int et, float* st) {
+    const int n_eff = (ti.nrows + 15) & ~15;
+    for (int c0 = 0; c0 < n_eff; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tacc + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+        tc::named_bar_sync(1, 128);   // previous chunk's readers are done
+#pragma unroll
+        for (int j = 0; j < 16; ++j) st[(32 * q + lane) * kStLd + j] = v[j];
+        tc::named_bar_sync(1, 128);
+        const int tok_left = ti.nrows - c0;
+        if (sg.epi == SUB_STORE) {
+            // 16 tokens x 16 groups of 8 features: two items per thread
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+#pragma unroll
+            for (int it = 0; it < 2; ++it) {
+                const int item = et + 128 * it;
+                const int j = item >> 4, fg = item & 15;
+                const int f = f_base + fg * 8;
+                if (j < tok_left && f < sg.F) {
+                    __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(st[(fg * 8 + u) * kStLd + j]);
+                    *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
+                        *reinterpret_cast<const uint4*>(o);
+                }
+            }
+        } else if (sg.epi == SUB_ROUTER) {
+            // 16 tokens x 32 groups of 4 features (fp32)
+            float* out = static_cast<float*>(sg.out);
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int item = et + 128 * it;
+                const int j = item >> 5, fg = item & 31;
+                const int f = f_base + fg * 4;
+                if (j < tok_left && f < sg.F) {
+                    float4 o;
+                    float* op = &o.x;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float lg = st[(fg * 4 + u) * kStLd + j];
+                        if (sg.col_bias) lg = __fadd_rn(lg, sg.col_bias[f + u]);
+                        op[u] = score_of_logit(lg);
+                    }
+                    *reinterpret_cast<float4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) = o;
+                }
+            }
+        } else {
+            // SITU: 16 tokens x 8 groups of 8 features, gate rows 0..63, up rows 64..127
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+            const int j = et >> 3, fg = et & 7;
+            const int f = f_base + fg * 8;
+            if (j < tok_left && f < sg.F) {
+                __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float g = st[(fg * 8 + u) * kStLd + j];
+                    const float up = st[(64 + fg * 8 + u) * kStLd + j];
+                    o[u] = __float2bfloat16_rn(situ_glu(g, up, p.beta1, p.beta2));
+                }
+                *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
+                    *reinterpret_cast<const uint4*>(o);
+            }
+        }
+    }
+}
+
+template <int BN, int S, bool MX>
+__global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
     constexpr int kBBytes = BN * kBK * 2;
     constexpr uint32_t kCols = (2 * BN <= 32) ? 32 : (2 * BN <= 128 ? 128 : 512);   // two accumulators, power of two
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* a_ring = smem;                                  // SA x 16 KB weight tiles
-    uint8_t* b_ring = smem + SA * kATileBytes;               // SB x BN*128 B token tiles
-    uint64_t* fullA = reinterpret_cast<uint64_t*>(b_ring + SB * kBBytes);
-    uint64_t* emptyA = fullA + SA;
-    uint64_t* fullB = emptyA + SA;
-    uint64_t* emptyB = fullB + SB;
-    uint64_t* accf = emptyB + SB;
+    // S stages, each a 16 KB weight tile and a BN-row token tile that share
+    // one "full" barrier (both producers arrive) and one "empty" barrier (one
+    // MMA commit per stage).
+    // MXFP4 weights add: a ring of packed E2M1 blocks (S x 4 KB), two scale
+    // slots (2 x 2 KB, 8 K blocks each) and a byte -> bf16x2 table (2 KB).
+    uint8_t* a_ring = smem;
+    uint8_t* b_ring = smem + S * kATileBytes;
+    uint8_t* p_ring = b_ring + S * kBBytes;
+    uint8_t* sc_ring = p_ring + (MX ? S * kPackBytes : 0);
+    uint2* lut = reinterpret_cast<uint2*>(sc_ring + (MX ? 2 * kScaleBytes : 0));
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(lut) + (MX ? 256 * sizeof(uint2) : 0));
+    uint64_t* empty = full + S;
+    uint64_t* fullP = empty + S;                 // MX: packed block landed
+    uint64_t* fullS = fullP + (MX ? S : 0);      // MX: scale group landed
+    uint64_t* emptyS = fullS + (MX ? 2 : 0);     // MX: scale group consumed
+    uint64_t* accf = emptyS + (MX ? 2 : 0);
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -158,14 +244,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         }
     }
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < SA; ++s) {
-            tc::mbar_init(&fullA[s], 1);
-            tc::mbar_init(&emptyA[s], 1);
+    if constexpr (MX) {
+        // bf16 pair of the two E2M1 codes of byte b (low nibble first) at scale
+        // 2^0, and the bf16 exponent-field unit of each nonzero half.
+        for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+            uint32_t v = 0, nz = 0;
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t c = (b >> (4 * h)) & 15u;
+                const uint32_t ex = (c >> 1) & 3u, man = c & 1u;
+                uint32_t bits = 0;
+                if (ex) bits = ((126u + ex) << 7) | (man << 6);      // (1 + man/2) * 2^(ex-1)
+                else if (man) bits = 126u << 7;                      // 0.5
+                if (bits) {
+                    bits |= (c & 8u) << 12;
+                    nz |= 0x80u << (16 * h);
+                }
+                v |= bits << (16 * h);
+            }
+            lut[b] = make_uint2(v, nz);
         }
-        for (int s = 0; s < SB; ++s) {
-            tc::mbar_init(&fullB[s], 1);
-            tc::mbar_init(&emptyB[s], 1);
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            // token producer + weight producer (bf16) or + four converter warps (MXFP4)
+            tc::mbar_init(&full[s], MX ? 5 : 2);
+            tc::mbar_init(&empty[s], 1);   // one MMA commit per stage
+            if (MX) tc::mbar_init(&fullP[s], 1);
+        }
+        if (MX) {
+            for (int g = 0; g < 2; ++g) {
+                tc::mbar_init(&fullS[g], 1);
+                tc::mbar_init(&emptyS[g], 4);
+            }
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&accf[a], 1);
@@ -175,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::fence_proxy_async_smem();
-        for (int i = 0; i < 5; ++i) tc::prefetch_tmap(&p.bx[i]);
+        for (int i = 0; i < 6; ++i) tc::prefetch_tmap(&p.bx[i]);
     }
     if (warp == kMmaWarp) {
         tc::tmem_alloc(tmem_slot, kCols);
@@ -191,14 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
 
     if (warp == kProdAWarp || warp == kProdBWarp) {
         // ------------------------------------------------- producers (one lane each)
-        // Warp kProdAWarp streams the weight tiles through the deep A ring,
-        // warp kProdBWarp the token tiles through the B ring, so the weight
-        // stream can run SA blocks ahead whatever the token-tile size.
+        // Warp kProdAWarp loads the weight tiles, warp kProdBWarp the token
+        // tiles (up to 5 TMA issues each), in parallel into the same stage.
         const bool is_a = warp == kProdAWarp;
-        const int S = is_a ? SA : SB;
-        uint64_t* fullx = is_a ? fullA : fullB;
-        uint64_t* emptyx = is_a ? emptyA : emptyB;
+        uint64_t* fullx = (MX && is_a) ? fullP : full;
+        uint64_t* emptyx = empty;
         uint32_t issued = 0, last_par = 0;
+        uint32_t sc_issued = 0, sc_par = 0;
+        int gidx = 0;
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
@@ -213,7 +323,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
                         *abort_flag = 1;
                         break;
                     }
-                    if (is_a) {
+                    if (MX && is_a) {
+                        // packed E2M1 block (and, every kScaleGroup blocks, the scales) for the converters
+                        const bool situ = sg.epi == SUB_SITU;
+                        const int y = ti.g * sg.F + ti.mt * (situ ? 64 : 128);
+                        if (kb % kScaleGroup == 0) {
+                            const int slot = gidx & 1;
+                            if (!tc::mbar_wait(&emptyS[slot], ((gidx >> 1) & 1) ^ 1u, lim)) {
+                                set_status(p.status, QBMOE_ETIMEOUT);
+                                *abort_flag = 1;
+                                break;
+                            }
+                            uint8_t* SC = sc_ring + slot * kScaleBytes;
+                            tc::mbar_expect_tx(&fullS[slot], kScaleBytes);
+                            const int xs = (kb / kScaleGroup) * 16;
+                            if (situ) {
+                                tc::tma_load_2d(SC, &p.sc0, &fullS[slot], xs, y);
+                                tc::tma_load_2d(SC + kScaleBytes / 2, &p.sc1, &fullS[slot], xs, y);
+                            } else {
+                                tc::tma_load_2d(SC, &p.sc0, &fullS[slot], xs, y);
+                            }
+                            sc_issued |= 1u << slot;
+                            sc_par = (sc_par & ~(1u << slot)) | (((gidx >> 1) & 1u) << slot);
+                            ++gidx;
+                        }
+                        uint8_t* PK = p_ring + s * kPackBytes;
+                        tc::mbar_expect_tx(&fullP[s], kPackBytes);
+                        if (situ) {
+                            tc::tma_load_2d(PK, &p.a0[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                            tc::tma_load_2d(PK + kPackBytes / 2, &p.a1[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                        } else {
+                            tc::tma_load_2d(PK, &p.a0[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                        }
+                    } else if (is_a) {
                         uint8_t* A = a_ring + s * kATileBytes;
                         tc::mbar_expect_tx(&fullx[s], kATileBytes);
                         if (sg.epi == SUB_SITU) {
@@ -233,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
                         // n_eff rows as a sum of power-of-two boxes (largest first): <= 5 TMA issues
                         int r = 0;
 #pragma unroll
-                        for (int i = 4; i >= 0; --i) {
-                            const int h = 16 << i;
+                        for (int i = 5; i >= 1; --i) {
+                            const int h = 8 << i;
                             if (h <= BN && (n_eff - r) >= h) {
                                 tc::tma_load_2d(B + r * kBK * 2, &p.bx[i], &fullx[s], kb * kBK, ti.row0 + r);
                                 r += h;
@@ -251,13 +393,82 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
         // drain: every TMA this thread issued has landed before SMEM is released
         if (lane == 0 && *abort_flag) {
             for (int s = 0; s < S; ++s)
-                if ((issued >> s) & 1u) tc::mbar_wait(&fullx[s], (last_par >> s) & 1u, kDefaultWait);
+                if ((issued >> s) & 1u) tc::mbar_wait(&fullx[s], (last_par >> s) & 1u, kDrainWait);
+            for (int g = 0; g < 2; ++g)
+                if ((sc_issued >> g) & 1u) tc::mbar_wait(&fullS[g], (sc_par >> g) & 1u, kDrainWait);
         }
+    } else if (MX && warp >= kConvFirstWarp) {
+        // ------------------------------------------------- MXFP4 converters
+        // Thread r decodes weight row r of each 128 x 64 block: 32 packed
+        // bytes -> 64 bf16 (table value plus the E8M0 exponent), written into
+        // the stage's A tile in the 128-byte swizzled layout.
+        const int r = threadIdx.x - kConvFirstWarp * 32;
+        int s = 0, gidx = 0;
+        uint32_t ph = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                const int slot = gidx & 1;
+                int w = 1;
+                if (lane == 0) {
+                    if (kb % kScaleGroup == 0) w = tc::mbar_wait(&fullS[slot], (gidx >> 1) & 1u, lim);
+                    if (w) w = tc::mbar_wait(&fullP[s], ph, lim);
+                    if (!w) {
+                        set_status(p.status, QBMOE_ETIMEOUT);
+                        *abort_flag = 1;
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+                const uint4* src = reinterpret_cast<const uint4*>(p_ring + s * kPackBytes + r * (kBK / 2));
+                const uint4 q0 = src[0], q1 = src[1];
+                const uint8_t* scr = sc_ring + slot * kScaleBytes + r * 16 + (kb % kScaleGroup) * 2;
+                const int sc0 = scr[0], sc1 = scr[1];
+                uint8_t* dst = a_ring + s * kATileBytes + r * 128;
+                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                const bool fast = sc0 >= 2 && sc0 <= 252 && sc1 >= 2 && sc1 <= 252;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int sc = c < 4 ? sc0 : sc1;
+                    const uint32_t wd = words[c];
+                    uint32_t o[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t byte = (wd >> (8 * j)) & 0xFFu;
+                        if (fast) {
+                            const uint2 e = lut[byte];
+                            o[j] = e.x + (uint32_t)(sc - 127) * e.y;
+                        } else {
+                            // exact fallback: code value times 2^(sc-127), rounded to bf16
+                            const float m = __int_as_float(sc == 0 ? 0x00400000 : (sc << 23));
+                            uint32_t pr = 0;
+                            for (int h = 0; h < 2; ++h) {
+                                const uint32_t hb = (lut[byte].x >> (16 * h)) & 0xFFFFu;
+                                const float v = __uint_as_float(hb << 16) * m;
+                                pr |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)) << (16 * h);
+                            }
+                            o[j] = pr;
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                tc::fence_proxy_async_smem();   // generic-proxy writes -> tcgen05.mma reads
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&full[s]);
+                if (kb % kScaleGroup == kScaleGroup - 1 || kb == p.nkb - 1) {
+                    if (lane == 0) tc::mbar_arrive(&emptyS[slot]);
+                    ++gidx;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            const int stop = __shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0);
+            if (!ok || stop) break;
+        }
+        __syncthreads();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int sa = 0, sb = 0;
-            uint32_t pha = 0, phb = 0;
+            int sa = 0;
+            uint32_t pha = 0;
             int ab = 0;
             uint32_t aph = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
@@ -274,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
                 const uint32_t d = tbase + ab * BN;
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait(&fullA[sa], pha, lim) || !tc::mbar_wait(&fullB[sb], phb, lim)) {
+                    if (!tc::mbar_wait(&full[sa], pha, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         ok = false;
@@ -282,15 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
                     }
                     tc::tc_fence_after();
                     const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
-                    const uint32_t b_addr = tc::smem_u32(b_ring + sb * kBBytes);
+                    const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         tc::tc_mma_bf16(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32), idesc,
                                         (kb | kk) != 0);
-                    tc::tc_commit(&emptyA[sa]);
-                    tc::tc_commit(&emptyB[sb]);
-                    if (++sa == SA) { sa = 0; pha ^= 1u; }
-                    if (++sb == SB) { sb = 0; phb ^= 1u; }
+                    tc::tc_commit(&empty[sa]);
+                    if (++sa == S) { sa = 0; pha ^= 1u; }
                 }
                 if (!ok) break;
                 if (!(p.stall_first_tile && tile == (int)blockIdx.x)) tc::tc_commit(&accf[ab]);
@@ -329,68 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
             tc::named_bar_sync(1, 128);
             if (!ok) break;
             tc::tc_fence_after();
-            for (int c0 = 0; c0 < n_eff; c0 += 16) {
-                float v[16];
-                tc::tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + ab * BN + c0, v);
-                tc::named_bar_sync(1, 128);   // previous chunk's readers are done
-#pragma unroll
-                for (int j = 0; j < 16; ++j) st[(32 * q + lane) * kStLd + j] = v[j];
-                tc::named_bar_sync(1, 128);
-                const int tok_left = ti.nrows - c0;
-                if (sg.epi == SUB_STORE) {
-                    // 16 tokens x 16 groups of 8 features: two items per thread
-                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
-#pragma unroll
-                    for (int it = 0; it < 2; ++it) {
-                        const int item = et + 128 * it;
-                        const int j = item >> 4, fg = item & 15;
-                        const int f = ti.mt * 128 + fg * 8;
-                        if (j < tok_left && f < sg.F) {
-                            __align__(16) __nv_bfloat16 o[8];
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(st[(fg * 8 + u) * kStLd + j]);
-                            *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
-                                *reinterpret_cast<const uint4*>(o);
-                        }
-                    }
-                } else if (sg.epi == SUB_ROUTER) {
-                    // 16 tokens x 32 groups of 4 features (fp32)
-                    float* out = static_cast<float*>(sg.out);
-#pragma unroll
-                    for (int it = 0; it < 4; ++it) {
-                        const int item = et + 128 * it;
-                        const int j = item >> 5, fg = item & 31;
-                        const int f = ti.mt * 128 + fg * 4;
-                        if (j < tok_left && f < sg.F) {
-                            float4 o;
-                            float* op = &o.x;
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                float lg = st[(fg * 4 + u) * kStLd + j];
-                                if (sg.col_bias) lg = __fadd_rn(lg, sg.col_bias[f + u]);
-                                op[u] = score_of_logit(lg);
-                            }
-                            *reinterpret_cast<float4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) = o;
-                        }
-                    }
-                } else {
-                    // SITU: 16 tokens x 8 groups of 8 features, gate rows 0..63, up rows 64..127
-                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
-                    const int j = et >> 3, fg = et & 7;
-                    const int f = ti.mt * 64 + fg * 8;
-                    if (j < tok_left && f < sg.F) {
-                        __align__(16) __nv_bfloat16 o[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const float g = st[(fg * 8 + u) * kStLd + j];
-                            const float up = st[(64 + fg * 8 + u) * kStLd + j];
-                            o[u] = __float2bfloat16_rn(situ_glu(g, up, p.beta1, p.beta2));
-                        }
-                        *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
-                            *reinterpret_cast<const uint4*>(o);
-                    }
-                }
-            }
+            epilogue_tile(p, ti, sg, sg.epi == SUB_SITU ? ti.mt * 64 : ti.mt * 128, tbase + ab * BN, q, lane, et, st);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acce[ab]);
@@ -407,6 +555,231 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm(const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
+// 2-SM variant for the large (prefill-size) GEMMs: a cluster of two CTAs
+// computes a 256-row weight tile x N tokens with tcgen05.mma.cta_group::2.
+// Each CTA loads its own 128 weight rows and half of the N token rows, so
+// per SM the tile moves 16 KB + N*64 B per K block for twice the MMA work of
+// the one-CTA kernel.  The leader CTA (rank 0) issues the MMAs; both CTAs'
+// TMA loads complete on the leader's "full" barriers; the MMA commits are
+// multicast to both CTAs' "empty" and accumulator-ready barriers; each CTA's
+// epilogue drains its own TMEM lanes (weight rows) and arrives on the
+// leader's accumulator-free barrier.
+template <int BN, int S>
+__global__ void __launch_bounds__(kThreads, 1) k_tc_gemm2(const __grid_constant__ TcParams p) {
+    constexpr int kHalf = BN / 2;                            // token rows per CTA per stage
+    constexpr int kBBytes = kHalf * kBK * 2;
+    constexpr uint32_t kCols = (2 * BN <= 128) ? 128 : 512;  // two accumulators of BN columns
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* a_ring = smem;
+    uint8_t* b_ring = smem + S * kATileBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(b_ring + S * kBBytes);
+    uint64_t* empty = full + S;
+    uint64_t* accf = empty + S;
+    uint64_t* acce = accf + 2;
+    uint64_t* drain = acce + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* st = reinterpret_cast<float*>(tmem_slot + 4);
+    int* s_toff = reinterpret_cast<int*>(st + 128 * kStLd);
+    int* s_seg = s_toff + (QBMOE_MAX_EXPERTS + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_ctarank();
+    const bool leader = rank == 0;
+    const long long lim = p.wait_limit > 0 ? p.wait_limit : kDefaultWait;
+    if (p.n_groups > 0) {
+        for (int i = threadIdx.x; i <= p.n_groups; i += blockDim.x) {
+            s_toff[i] = __ldg(p.tile_off + i);
+            s_seg[i] = __ldg(p.seg_off + i);
+        }
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            tc::mbar_init(&full[s], 2);    // the leader's two producers arrive; both CTAs' copies complete on it
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&accf[a], 1);
+            tc::mbar_init(&acce[a], 8);   // 4 epilogue warps in each CTA of the pair
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        tc::fence_proxy_async_smem();
+        for (int i = 0; i < 6; ++i) tc::prefetch_tmap(&p.bx[i]);
+    }
+    if (warp == kMmaWarp) {
+        tc::tmem_alloc_pair(tmem_slot, kCols);
+        tc::tmem_relinquish_pair();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::cluster_sync();   // both CTAs' barriers are initialised before any cross-CTA signal
+    tc::tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int n_tiles_dense = p.n_groups > 0 ? 0 : (p.rows + BN - 1) / BN;
+    const int n_tiles = p.n_groups > 0 ? s_toff[p.n_groups] * p.m_total : n_tiles_dense * p.m_total;
+
+    if (warp == kProdAWarp || warp == kProdBWarp) {
+        const bool is_a = warp == kProdAWarp;
+        uint64_t* fullx = full;
+        uint64_t* emptyx = empty;
+        uint32_t issued = 0, last_par = 0;
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int tile = cl; tile < n_tiles && !*abort_flag; tile += ncl) {
+                TileInfo ti;
+                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                const SubGemm& sg = p.sub[ti.sub];
+                const int n_eff = (ti.nrows + 15) & ~15;
+                const int half = n_eff >> 1;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!tc::mbar_wait(&emptyx[s], ph ^ 1u, lim)) {
+                        set_status(p.status, QBMOE_ETIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    const uint32_t bar = tc::mapa_cluster(&fullx[s], 0);   // the leader's barrier
+                    if (is_a) {
+                        uint8_t* A = a_ring + s * kATileBytes;
+                        if (leader) tc::mbar_expect_tx(&fullx[s], 2 * kATileBytes);
+                        if (sg.epi == SUB_SITU) {
+                            const int y = ti.g * sg.F + ti.mt * 128 + (int)rank * 64;
+                            tc::tma_load_2d_pair(A, &p.a0[ti.sub], bar, kb * kBK, y);
+                            tc::tma_load_2d_pair(A + kATileBytes / 2, &p.a1[ti.sub], bar, kb * kBK, y);
+                        } else {
+                            const int y = ti.g * sg.F + ti.mt * 256 + (int)rank * 128;
+                            if (kb < sg.k_split)
+                                tc::tma_load_2d_pair(A, &p.a0[ti.sub], bar, kb * kBK, y);
+                            else
+                                tc::tma_load_2d_pair(A, &p.a1[ti.sub], bar, (kb - sg.k_split) * kBK, y);
+                        }
+                    } else {
+                        uint8_t* B = b_ring + s * kBBytes;
+                        if (leader) tc::mbar_expect_tx(&fullx[s], n_eff * kBK * 2);
+                        const int row0 = ti.row0 + (int)rank * half;
+                        int r = 0;
+#pragma unroll
+                        for (int i = 4; i >= 0; --i) {
+                            const int h = 8 << i;
+                            if (h <= kHalf && (half - r) >= h) {
+                                tc::tma_load_2d_pair(B + r * kBK * 2, &p.bx[i], bar, kb * kBK, row0 + r);
+                                r += h;
+                            }
+                        }
+                    }
+                    issued |= 1u << s;
+                    last_par = (last_par & ~(1u << s)) | (ph << s);
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+            }
+        }
+        __syncthreads();
+        if (lane == 0 && *abort_flag) {
+            if (leader) {
+                for (int s = 0; s < S; ++s)
+                    if ((issued >> s) & 1u) tc::mbar_wait(&fullx[s], (last_par >> s) & 1u, kDrainWait);
+            } else {
+                // this CTA's copies signal the leader's barriers: give them time to land
+                for (int i = 0; i < 200; ++i) __nanosleep(10000);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0 && leader) {
+            int sa = 0;
+            uint32_t pha = 0;
+            int ab = 0;
+            uint32_t aph = 0;
+            for (int tile = cl; tile < n_tiles && !*abort_flag; tile += ncl) {
+                TileInfo ti;
+                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                const uint32_t n_eff = (ti.nrows + 15) & ~15;
+                const uint32_t idesc = tc::idesc_bf16_m256(n_eff);
+                if (!tc::mbar_wait(&acce[ab], aph ^ 1u, lim)) {
+                    set_status(p.status, QBMOE_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t d = tbase + ab * BN;
+                bool ok = true;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!tc::mbar_wait(&full[sa], pha, lim)) {
+                        set_status(p.status, QBMOE_ETIMEOUT);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
+                    const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc::tc_mma_bf16_pair(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
+                                             idesc, (kb | kk) != 0);
+                    tc::tc_commit_pair(&empty[sa], 0x3);
+                    if (++sa == S) { sa = 0; pha ^= 1u; }
+                }
+                if (!ok) break;
+                tc::tc_commit_pair(&accf[ab], 0x3);
+                ab ^= 1;
+                if (ab == 0) aph ^= 1u;
+            }
+            tc::tc_commit_pair(drain, 0x1);
+            tc::mbar_wait(drain, 0, kDefaultWait);
+        }
+        __syncwarp();
+        __syncthreads();
+    } else {
+        const int q = warp & 3;
+        const int et = threadIdx.x - kEpiFirstWarp * 32;
+        int ab = 0;
+        uint32_t aph = 0;
+        volatile int* ok_slot = abort_flag + 1;
+        for (int tile = cl; tile < n_tiles; tile += ncl) {
+            TileInfo ti;
+            decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+            const SubGemm& sg = p.sub[ti.sub];
+            if (et == 0) {
+                const bool ok = tc::mbar_wait(&accf[ab], aph, lim);
+                if (!ok) {
+                    set_status(p.status, QBMOE_ETIMEOUT);
+                    *abort_flag = 1;
+                }
+                *ok_slot = ok ? 1 : 0;
+            }
+            tc::named_bar_sync(1, 128);
+            const bool ok = *ok_slot != 0;
+            tc::named_bar_sync(1, 128);
+            if (!ok) break;
+            tc::tc_fence_after();
+            const int f_base = sg.epi == SUB_SITU ? ti.mt * 128 + (int)rank * 64 : ti.mt * 256 + (int)rank * 128;
+            epilogue_tile(p, ti, sg, f_base, tbase + ab * BN, q, lane, et, st);
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) tc::mbar_arrive(&acce[ab]);
+                else tc::mbar_arrive_cluster(tc::mapa_cluster(&acce[ab], 0));
+            }
+            ab ^= 1;
+            if (ab == 0) aph ^= 1u;
+        }
+        __syncthreads();
+    }
+    __syncthreads();
+    tc::tc_fence_before();
+    tc::cluster_sync();   // the pair's MMAs and remote signals are done before TMEM and SMEM go
+    if (warp == kMmaWarp) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc_pair(tbase, kCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Row gather: dst[r] = src[rows[r]] (16-byte vectors), r < n_rows.
 __global__ void k_gather_rows(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ rows,
                               int n_rows, uint4* __restrict__ dst) {
@@ -419,18 +792,36 @@ __global__ void k_gather_rows(const uint4* __restrict__ src, int vec_per_row, co
     }
 }
 
-// Ring depths (weight tiles A, token tiles B), chosen by measurement on
-// GB300: the token ring must cover its own load latency, the weight ring the
-// DRAM latency of the streamed weights.
-template <int BN> struct Rings;
-template <> struct Rings<16> { static constexpr int SA = 11, SB = 11; };
-template <> struct Rings<64> { static constexpr int SA = 9, SB = 7; };
-template <> struct Rings<160> { static constexpr int SA = 6, SB = 5; };
-template <> struct Rings<256> { static constexpr int SA = 5, SB = 4; };
+// Pipeline depths (stages of one weight tile + one token tile), chosen by
+// measurement on GB300 within the 227 KB of shared memory per CTA.
+template <int BN> struct Stages;
+template <> struct Stages<16> { static constexpr int S = 11; };
+template <> struct Stages<64> { static constexpr int S = 8; };
+template <> struct Stages<160> { static constexpr int S = 5; };
+template <> struct Stages<256> { static constexpr int S = 4; };
+
+// 2-SM kernel: per-CTA token stages hold BN/2 rows.
+template <int BN> struct Stages2;
+template <> struct Stages2<160> { static constexpr int S = 7; };
+template <> struct Stages2<256> { static constexpr int S = 6; };
 template <int BN>
-constexpr size_t smem_for() {
-    return 1024 + (size_t)Rings<BN>::SA * kATileBytes + (size_t)Rings<BN>::SB * BN * kBK * 2 + 512 + 128 * kStLd * 4 +
+constexpr size_t smem2_for() {
+    return 1024 + (size_t)Stages2<BN>::S * (kATileBytes + (BN / 2) * kBK * 2) + 512 + 128 * kStLd * 4 +
            2 * (QBMOE_MAX_EXPERTS + 1) * 4;
+}
+
+// MXFP4 weights: each stage also holds a 4 KB packed block.
+template <int BN> struct StagesMx;
+template <> struct StagesMx<16> { static constexpr int S = 9; };
+template <> struct StagesMx<64> { static constexpr int S = 7; };
+template <> struct StagesMx<160> { static constexpr int S = 5; };
+template <> struct StagesMx<256> { static constexpr int S = 3; };
+
+template <int BN, bool MX>
+constexpr size_t smem_for() {
+    constexpr int S = MX ? StagesMx<BN>::S : Stages<BN>::S;
+    return 1024 + (size_t)S * (kATileBytes + BN * kBK * 2 + (MX ? kPackBytes : 0)) +
+           (MX ? 2 * kScaleBytes + 256 * sizeof(uint2) : 0) + 768 + 128 * kStLd * 4 + 2 * (QBMOE_MAX_EXPERTS + 1) * 4;
 }
 
 }  // namespace
@@ -445,6 +836,8 @@ struct TcPlan {
     int num_sms = 0;
     long long wait_limit = 0;
     int stall = 0;
+    bool pair_ok = false;  // 2-SM kernel enabled (QBMOE_ENABLE_2SM=1)
+    int pair_clusters[2] = {0, 0};   // co-resident clusters of the 160 / 256 variants (0 = not queried)
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
 
@@ -478,36 +871,98 @@ bool make_map(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long 
     return r == CUDA_SUCCESS;
 }
 
-// Token-tile maps with box heights 16, 32, 64, 128, 256 (those above BN unused).
+// Token-tile maps with box heights 8, 16, ..., 256 (those above BN unused).
 bool make_token_maps(TcPlan* P, TcParams& prm, const void* x, long long rows, long long K, long long ld, int BN) {
-    for (int i = 0; i < 5; ++i) {
-        const int h = std::min(16 << i, BN);
+    for (int i = 0; i < 6; ++i) {
+        const int h = std::min(8 << i, BN);
         if (!make_map(P, &prm.bx[i], x, rows, K, ld, h)) return false;
     }
     return true;
 }
 
-template <int BN>
+// 2-D uint8 tensor [rows, cols] (row stride ld bytes), box {box_x, box_rows}, no swizzle.
+bool make_map_u8(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_x,
+                 int box_rows) {
+    if (!P->encode || rows <= 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {(cuuint32_t)box_x, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = P->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool MX>
 int launch_bn(TcParams& prm, int grid, cudaStream_t s) {
-    constexpr size_t smem = smem_for<BN>();
+    constexpr size_t smem = smem_for<BN, MX>();
     static_assert(smem <= 232448, "shared memory per CTA");
-    auto kern = k_tc_gemm<BN, Rings<BN>::SA, Rings<BN>::SB>;
+    constexpr int S = MX ? StagesMx<BN>::S : Stages<BN>::S;
+    auto kern = k_tc_gemm<BN, S, MX>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
     if (attr_err != cudaSuccess) return QBMOE_ECUDA;
-    kern<<<grid, kThreads, smem, s>>>(prm);
+    kern<<<grid, MX ? kThreadsMx : kThreads, smem, s>>>(prm);
     return cuda_err(cudaGetLastError());
+}
+
+template <int BN>
+int launch_bn2(TcPlan* P, TcParams& prm, int tiles, cudaStream_t s) {
+    constexpr size_t smem = smem2_for<BN>();
+    static_assert(smem <= 232448, "shared memory per CTA");
+    auto kern = k_tc_gemm2<BN, Stages2<BN>::S>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess) return QBMOE_ECUDA;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int& maxc = P->pair_clusters[BN == 256 ? 1 : 0];
+    if (maxc == 0) {
+        cfg.gridDim = dim3(P->num_sms & ~1, 1, 1);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            return QBMOE_ECUDA;
+        }
+        maxc = n;
+    }
+    const int clusters = std::max(1, std::min(maxc, tiles));
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return QBMOE_ECUDA;
+    return cuda_err(cudaGetLastError());
+}
+
+int launch_mx(int BN, TcParams& prm, int grid, cudaStream_t s) {
+    switch (BN) {
+        case 16: return launch_bn<16, true>(prm, grid, s);
+        case 64: return launch_bn<64, true>(prm, grid, s);
+        case 160: return launch_bn<160, true>(prm, grid, s);
+        default: return QBMOE_EINVAL;
+    }
 }
 
 int launch_any(int BN, TcParams& prm, int grid, cudaStream_t s) {
     switch (BN) {
-        case 16: return launch_bn<16>(prm, grid, s);
-        case 64: return launch_bn<64>(prm, grid, s);
-        case 160: return launch_bn<160>(prm, grid, s);
-        case 256: return launch_bn<256>(prm, grid, s);
+        case 16: return launch_bn<16, false>(prm, grid, s);
+        case 64: return launch_bn<64, false>(prm, grid, s);
+        case 160: return launch_bn<160, false>(prm, grid, s);
+        case 256: return launch_bn<256, false>(prm, grid, s);
         default: return QBMOE_EINVAL;
     }
 }
@@ -521,19 +976,27 @@ void base_params(TcPlan* P, TcParams& prm, int* status) {
     prm.stall_first_tile = P->stall;
 }
 
+// Token tile of a dense launch: 256 rows unless that leaves too few tiles.
+int dense_bn(long long m_tiles_128, int T) {
+    if (m_tiles_128 * ((T + 255) / 256) < 64) return T <= 16 ? 16 : 64;
+    return 256;
+}
+
+// Whether a launch with token tile BN runs on the 2-SM kernel.
+bool use_pair(const TcPlan* P, int BN) { return P->pair_ok && (BN == 256 || BN == 160); }
+
 // Dense launch over T token rows; n_tiles x m_total tiles.
-int launch_dense(TcPlan* P, TcParams& prm, int T, const void* x, long long ldx, long long K, cudaStream_t s,
-                 int* nl) {
-    int BN = 256;
-    if ((long long)prm.m_total * ((T + 255) / 256) < 64) BN = T <= 16 ? 16 : 64;
+int launch_dense(TcPlan* P, TcParams& prm, int BN, bool pair, int T, const void* x, long long ldx, long long K,
+                 cudaStream_t s, int* nl) {
     if (!make_token_maps(P, prm, x, T, K, ldx, BN)) return QBMOE_ECUDA;
     prm.rows = T;
     prm.nkb = (int)((K + kBK - 1) / kBK);
     prm.n_groups = 0;
-    prm.raster_g = std::min(prm.m_total, 16);
+    prm.raster_g = std::min(prm.m_total, pair ? 8 : 16);
     const long long tiles = (long long)prm.m_total * ((T + BN - 1) / BN);
-    const int grid = (int)std::min<long long>(tiles, P->num_sms);
     if (nl) ++*nl;
+    if (pair) return BN == 256 ? launch_bn2<256>(P, prm, (int)std::min<long long>(tiles, 1 << 30), s) : QBMOE_EINVAL;
+    const int grid = (int)std::min<long long>(tiles, P->num_sms);
     return launch_any(BN, prm, std::max(grid, 1), s);
 }
 
@@ -546,11 +1009,18 @@ TcPlan* tc_plan_create(const qbmoe_config& cfg) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, dev);
     P->encode = get_encode();
-    const bool shapes_ok = cfg.act_dtype == QBMOE_BF16 && cfg.expert_wfmt == QBMOE_W_BF16 && cfg.d % kBK == 0 &&
+    // MXFP4 expert weights: the scale rows (K/32 bytes) must be TMA-aligned (16 B), so K % 512 == 0.
+    const bool wfmt_ok = cfg.expert_wfmt == QBMOE_W_BF16 ||
+                         (cfg.expert_wfmt == QBMOE_W_MXFP4 && cfg.latent % 512 == 0 && cfg.expert_inter % 512 == 0);
+    const bool shapes_ok = cfg.act_dtype == QBMOE_BF16 && wfmt_ok && cfg.d % kBK == 0 &&
                            cfg.latent % kBK == 0 && cfg.expert_inter % kBK == 0 && cfg.shared_inter % kBK == 0 &&
                            cfg.n_experts % 4 == 0 && cfg.latent % 128 == 0 && cfg.d % 128 == 0;
     const char* env = getenv("QBMOE_DISABLE_TC");
     P->enabled = shapes_ok && P->encode != nullptr && !(env && env[0] == '1');
+    // The 2-SM kernel is measured slower than the one-CTA kernel on GB300 at
+    // the prefill shape, so it is opt-in (QBMOE_ENABLE_2SM=1).
+    const char* env2 = getenv("QBMOE_ENABLE_2SM");
+    P->pair_ok = env2 && env2[0] == '1';
     return P;
 }
 
@@ -580,15 +1050,27 @@ int tc_token_tile(const TcPlan* P, int T) {
     return avg <= 16 ? 16 : (avg <= 64 ? 64 : 160);
 }
 
+// m-tiles of a sub-GEMM over F outputs: the one-CTA kernel covers 128 weight
+// rows per tile (64 features for SiTU, whose tile stacks gate over up rows),
+// the 2-SM kernel twice that.
+static int m_tiles_of(int F, bool situ, bool pair) {
+    const int rows = (situ ? 64 : 128) * (pair ? 2 : 1);
+    return (F + rows - 1) / rows;
+}
+
 int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, void* h, void* zcat, long long ldz,
              int* status, cudaStream_t s, int* nl) {
     const qbmoe_config& c = P->cfg;
+    const long long m128 = (with_router ? (c.n_experts + 127) / 128 : 0) + (c.latent + 127) / 128 +
+                           (c.shared_inter + 63) / 64;
+    const int BN = dense_bn(m128, T);
+    const bool pair = use_pair(P, BN);
     TcParams prm;
     base_params(P, prm, status);
     int m = 0, ns = 0;
     if (with_router) {
         SubGemm& r = prm.sub[ns];
-        r.epi = SUB_ROUTER; r.F = c.n_experts; r.m_tiles = (c.n_experts + 127) / 128; r.m_begin = m;
+        r.epi = SUB_ROUTER; r.F = c.n_experts; r.m_tiles = m_tiles_of(c.n_experts, false, pair); r.m_begin = m;
         r.k_split = 1 << 30; r.out = scores; r.ldo = c.n_experts; r.col_bias = P->w.router_offset;
         if (!make_map(P, &prm.a0[ns], P->w.w_router, c.n_experts, c.d, c.d, 128)) return QBMOE_ECUDA;
         prm.a1[ns] = prm.a0[ns];
@@ -597,7 +1079,7 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, v
     }
     {
         SubGemm& g = prm.sub[ns];
-        g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = (c.latent + 127) / 128; g.m_begin = m;
+        g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = m_tiles_of(c.latent, false, pair); g.m_begin = m;
         g.k_split = 1 << 30; g.out = h; g.ldo = c.latent;
         if (!make_map(P, &prm.a0[ns], P->w.w_down, c.latent, c.d, c.d, 128)) return QBMOE_ECUDA;
         prm.a1[ns] = prm.a0[ns];
@@ -606,7 +1088,7 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, v
     }
     if (c.shared_inter > 0) {
         SubGemm& g = prm.sub[ns];
-        g.epi = SUB_SITU; g.F = c.shared_inter; g.m_tiles = (c.shared_inter + 63) / 64; g.m_begin = m;
+        g.epi = SUB_SITU; g.F = c.shared_inter; g.m_tiles = m_tiles_of(c.shared_inter, true, pair); g.m_begin = m;
         g.k_split = 1 << 30;
         g.out = static_cast<__nv_bfloat16*>(zcat) + c.latent; g.ldo = ldz;
         if (!make_map(P, &prm.a0[ns], P->w.w_shared_gate, c.shared_inter, c.d, c.d, 64) ||
@@ -617,7 +1099,7 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, v
     }
     prm.n_sub = ns;
     prm.m_total = m;
-    return launch_dense(P, prm, T, x, c.d, c.d, s, nl);
+    return launch_dense(P, prm, BN, pair, T, x, c.d, c.d, s, nl);
 }
 
 int tc_gather(const void* src, int cols, const int* perm, int n_rows, void* dst, cudaStream_t s, int* nl) {
@@ -630,8 +1112,8 @@ int tc_gather(const void* src, int cols, const int* perm, int n_rows, void* dst,
     return cuda_err(cudaGetLastError());
 }
 
-static int launch_grouped(TcPlan* P, TcParams& prm, const void* act, long long routes, long long K,
-                          const int* offsets, const int* tile_off, int BN, cudaStream_t s, int* nl) {
+static int launch_grouped(TcPlan* P, TcParams& prm, bool pair, const void* act, long long routes, long long K,
+                          const int* offsets, const int* tile_off, int BN, cudaStream_t s, int* nl, bool mx = false) {
     if (!make_token_maps(P, prm, act, routes, K, K, BN)) return QBMOE_ECUDA;
     prm.nkb = (int)((K + kBK - 1) / kBK);
     prm.n_groups = P->cfg.n_experts;
@@ -640,6 +1122,8 @@ static int launch_grouped(TcPlan* P, TcParams& prm, const void* act, long long r
     prm.rows = 0;
     prm.raster_g = 1;
     if (nl) ++*nl;
+    if (mx) return launch_mx(BN, prm, P->num_sms, s);
+    if (pair) return BN == 160 ? launch_bn2<160>(P, prm, 1 << 30, s) : launch_bn2<256>(P, prm, 1 << 30, s);
     return launch_any(BN, prm, P->num_sms, s);
 }
 
@@ -647,45 +1131,69 @@ int tc_expert_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets, 
                       int* status, cudaStream_t s, int* nl) {
     const qbmoe_config& c = P->cfg;
     const long long routes = (long long)T * c.top_k;
+    const int BN = tc_token_tile(P, T);
+    const bool mx = c.expert_wfmt == QBMOE_W_MXFP4;
+    const bool pair = !mx && use_pair(P, BN);
     TcParams prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
     SubGemm& g = prm.sub[0];
-    g.epi = SUB_SITU; g.F = c.expert_inter; g.m_tiles = (c.expert_inter + 63) / 64; g.m_begin = 0;
+    g.epi = SUB_SITU; g.F = c.expert_inter; g.m_tiles = m_tiles_of(c.expert_inter, true, pair); g.m_begin = 0;
     g.k_split = 1 << 30; g.out = act; g.ldo = c.expert_inter;
     const long long wrows = (long long)c.n_experts * c.expert_inter;
-    if (!make_map(P, &prm.a0[0], P->w.w_gate, wrows, c.latent, c.latent, 64) ||
-        !make_map(P, &prm.a1[0], P->w.w_up, wrows, c.latent, c.latent, 64))
+    if (mx) {
+        // packed E2M1 [rows, K/2] (box 32 bytes x 64 rows) and E8M0 scales [rows, K/32] (box 16 x 64)
+        const long long K = c.latent;
+        if (!make_map_u8(P, &prm.a0[0], P->w.w_gate, wrows, K / 2, K / 2, kBK / 2, 64) ||
+            !make_map_u8(P, &prm.a1[0], P->w.w_up, wrows, K / 2, K / 2, kBK / 2, 64) ||
+            !make_map_u8(P, &prm.sc0, P->w.s_gate, wrows, K / 32, K / 32, 16, 64) ||
+            !make_map_u8(P, &prm.sc1, P->w.s_up, wrows, K / 32, K / 32, 16, 64))
+            return QBMOE_ECUDA;
+    } else if (!make_map(P, &prm.a0[0], P->w.w_gate, wrows, c.latent, c.latent, 64) ||
+               !make_map(P, &prm.a1[0], P->w.w_up, wrows, c.latent, c.latent, 64)) {
         return QBMOE_ECUDA;
+    }
     prm.m_total = g.m_tiles;
-    return launch_grouped(P, prm, h_perm, routes, c.latent, offsets, tile_off, tc_token_tile(P, T), s, nl);
+    return launch_grouped(P, prm, pair, h_perm, routes, c.latent, offsets, tile_off, BN, s, nl, mx);
 }
 
 int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const int* tile_off, void* e,
                    int* status, cudaStream_t s, int* nl) {
     const qbmoe_config& c = P->cfg;
     const long long routes = (long long)T * c.top_k;
+    const int BN = tc_token_tile(P, T);
+    const bool mx = c.expert_wfmt == QBMOE_W_MXFP4;
+    const bool pair = !mx && use_pair(P, BN);
     TcParams prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
     SubGemm& g = prm.sub[0];
-    g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = (c.latent + 127) / 128; g.m_begin = 0;
+    g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = m_tiles_of(c.latent, false, pair); g.m_begin = 0;
     g.k_split = 1 << 30; g.out = e; g.ldo = c.latent;
     const long long wrows = (long long)c.n_experts * c.latent;
-    if (!make_map(P, &prm.a0[0], P->w.w_out, wrows, c.expert_inter, c.expert_inter, 128)) return QBMOE_ECUDA;
+    if (mx) {
+        const long long K = c.expert_inter;
+        if (!make_map_u8(P, &prm.a0[0], P->w.w_out, wrows, K / 2, K / 2, kBK / 2, 128) ||
+            !make_map_u8(P, &prm.sc0, P->w.s_out, wrows, K / 32, K / 32, 16, 128))
+            return QBMOE_ECUDA;
+    } else if (!make_map(P, &prm.a0[0], P->w.w_out, wrows, c.expert_inter, c.expert_inter, 128)) {
+        return QBMOE_ECUDA;
+    }
     prm.a1[0] = prm.a0[0];
     prm.m_total = g.m_tiles;
-    return launch_grouped(P, prm, act, routes, c.expert_inter, offsets, tile_off, tc_token_tile(P, T), s, nl);
+    return launch_grouped(P, prm, pair, act, routes, c.expert_inter, offsets, tile_off, BN, s, nl, mx);
 }
 
 int tc_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, int* status, cudaStream_t s,
                  int* nl) {
     const qbmoe_config& c = P->cfg;
+    const int BN = dense_bn((c.d + 127) / 128, T);
+    const bool pair = use_pair(P, BN);
     TcParams prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
     SubGemm& g = prm.sub[0];
-    g.epi = SUB_STORE; g.F = c.d; g.m_tiles = (c.d + 127) / 128; g.m_begin = 0;
+    g.epi = SUB_STORE; g.F = c.d; g.m_tiles = m_tiles_of(c.d, false, pair); g.m_begin = 0;
     g.k_split = c.latent / kBK; g.out = out; g.ldo = c.d;
     if (!make_map(P, &prm.a0[0], P->w.w_proj_up, c.d, c.latent, c.latent, 128)) return QBMOE_ECUDA;
     if (c.shared_inter > 0) {
@@ -695,7 +1203,7 @@ int tc_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, i
         prm.a1[0] = prm.a0[0];
     }
     prm.m_total = g.m_tiles;
-    return launch_dense(P, prm, T, zcat, ldz, (long long)c.latent + c.shared_inter, s, nl);
+    return launch_dense(P, prm, BN, pair, T, zcat, ldz, (long long)c.latent + c.shared_inter, s, nl);
 }
 
 }  // namespace qbh

@@ -20,12 +20,29 @@ ONE_TOKEN = SMALL_BF16.with_(name="one_token", T=1)
 TC_DECODE_LIKE = SMALL_BF16.with_(name="tc_decode_like", T=64)
 TC_PREFILL_LIKE = QI.LayerShape("tc_prefill_like", T=2100, d=512, latent=256, n=32, k=8, m=128, m_s=512,
                                 dtype="bf16", wfmt="bf16", offset_var=2.0)
+# MXFP4 expert weights on the tensor-core path (K multiples of 512 for the
+# scale loads): 64-, 16- and 160-row token tiles
+TC_MXFP4 = QI.LayerShape("tc_mxfp4", T=300, d=1024, latent=512, n=64, k=8, m=512, m_s=512,
+                         dtype="bf16", wfmt="mxfp4", offset_var=1.0)
+TC_MXFP4_DECODE_LIKE = TC_MXFP4.with_(name="tc_mxfp4_decode_like", T=64)
+TC_MXFP4_PREFILL_LIKE = TC_MXFP4.with_(name="tc_mxfp4_prefill_like", T=1200, n=32, offset_var=2.0)
 
 
 @pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16, SMALL_MXFP4, FROZEN_BF16, ONE_TOKEN,
-                                   TC_DECODE_LIKE, TC_PREFILL_LIKE], ids=lambda s: s.name)
+                                   TC_DECODE_LIKE, TC_PREFILL_LIKE, TC_MXFP4, TC_MXFP4_DECODE_LIKE,
+                                   TC_MXFP4_PREFILL_LIKE], ids=lambda s: s.name)
 def test_layer_fed_logits(shape):
     compare_fed(shape)
+
+
+def test_mxfp4_layers_run_on_tensor_cores():
+    from qb_inputs.device import layer_for
+    lay = layer_for(TC_MXFP4)
+    assert lay.uses_tensor_cores
+    lay.close()
+    lay = layer_for(SMALL_MXFP4)      # latent 256: scale rows too short for the scale loads
+    assert not lay.uses_tensor_cores
+    lay.close()
 
 
 def test_bf16_layers_run_on_tensor_cores(monkeypatch):
@@ -47,6 +64,13 @@ def test_layer_cuda_core_path_matches_oracle(shape, monkeypatch):
     """The CUDA-core GEMMs (used for fp32 and untiled shapes) on bf16 shapes."""
     monkeypatch.setenv("QBMOE_DISABLE_TC", "1")
     compare_fed(shape)
+
+
+def test_two_sm_kernel_on_prefill_tiles_matches_oracle(monkeypatch):
+    """The prefill-size GEMMs on the opt-in 2-SM (cta_group::2) kernel: 256-row
+    weight tiles across a CTA pair, 160- and 256-row token tiles."""
+    monkeypatch.setenv("QBMOE_ENABLE_2SM", "1")
+    compare_fed(TC_PREFILL_LIKE)
 
 
 def test_bounded_wait_expires_and_context_stays_usable():
