@@ -31,7 +31,8 @@ import numpy as np  # noqa: E402
 
 import qb_inputs as QI  # noqa: E402
 
-WORKLOADS = {"decode": QI.DECODE, "prefill": QI.PREFILL, "prefill_mxfp4": QI.PREFILL_MXFP4}
+WORKLOADS = {"decode": QI.DECODE, "prefill": QI.PREFILL, "prefill_mxfp4": QI.PREFILL_MXFP4,
+             "decode_mxfp4": QI.DECODE_MXFP4}
 METRIC = "MoE-layer fwd routed tokens/s on 1 GB300; % of HBM / tensor-core roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -43,6 +44,38 @@ def peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "tc_ptx.cuh"):
+        with open(os.path.join(ROOT, "quantile_balanced_routing_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, workload):
+    """Per-launch DRAM bytes of `kernel` on `workload` from an ncu summary under
+    profiles/, if it was taken with the current kernel source; else None."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = kernel_source_sha256()
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        kv = {}
+        with open(os.path.join(pdir, name)) as f:
+            for line in f:
+                if ":" in line and line.split(":", 1)[0].strip() in (
+                        "traffic_bytes_full_launch", "kernel", "workload", "kernel_source_sha256"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if (kv.get("kernel") == kernel and kv.get("workload") == workload
+                and kv.get("kernel_source_sha256") == sha and "traffic_bytes_full_launch" in kv):
+            return int(kv["traffic_bytes_full_launch"])
+    return None
 
 
 def weight_bytes_per_elt(shape):
@@ -87,7 +120,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -317,7 +350,7 @@ def run_ours(args, shape, world, rank, local):
         achieved = b / (dom_ms * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
-    roof.update({"traffic": None, "kernel": dom_name, "ms_per_launch": dom_ms,
+    roof.update({"traffic": recorded_traffic(dom_name, shape.name), "kernel": dom_name, "ms_per_launch": dom_ms,
                  "algorithmic_bytes": b, "algorithmic_flops": f, "peak_source": src})
     n_cpu_tok = int(os.environ.get("QB_ORACLE_TOKENS", "4"))
     cpu = cpu_baseline(shape, n_cpu_tok) if world == 1 and not args.no_cpu else None
@@ -342,7 +375,7 @@ def run_ours(args, shape, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))

@@ -127,8 +127,10 @@ DECODE = LayerShape("k3_decode_T256", T=256, d=7168, latent=3584, n=896, k=16, m
 PREFILL = LayerShape("k3_prefill_T16384", T=16384, d=7168, latent=3584, n=896, k=16, m=1024,
                      m_s=6144, dtype="bf16", wfmt="bf16", offset_var=2.0)
 PREFILL_MXFP4 = PREFILL.with_(name="k3_prefill_mxfp4_T16384", wfmt="mxfp4")
+# The decode shape with the deployment weight format (routed experts MXFP4).
+DECODE_MXFP4 = DECODE.with_(name="k3_decode_mxfp4_T256", wfmt="mxfp4")
 
-WORKLOADS = {w.name: w for w in (TINY_F32, ROUTE_QB, DECODE, PREFILL, PREFILL_MXFP4)}
+WORKLOADS = {w.name: w for w in (TINY_F32, ROUTE_QB, DECODE, PREFILL, PREFILL_MXFP4, DECODE_MXFP4)}
 
 
 def _sig(fan_in: int) -> float:

@@ -44,7 +44,8 @@ using namespace qb;
 
 constexpr int kProdAWarp = 0, kProdBWarp = 1, kMmaWarp = 2, kEpiFirstWarp = 3, kConvFirstWarp = 7;
 constexpr int kThreads = (kEpiFirstWarp + 4) * 32;     // 224
-constexpr int kThreadsMx = (kConvFirstWarp + 4) * 32;  // 352: four MXFP4 converter warps added
+constexpr int kConvWarps = 8;                          // MXFP4 converter warps (two threads per weight row)
+constexpr int kThreadsMx = (kConvFirstWarp + kConvWarps) * 32;  // 480
 constexpr int kBK = 64;                        // K elements per block (128 bytes of bf16)
 constexpr int kATileBytes = 128 * kBK * 2;     // 16 KB
 constexpr int kPackBytes = 128 * kBK / 2;              // packed E2M1 bytes of one 128 x 64 weight block
@@ -205,6 +206,44 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
     }
 }
 
+// ---- MXFP4 (OCP MX: E2M1 elements, E8M0 scale per 32) -> bf16 ----------------
+// E2M1 magnitude index i = code & 7 has value {0, .5, 1, 1.5, 2, 3, 4, 6}[i].
+// Times 2^d its bf16 has exponent field f_i + d with f = {-, 126, 127, 127,
+// 128, 128, 129, 129} and mantissa {0, 0, 0, 0x40, 0, 0x40, 0, 0x40}; the
+// decode is exact while every field stays in [1, 254] (|d| <= 125).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
+    const uint32_t ex = (code >> 1) & 3u, man = code & 1u;
+    const float v = ex == 0u ? 0.5f * (float)man : __int_as_float((int)(ex + 126u) << 23) * (1.0f + 0.5f * (float)man);
+    return (code & 8u) ? -v : v;
+}
+
+// High and low bytes of the eight magnitudes' bf16 at scale 2^d, packed four
+// per register for byte-permute lookups (h[0]/l[0]: indices 0-3, h[1]/l[1]: 4-7).
+__device__ __forceinline__ void mx_tables(int d, uint32_t (&h)[2], uint32_t (&l)[2]) {
+    const uint32_t a = 126 + d, b = a + 1, c = a + 2, e = a + 3;   // exponent fields
+    h[0] = ((a >> 1) << 8) | ((b >> 1) << 16) | ((b >> 1) << 24);
+    h[1] = (c >> 1) | ((c >> 1) << 8) | ((e >> 1) << 16) | ((e >> 1) << 24);
+    l[0] = ((a & 1u) << 15) | ((b & 1u) << 23) | (((b & 1u) << 31) | (0x40u << 24));
+    l[1] = ((c & 1u) << 7) | ((((c & 1u) << 7) | 0x40u) << 8) | ((e & 1u) << 23) | ((((e & 1u) << 7) | 0x40u) << 24);
+}
+
+// Eight E2M1 codes of one 32-bit word (code j in bits 4j..4j+3) -> four bf16
+// pairs (elements 2q and 2q+1 in o[q]).
+__device__ __forceinline__ void mx_decode_word(uint32_t w, const uint32_t (&h)[2], const uint32_t (&l)[2],
+                                               uint32_t (&o)[4]) {
+    const uint32_t sel0 = w & 0x7777u, sel1 = (w >> 16) & 0x7777u;     // magnitudes of codes 0-3, 4-7
+    const uint32_t h0 = __byte_perm(h[0], h[1], sel0), l0 = __byte_perm(l[0], l[1], sel0);
+    const uint32_t h1 = __byte_perm(h[0], h[1], sel1), l1 = __byte_perm(l[0], l[1], sel1);
+    o[0] = __byte_perm(l0, h0, 0x5140);
+    o[1] = __byte_perm(l0, h0, 0x7362);
+    o[2] = __byte_perm(l1, h1, 0x5140);
+    o[3] = __byte_perm(l1, h1, 0x7362);
+    // sign of code 2q is bit 3 of byte q (-> bit 15), of code 2q+1 bit 7 (-> bit 31)
+    const uint32_t w4 = w << 4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] |= __byte_perm(w, w4, (q << 12) | ((4 + q) << 4)) & 0x80008000u;
+}
+
 template <int BN, int S, bool MX>
 __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
     constexpr int kBBytes = BN * kBK * 2;
@@ -214,14 +253,13 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
     // S stages, each a 16 KB weight tile and a BN-row token tile that share
     // one "full" barrier (both producers arrive) and one "empty" barrier (one
     // MMA commit per stage).
-    // MXFP4 weights add: a ring of packed E2M1 blocks (S x 4 KB), two scale
-    // slots (2 x 2 KB, 8 K blocks each) and a byte -> bf16x2 table (2 KB).
+    // MXFP4 weights add: a ring of packed E2M1 blocks (S x 4 KB) and two
+    // scale slots (2 x 2 KB, 8 K blocks each).
     uint8_t* a_ring = smem;
     uint8_t* b_ring = smem + S * kATileBytes;
     uint8_t* p_ring = b_ring + S * kBBytes;
     uint8_t* sc_ring = p_ring + (MX ? S * kPackBytes : 0);
-    uint2* lut = reinterpret_cast<uint2*>(sc_ring + (MX ? 2 * kScaleBytes : 0));
-    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(lut) + (MX ? 256 * sizeof(uint2) : 0));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sc_ring + (MX ? 2 * kScaleBytes : 0));
     uint64_t* empty = full + S;
     uint64_t* fullP = empty + S;                 // MX: packed block landed
     uint64_t* fullS = fullP + (MX ? S : 0);      // MX: scale group landed
@@ -244,37 +282,17 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
         }
     }
 
-    if constexpr (MX) {
-        // bf16 pair of the two E2M1 codes of byte b (low nibble first) at scale
-        // 2^0, and the bf16 exponent-field unit of each nonzero half.
-        for (int b = threadIdx.x; b < 256; b += blockDim.x) {
-            uint32_t v = 0, nz = 0;
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t c = (b >> (4 * h)) & 15u;
-                const uint32_t ex = (c >> 1) & 3u, man = c & 1u;
-                uint32_t bits = 0;
-                if (ex) bits = ((126u + ex) << 7) | (man << 6);      // (1 + man/2) * 2^(ex-1)
-                else if (man) bits = 126u << 7;                      // 0.5
-                if (bits) {
-                    bits |= (c & 8u) << 12;
-                    nz |= 0x80u << (16 * h);
-                }
-                v |= bits << (16 * h);
-            }
-            lut[b] = make_uint2(v, nz);
-        }
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            // token producer + weight producer (bf16) or + four converter warps (MXFP4)
-            tc::mbar_init(&full[s], MX ? 5 : 2);
+            // token producer + weight producer (bf16) or + the converter warps (MXFP4)
+            tc::mbar_init(&full[s], MX ? 1 + kConvWarps : 2);
             tc::mbar_init(&empty[s], 1);   // one MMA commit per stage
             if (MX) tc::mbar_init(&fullP[s], 1);
         }
         if (MX) {
             for (int g = 0; g < 2; ++g) {
                 tc::mbar_init(&fullS[g], 1);
-                tc::mbar_init(&emptyS[g], 4);
+                tc::mbar_init(&emptyS[g], kConvWarps);
             }
         }
         for (int a = 0; a < 2; ++a) {
@@ -399,10 +417,11 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
         }
     } else if (MX && warp >= kConvFirstWarp) {
         // ------------------------------------------------- MXFP4 converters
-        // Thread r decodes weight row r of each 128 x 64 block: 32 packed
-        // bytes -> 64 bf16 (table value plus the E8M0 exponent), written into
-        // the stage's A tile in the 128-byte swizzled layout.
-        const int r = threadIdx.x - kConvFirstWarp * 32;
+        // Two threads per weight row: thread (r, hh) decodes elements
+        // 32*hh .. 32*hh+31 of row r of each 128 x 64 block (16 packed bytes,
+        // one E8M0 scale) into bf16 in the stage's swizzled A tile.
+        const int ct = threadIdx.x - kConvFirstWarp * 32;
+        const int r = ct >> 1, hh = ct & 1;
         int s = 0, gidx = 0;
         uint32_t ph = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
@@ -419,37 +438,38 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-                const uint4* src = reinterpret_cast<const uint4*>(p_ring + s * kPackBytes + r * (kBK / 2));
-                const uint4 q0 = src[0], q1 = src[1];
-                const uint8_t* scr = sc_ring + slot * kScaleBytes + r * 16 + (kb % kScaleGroup) * 2;
-                const int sc0 = scr[0], sc1 = scr[1];
+                const uint4 q = *reinterpret_cast<const uint4*>(p_ring + s * kPackBytes + r * (kBK / 2) + hh * 16);
+                const int sc = sc_ring[slot * kScaleBytes + r * 16 + (kb % kScaleGroup) * 2 + hh];
                 uint8_t* dst = a_ring + s * kATileBytes + r * 128;
-                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                const bool fast = sc0 >= 2 && sc0 <= 252 && sc1 >= 2 && sc1 <= 252;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int sc = c < 4 ? sc0 : sc1;
-                    const uint32_t wd = words[c];
-                    uint32_t o[4];
+                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                if (sc >= 2 && sc <= 252) {
+                    uint32_t th[2], tl[2];
+                    mx_tables(sc - 127, th, tl);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint32_t byte = (wd >> (8 * j)) & 0xFFu;
-                        if (fast) {
-                            const uint2 e = lut[byte];
-                            o[j] = e.x + (uint32_t)(sc - 127) * e.y;
-                        } else {
-                            // exact fallback: code value times 2^(sc-127), rounded to bf16
-                            const float m = __int_as_float(sc == 0 ? 0x00400000 : (sc << 23));
+                        const int c = hh * 4 + j;
+                        uint32_t o[4];
+                        mx_decode_word(words[j], th, tl, o);
+                        *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                } else {
+                    const float m = __int_as_float(sc == 0 ? 0x00400000 : (sc << 23));   // 2^(sc-127)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = hh * 4 + j;
+                        uint32_t o[4];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
                             uint32_t pr = 0;
+#pragma unroll
                             for (int h = 0; h < 2; ++h) {
-                                const uint32_t hb = (lut[byte].x >> (16 * h)) & 0xFFFFu;
-                                const float v = __uint_as_float(hb << 16) * m;
+                                const float v = e2m1_to_f32((words[j] >> (8 * b + 4 * h)) & 15u) * m;
                                 pr |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v)) << (16 * h);
                             }
-                            o[j] = pr;
+                            o[b] = pr;
                         }
+                        *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                     }
-                    *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 tc::fence_proxy_async_smem();   // generic-proxy writes -> tcgen05.mma reads
                 __syncwarp();
@@ -821,7 +841,7 @@ template <int BN, bool MX>
 constexpr size_t smem_for() {
     constexpr int S = MX ? StagesMx<BN>::S : Stages<BN>::S;
     return 1024 + (size_t)S * (kATileBytes + BN * kBK * 2 + (MX ? kPackBytes : 0)) +
-           (MX ? 2 * kScaleBytes + 256 * sizeof(uint2) : 0) + 768 + 128 * kStLd * 4 + 2 * (QBMOE_MAX_EXPERTS + 1) * 4;
+           (MX ? 2 * kScaleBytes : 0) + 768 + 128 * kStLd * 4 + 2 * (QBMOE_MAX_EXPERTS + 1) * 4;
 }
 
 }  // namespace
