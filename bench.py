@@ -179,54 +179,74 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Max of x over the ranks (NCCL on GPUs, gloo on CPU)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(tokens_per_rank, ms_local, world):
+    """Whole-job routed tokens/s of `world` independent replicas: all ranks'
+    tokens over the slowest rank's time (weak scaling)."""
+    ms = max_over_ranks(ms_local, world)
+    return tokens_per_rank * world / (ms * 1e-3), ms
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(shape, n_tok, seed=0):
-    """Time the oracle on: full routing of the batch + the dense layer for
-    n_tok sampled tokens.  Weight draws happen before the clock starts.
-    Returns (seconds for routing, seconds for the dense part, tokens)."""
-    from oracle import qb_oracle as O
-    inp = QI.LayerInputs(shape)
-    rng = np.random.default_rng(seed)
-    tokens = np.sort(rng.choice(shape.T, n_tok, replace=False))
+class OracleSample:
+    """The CPU oracle on a bounded sample of a workload: full routing of the
+    batch (QB quantiles are over all T tokens) plus the dense layer for n_tok
+    seeded sampled tokens.  Weight draws (and fp32 caches of the sampled
+    tokens' experts) are made once, before any clock starts."""
 
-    class Cached(O.LayerWeights):
-        def __init__(self, inputs):
-            super().__init__(inputs)
-            self.cache = {}
+    def __init__(self, shape, n_tok, seed=0):
+        from oracle import qb_oracle as O
+        self.O = O
+        self.shape = shape
+        self.inp = QI.LayerInputs(shape)
+        rng = np.random.default_rng(seed)
+        self.tokens = np.sort(rng.choice(shape.T, n_tok, replace=False))
 
-        def expert(self, name, e):
-            return self.cache[(name, int(e))].astype(np.float64)
+        class Cached(O.LayerWeights):
+            def __init__(self, inputs):
+                super().__init__(inputs)
+                self.cache = {}
 
-    W = Cached(inp)
-    for nm in ("x", "w_router", "router_offset", "w_down", "gamma", "w_proj_up", "w_shared_gate",
-               "w_shared_up", "w_shared_out"):
-        if nm in inp.specs:
-            W.dense(nm)
-    t0 = time.perf_counter()
-    logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
-    route = O.moe_route_qb(logits, None, shape.k, shape.qb_sweeps)
-    t_route = time.perf_counter() - t0
-    for e in np.unique(route[2][tokens]):
-        for nm in ("w_gate", "w_up", "w_out"):
-            W.cache[(nm, int(e))] = O.LayerWeights.expert(W, nm, e).astype(np.float32)
-    t1 = time.perf_counter()
-    O.layer_forward(inp, tokens=tokens, logits=logits, weights=W)
-    t_layer = time.perf_counter() - t1
-    # layer_forward re-runs the routing over all T tokens; count it once
-    t_dense = max(t_layer - t_route, 1e-9)
-    return t_route, t_dense, n_tok
+            def expert(self, name, e):
+                return self.cache[(name, int(e))].astype(np.float64)
+
+        W = Cached(self.inp)
+        for nm in ("x", "w_router", "router_offset", "w_down", "gamma", "w_proj_up", "w_shared_gate",
+                   "w_shared_up", "w_shared_out"):
+            if nm in self.inp.specs:
+                W.dense(nm)
+        logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
+        idx = O.moe_route_qb(logits, None, shape.k, shape.qb_sweeps)[2]
+        for e in np.unique(idx[self.tokens]):
+            for nm in ("w_gate", "w_up", "w_out"):
+                W.cache[(nm, int(e))] = O.LayerWeights.expert(W, nm, e).astype(np.float32)
+        self.W = W
+
+    def run(self):
+        """Seconds for (routing of all T tokens, dense layer of the sample)."""
+        O, W, shape = self.O, self.W, self.shape
+        t0 = time.perf_counter()
+        logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
+        O.moe_route_qb(logits, None, shape.k, shape.qb_sweeps)
+        t_route = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        O.layer_forward(self.inp, tokens=self.tokens, logits=logits, weights=W)
+        t_layer = time.perf_counter() - t1
+        # layer_forward re-runs the routing over all T tokens; count it once
+        return t_route, max(t_layer - t_route, 1e-9)
 
 
 def cpu_cores():
@@ -237,7 +257,8 @@ def cpu_cores():
 
 
 def cpu_baseline(shape, n_tok):
-    t_route, t_dense, S = oracle_sample(shape, n_tok)
+    t_route, t_dense = OracleSample(shape, n_tok).run()
+    S = n_tok
     est = t_route + t_dense * shape.T / S
     return {"value": shape.T / est, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": (f"numpy oracle: router GEMM (fp64) + QB routing of all {shape.T} tokens "
@@ -251,11 +272,12 @@ def run_reference(args, shape, world, rank):
     if rank != 0:
         return
     n_tok = max(1, int(os.environ.get("QB_ORACLE_TOKENS", "2")))
+    sample = OracleSample(shape, n_tok)
     times = []
     for i in range(args.warmup + args.steps):
-        t_route, t_dense, S = oracle_sample(shape, n_tok, seed=i)
+        t_route, t_dense = sample.run()
         if i >= args.warmup:
-            times.append(t_route + t_dense * shape.T / S)
+            times.append(t_route + t_dense * shape.T / n_tok)
     sec = statistics.mean(times)
     val = shape.T / sec
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "routed tokens/s", "n_gpus": 1,
@@ -312,7 +334,7 @@ def run_ours(args, shape, world, rank, local):
     if rc:
         raise RuntimeError(f"device status {rc} in the timed region")
     stages = lay.stage_times()
-    ms_max = max_over_ranks(ms, world)
+    value_job, ms_max = replica_throughput(shape.T, ms, world)
 
     # end to end: pinned host input -> device, forward, device -> host output
     x_host = x.cpu().pin_memory()
@@ -356,7 +378,7 @@ def run_ours(args, shape, world, rank, local):
     cpu = cpu_baseline(shape, n_cpu_tok) if world == 1 and not args.no_cpu else None
     tok = shape.T * world
     line = {
-        "metric": METRIC, "value": tok / (ms_max * 1e-3), "unit": "routed tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": value_job, "unit": "routed tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if shape.wfmt == "bf16" else ("bf16+mxfp4" if shape.wfmt == "mxfp4" else "f32"),
