@@ -100,6 +100,33 @@ int moe_route_qb(int T, int n, int k, int qb_sweeps,
                  void* workspace, size_t workspace_bytes, qbmoe_stream_t stream);
 
 /*
+ * moe_route_qb_gs — Quantile Balancing by cyclic coordinate descent.
+ *
+ * [K3-width] 延伸解读 "QB vs DeepSeek-V3": QB solves the balanced-assignment
+ * dual by coordinate descent, jumping to the exact coordinate minimiser.
+ * This is the literal cyclic form: within a sweep the experts are updated in
+ * order j = 0..n-1, each step computing expert j's margins under the latest
+ * biases (tau[t][j] = k-th best fl(s + b) among the other experts) and
+ * setting b_j = -midpoint of its r_j-th and (r_j+1)-th largest margins, as in
+ * moe_route_qb; after the sweep the common offset is subtracted.  Repeated
+ * sweeps never raise the dual; once every expert's load equals its target
+ * the assignment is optimal for the balanced problem.
+ *
+ * max_sweeps >= 0 sweeps are run; with stop_when_balanced != 0 the sweeps
+ * stop (on the device) after the first sweep whose loads equal the targets.
+ * sweeps_done: device int32 or NULL, receives the number of sweeps run.
+ * Other arguments as moe_route_qb; workspace >= qbmoe_route_gs_workspace_bytes.
+ * Cost: about 2n + 5 kernel launches per sweep (a quality mode for balancing,
+ * not the layer's hot path, which uses the one-pass Jacobi sweep).
+ */
+size_t qbmoe_route_gs_workspace_bytes(int T, int n, int k);
+int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_when_balanced,
+                    const float* logits, const float* bias_in, float* bias_out,
+                    float* scores, int32_t* topk_idx, float* topk_w, int32_t* loads,
+                    int32_t* sweeps_done, void* workspace, size_t workspace_bytes,
+                    qbmoe_stream_t stream);
+
+/*
  * moe_route_qb_noalloc — moe_route_qb for callers that cannot allocate.
  *
  * The pages have no counterpart: this is a deployment variant of the router

@@ -65,6 +65,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qbmoe_route_workspace_bytes.restype = sz
     lib.moe_route_qb.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.moe_route_qb.restype = i
+    lib.qbmoe_route_gs_workspace_bytes.argtypes = [i, i, i]
+    lib.qbmoe_route_gs_workspace_bytes.restype = sz
+    lib.moe_route_qb_gs.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_route_qb_gs.restype = i
     lib.moe_route_qb_noalloc.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.moe_route_qb_noalloc.restype = i
     lib.qbmoe_route_noalloc_max_bytes.argtypes = []
@@ -176,6 +180,31 @@ def route_qb(logits, k: int, qb_sweeps: int = 1, bias_in=None, bias_out=None, wo
     if rc:
         raise QbmoeError(rc, "moe_route_qb")
     return scores, bias_out, idx, w, loads
+
+
+def route_qb_gs(logits, k: int, max_sweeps: int = 1, stop_when_balanced: bool = False, bias_in=None,
+                stream=None):
+    """Cyclic coordinate-descent QB on fp32 logits [T, n] (moe_route_qb_gs).
+    Returns (scores, bias, idx, w, loads, sweeps_done)."""
+    import torch
+    T, n = logits.shape
+    dev = logits.device
+    assert logits.dtype == torch.float32 and logits.is_contiguous() and dev.type == "cuda"
+    scores = torch.empty((T, n), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    loads = torch.empty((n,), dtype=torch.int32, device=dev)
+    bias_out = torch.empty((n,), dtype=torch.float32, device=dev)
+    done = torch.zeros((4,), dtype=torch.int32, device=dev)
+    lib = load_library()
+    need = lib.qbmoe_route_gs_workspace_bytes(T, n, k)
+    ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    rc = lib.moe_route_qb_gs(T, n, k, max_sweeps, int(stop_when_balanced), _p(logits), _p(bias_in), _p(bias_out),
+                             _p(scores), _p(idx), _p(w), _p(loads), _p(done), _p(ws), ws.numel(),
+                             _stream_ptr(stream))
+    if rc:
+        raise QbmoeError(rc, "moe_route_qb_gs")
+    return scores, bias_out, idx, w, loads, done[:1]
 
 
 class LatentMoE:

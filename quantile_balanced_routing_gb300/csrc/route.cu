@@ -191,24 +191,19 @@ QB_DEV uint32_t radix_select(const uint32_t* keys_smem, const float* col, int T,
     return prefix;
 }
 
+// Exact coordinate minimiser of one expert from its T margins `col` (keys
+// staged in SMEM when kSmem): returns -q, q the midpoint of the r-th and
+// (r+1)-th largest margins (r = 0: M_1 + 1; r >= T: M_T - 1).  Result valid
+// in thread 0; every thread of the CTA must call it.
 template <bool kSmem>
-__global__ void __launch_bounds__(kSelectThreads)
-k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw) {
-    extern __shared__ uint32_t keys[];
-    __shared__ unsigned hist[256];
-    __shared__ int s_digit, s_rank;
-    __shared__ float red[kSelectThreads / 32];
-    const int j = blockIdx.x;
-    const float* col = margins + (size_t)j * T;
-    const long long total = (long long)T * k;
-    const int r = (int)(total / n) + (j < (int)(total % n) ? 1 : 0);
+QB_DEV float coordinate_bias(int T, int r, const float* col, uint32_t* keys, unsigned* hist, int* s_digit,
+                             int* s_rank, float* red) {
     const int tid = threadIdx.x;
-
     if (kSmem) {
         for (int i = tid; i < T; i += blockDim.x) keys[i] = ~f32_order_key(col[i]);
         __syncthreads();
     }
-    float q;
+    float q = 0.0f;
     if (r <= 0 || r >= T) {
         // max margin (r = 0) or min margin (r >= T)
         const bool want_max = r <= 0;
@@ -228,18 +223,35 @@ k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* _
             float a = red[0];
             for (int w = 1; w < (int)(blockDim.x / 32); ++w) a = want_max ? fmaxf(a, red[w]) : fminf(a, red[w]);
             q = want_max ? __fadd_rn(a, 1.0f) : __fsub_rn(a, 1.0f);
-            bias_raw[j] = -q;
         }
-        return;
+        return -q;
     }
-    const uint32_t kr = radix_select<kSmem>(keys, col, T, r, hist, &s_digit, &s_rank);
-    const uint32_t kr1 = radix_select<kSmem>(keys, col, T, r + 1, hist, &s_digit, &s_rank);
+    const uint32_t kr = radix_select<kSmem>(keys, col, T, r, hist, s_digit, s_rank);
+    const uint32_t kr1 = radix_select<kSmem>(keys, col, T, r + 1, hist, s_digit, s_rank);
     if (tid == 0) {
         const float Mr = f32_from_order_key(~kr);
         const float Mr1 = f32_from_order_key(~kr1);
         q = __fmul_rn(__fadd_rn(Mr, Mr1), 0.5f);
-        bias_raw[j] = -q;
     }
+    return -q;
+}
+
+QB_DEV int target_load(int T, int n, int k, int j) {
+    const long long total = (long long)T * k;
+    return (int)(total / n) + (j < (int)(total % n) ? 1 : 0);
+}
+
+template <bool kSmem>
+__global__ void __launch_bounds__(kSelectThreads)
+k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw) {
+    extern __shared__ uint32_t keys[];
+    __shared__ unsigned hist[256];
+    __shared__ int s_digit, s_rank;
+    __shared__ float red[kSelectThreads / 32];
+    const int j = blockIdx.x;
+    const float b = coordinate_bias<kSmem>(T, target_load(T, n, k, j), margins + (size_t)j * T, keys, hist,
+                                           &s_digit, &s_rank, red);
+    if (threadIdx.x == 0) bias_raw[j] = b;
 }
 
 // b = fl(b' - c), c = fl(tree(b') / n); one warp.  Optionally also writes out2.
@@ -358,6 +370,172 @@ __global__ void k_block_scan(int nblk, int n, int* __restrict__ blk_cnt, int32_t
     }
     if (lane == 0 && loads) loads[j] = running;
 }
+
+// ---------------------------------------------------------------------------
+// Cyclic (Gauss-Seidel) QB sweep: experts updated one after another, each
+// coordinate step seeing the latest biases.  Per token the top-(k+1) list of
+// v = s + b is kept; expert j's step reads tau from it, and the next step
+// refreshes only the lists that expert j's new bias can change (j in the
+// list, or j's new value ranking before the list's last entry).
+
+// Full top-(k1) list of one token (warp): lane r < k1 ends with the r-th
+// ranked (value, index).
+template <int NPL>
+QB_DEV void top_list(const float (&v)[NPL], int k1, int lane, float& my_v, int& my_j) {
+    uint32_t removed = 0;
+    float bv;
+    int bj;
+    lane_best<NPL>(v, removed, lane, bv, bj);
+    for (int r = 0; r < k1; ++r) {
+        float wv = bv;
+        int wj = bj;
+        warp_best(wv, wj);
+        if (lane == r) { my_v = wv; my_j = wj; }
+        if ((wj & 31) == lane) {
+            removed |= 1u << (wj >> 5);
+            lane_best<NPL>(v, removed, lane, bv, bj);
+        }
+    }
+}
+
+template <int NPL>
+QB_DEV void biased_row(const float* __restrict__ s_row, const float* __restrict__ b, int n, int lane, float (&v)[NPL]) {
+#pragma unroll
+    for (int c = 0; c < NPL; ++c) {
+        const int j = lane + 32 * c;
+        v[c] = j < n ? __fadd_rn(s_row[j], b[j]) : -INFINITY;
+    }
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(256)
+k_gs_lists(int T, int n, int k, const float* __restrict__ s, const float* __restrict__ b, float* __restrict__ lv,
+           int* __restrict__ li, const int* __restrict__ done) {
+    if (*done) return;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int K1 = k + 1;
+    float v[NPL];
+    biased_row<NPL>(s + (size_t)t * n, b, n, lane, v);
+    float my_v = 0.0f;
+    int my_j = 0;
+    top_list<NPL>(v, K1, lane, my_v, my_j);
+    if (lane < K1) {
+        lv[(size_t)t * K1 + lane] = my_v;
+        li[(size_t)t * K1 + lane] = my_j;
+    }
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(256)
+k_gs_token(int T, int n, int k, int j, int prev, const float* __restrict__ s, const float* __restrict__ b,
+           float* __restrict__ lv, int* __restrict__ li, float* __restrict__ mj, const int* __restrict__ done) {
+    if (*done) return;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int K1 = k + 1;
+    float ev = lane < K1 ? lv[(size_t)t * K1 + lane] : 0.0f;
+    int ej = lane < K1 ? li[(size_t)t * K1 + lane] : -1;
+    if (prev >= 0) {
+        const float vn = __fadd_rn(s[(size_t)t * n + prev], b[prev]);
+        const bool in_list = __any_sync(0xffffffffu, lane < K1 && ej == prev);
+        const float lastv = __shfl_sync(0xffffffffu, ev, k);
+        const int lastj = __shfl_sync(0xffffffffu, ej, k);
+        if (in_list || ranks_before(vn, prev, lastv, lastj)) {
+            float v[NPL];
+            biased_row<NPL>(s + (size_t)t * n, b, n, lane, v);
+            top_list<NPL>(v, K1, lane, ev, ej);
+            if (lane < K1) {
+                lv[(size_t)t * K1 + lane] = ev;
+                li[(size_t)t * K1 + lane] = ej;
+            }
+        }
+    }
+    // tau: the k-th best biased score among the experts other than j
+    const bool in_top = __any_sync(0xffffffffu, lane < k && ej == j);
+    const float tau = __shfl_sync(0xffffffffu, ev, in_top ? k : k - 1);
+    if (lane == 0) {
+        float m = __fsub_rn(s[(size_t)t * n + j], tau);
+        if (m == 0.0f) m = 0.0f;
+        mj[t] = m;
+    }
+}
+
+template <bool kSmem>
+__global__ void __launch_bounds__(kSelectThreads)
+k_gs_select(int T, int n, int k, int j, const float* __restrict__ mj, float* __restrict__ b,
+            const int* __restrict__ done) {
+    if (*done) return;
+    extern __shared__ uint32_t keys[];
+    __shared__ unsigned hist[256];
+    __shared__ int s_digit, s_rank;
+    __shared__ float red[kSelectThreads / 32];
+    const float bj = coordinate_bias<kSmem>(T, target_load(T, n, k, j), mj, keys, hist, &s_digit, &s_rank, red);
+    if (threadIdx.x == 0) b[j] = bj;
+}
+
+// In-place common offset of a sweep (skipped once the loads are balanced).
+__global__ void k_gs_offset(int n, float* __restrict__ b, const int* __restrict__ done) {
+    if (*done) return;
+    const int lane = threadIdx.x & 31;
+    int P = 1;
+    while (P < n) P <<= 1;
+    const int L = P >= 32 ? P / 32 : 1;
+    const int A = P / L;
+    float a[32];
+    float x = 0.0f;
+    if (lane < A) {
+        for (int i = 0; i < L; ++i) {
+            const int jj = lane * L + i;
+            a[i] = jj < n ? b[jj] : 0.0f;
+        }
+        for (int w = L; w > 1; w >>= 1)
+            for (int i = 0; i < w / 2; ++i) a[i] = __fadd_rn(a[2 * i], a[2 * i + 1]);
+        x = a[0];
+    }
+    for (int off = 1; off < A; off <<= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, x, off);
+        if ((lane % (2 * off)) == 0) x = __fadd_rn(x, o);
+    }
+    const float c = __fdiv_rn(__shfl_sync(0xffffffffu, x, 0), (float)n);
+    __syncwarp();
+    for (int jj = lane; jj < n; jj += 32) b[jj] = __fsub_rn(b[jj], c);
+}
+
+// After a sweep: record the sweep count; stop further sweeps once every
+// expert's load equals its target (when asked to).
+__global__ void __launch_bounds__(1024)
+k_gs_check(int T, int n, int k, const int32_t* __restrict__ loads, int* __restrict__ done,
+           int32_t* __restrict__ sweeps_done, int sweep, int stop_when_balanced) {
+    if (*done) return;
+    const int j = threadIdx.x;
+    const int bad = (j < n) && loads[j] != target_load(T, n, k, j);
+    const int any_bad = __syncthreads_or(bad);
+    if (j == 0) {
+        if (sweeps_done) *sweeps_done = sweep + 1;
+        if (stop_when_balanced && !any_bad) *done = 1;
+    }
+}
+
+template <int NPL>
+struct GsListsLaunch {
+    static int run(int T, int n, int k, const float* s, const float* b, float* lv, int* li, const int* done,
+                   cudaStream_t st) {
+        k_gs_lists<NPL><<<(T + 7) / 8, 256, 0, st>>>(T, n, k, s, b, lv, li, done);
+        return qbh::cuda_err(cudaGetLastError());
+    }
+};
+
+template <int NPL>
+struct GsTokenLaunch {
+    static int run(int T, int n, int k, int j, int prev, const float* s, const float* b, float* lv, int* li,
+                   float* mj, const int* done, cudaStream_t st) {
+        k_gs_token<NPL><<<(T + 7) / 8, 256, 0, st>>>(T, n, k, j, prev, s, b, lv, li, mj, done);
+        return qbh::cuda_err(cudaGetLastError());
+    }
+};
 
 int npl_for(int n) {
     const int need = (n + 31) / 32;
@@ -542,5 +720,112 @@ extern "C" int moe_route_qb(int T, int n, int k, int qb_sweeps, const float* log
                                           rb.blk_cnt, rb, s, &nl);
     if (!rc) rc = qbh::launch_loads_from_counts(T, n, qbh::route_tokens_per_warp(T), rb.blk_cnt, loads, s, &nl);
     g_route_launches = nl;
+    return rc;
+}
+
+// ---------------------------------------------------------------------------
+// C ABI: moe_route_qb_gs (cyclic coordinate-descent QB)
+// ---------------------------------------------------------------------------
+namespace {
+
+struct GsBuffers {
+    float* lv;     // [T, k+1] top-(k+1) values per token
+    int* li;       // [T, k+1] their experts
+    float* mj;     // [T] margins of the expert being updated
+    float* b;      // [n] current biases
+    int* done;     // balanced flag
+};
+
+size_t gs_ws_layout(int T, int n, int k, qbh::RouteBuffers* rb, GsBuffers* gb, void* base) {
+    char* p = static_cast<char*>(base);
+    size_t off = qbh::align_up(qbh::route_ws_layout(T, n, k, rb, base), 256);
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = qbh::align_up(off + bytes, 256);
+        return p ? p + o : nullptr;
+    };
+    char* p_lv = take((size_t)T * (k + 1) * sizeof(float));
+    char* p_li = take((size_t)T * (k + 1) * sizeof(int));
+    char* p_mj = take((size_t)T * sizeof(float));
+    char* p_b = take((size_t)n * sizeof(float));
+    char* p_done = take(sizeof(int));
+    if (gb && p) {
+        gb->lv = reinterpret_cast<float*>(p_lv);
+        gb->li = reinterpret_cast<int*>(p_li);
+        gb->mj = reinterpret_cast<float*>(p_mj);
+        gb->b = reinterpret_cast<float*>(p_b);
+        gb->done = reinterpret_cast<int*>(p_done);
+    }
+    return off;
+}
+
+}  // namespace
+
+extern "C" size_t qbmoe_route_gs_workspace_bytes(int T, int n, int k) {
+    if (T < 1 || n < 2 || k < 1) return 0;
+    return gs_ws_layout(T, n, k, nullptr, nullptr, nullptr);
+}
+
+extern "C" int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_when_balanced, const float* logits,
+                               const float* bias_in, float* bias_out, float* scores, int32_t* topk_idx,
+                               float* topk_w, int32_t* loads, int32_t* sweeps_done, void* workspace,
+                               size_t workspace_bytes, qbmoe_stream_t stream) {
+    if (T < 1 || n < 2 || n > QBMOE_MAX_EXPERTS || k < 1 || k >= n || k > QBMOE_MAX_TOPK || max_sweeps < 0)
+        return QBMOE_EINVAL;
+    if (!logits || !scores || !topk_idx || !topk_w || !loads || !workspace) return QBMOE_EINVAL;
+    const void* ptrs[] = {logits, bias_in, bias_out, scores, topk_idx, topk_w, loads, sweeps_done};
+    for (const void* p : ptrs)
+        if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QBMOE_EINVAL;
+    if (workspace_bytes < qbmoe_route_gs_workspace_bytes(T, n, k)) return QBMOE_EWORKSPACE;
+    int rc = qbmoe_check_device_arch();
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    qbh::RouteBuffers rb;
+    GsBuffers gb;
+    gs_ws_layout(T, n, k, &rb, &gb, workspace);
+    const int npl = npl_for(n);
+    if (npl < 0) return QBMOE_EINVAL;
+    int nl = 0;
+    if ((rc = qbh::launch_scores(logits, scores, (long long)T * n, s, &nl))) return rc;
+    if (bias_in) {
+        if (cudaMemcpyAsync(gb.b, bias_in, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return QBMOE_ECUDA;
+    } else if (cudaMemsetAsync(gb.b, 0, (size_t)n * sizeof(float), s) != cudaSuccess) {
+        return QBMOE_ECUDA;
+    }
+    if (cudaMemsetAsync(gb.done, 0, sizeof(int), s) != cudaSuccess) return QBMOE_ECUDA;
+    if (sweeps_done && cudaMemsetAsync(sweeps_done, 0, sizeof(int32_t), s) != cudaSuccess) return QBMOE_ECUDA;
+    const bool smem_sel = T <= kSelectSmemMaxT;
+    const size_t sel_smem = smem_sel ? (size_t)T * sizeof(uint32_t) : 0;
+    if (smem_sel && cudaFuncSetAttribute(k_gs_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)std::max<size_t>(sel_smem, 1)) != cudaSuccess)
+        return QBMOE_ECUDA;
+    const int tpw = qbh::route_tokens_per_warp(T);
+    for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+        if ((rc = dispatch_npl<GsListsLaunch>(npl, T, n, k, (const float*)scores, (const float*)gb.b, gb.lv, gb.li,
+                                              (const int*)gb.done, s)))
+            return rc;
+        for (int j = 0; j < n; ++j) {
+            if ((rc = dispatch_npl<GsTokenLaunch>(npl, T, n, k, j, j - 1, (const float*)scores, (const float*)gb.b,
+                                                  gb.lv, gb.li, gb.mj, (const int*)gb.done, s)))
+                return rc;
+            if (smem_sel) k_gs_select<true><<<1, kSelectThreads, sel_smem, s>>>(T, n, k, j, gb.mj, gb.b, gb.done);
+            else k_gs_select<false><<<1, kSelectThreads, 0, s>>>(T, n, k, j, gb.mj, gb.b, gb.done);
+            if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
+        }
+        k_gs_offset<<<1, 32, 0, s>>>(n, gb.b, gb.done);
+        if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
+        // loads under the new biases, for the sweep count and the balance test
+        if ((rc = qbh::launch_qb_and_topk(T, n, k, 0, scores, gb.b, nullptr, topk_idx, topk_w, rb.blk_cnt, rb, s,
+                                          &nl)))
+            return rc;
+        if ((rc = qbh::launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, &nl))) return rc;
+        k_gs_check<<<1, 1024, 0, s>>>(T, n, k, loads, gb.done, sweeps_done, sweep, stop_when_balanced);
+        if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
+    }
+    // final routing with the final biases
+    rc = qbh::launch_qb_and_topk(T, n, k, 0, scores, gb.b, bias_out, topk_idx, topk_w, rb.blk_cnt, rb, s, &nl);
+    if (!rc) rc = qbh::launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, &nl);
     return rc;
 }
