@@ -32,7 +32,8 @@ import numpy as np  # noqa: E402
 import qb_inputs as QI  # noqa: E402
 
 WORKLOADS = {"decode": QI.DECODE, "prefill": QI.PREFILL, "prefill_mxfp4": QI.PREFILL_MXFP4,
-             "decode_mxfp4": QI.DECODE_MXFP4}
+             "decode_mxfp4": QI.DECODE_MXFP4, "route_qb": QI.ROUTE_QB, "route_qb_gs": QI.ROUTE_QB}
+ROUTE_WORKLOADS = ("route_qb", "route_qb_gs")
 METRIC = "MoE-layer fwd routed tokens/s on 1 GB300; % of HBM / tensor-core roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -272,12 +273,26 @@ def run_reference(args, shape, world, rank):
     if rank != 0:
         return
     n_tok = max(1, int(os.environ.get("QB_ORACLE_TOKENS", "2")))
-    sample = OracleSample(shape, n_tok)
     times = []
-    for i in range(args.warmup + args.steps):
-        t_route, t_dense = sample.run()
-        if i >= args.warmup:
-            times.append(t_route + t_dense * shape.T / n_tok)
+    if args.workload in ROUTE_WORKLOADS:
+        # the oracle's routing of the whole batch from the same fp32 logits
+        from oracle import qb_oracle as O
+        inp = QI.LayerInputs(shape)
+        logits = O.router_logits(inp.values("x"), inp.values("w_router"), inp.values("router_offset"))
+        mode = "gauss_seidel" if args.workload == "route_qb_gs" else "jacobi"
+        steps = min(args.warmup + args.steps, 4) if mode == "gauss_seidel" else args.warmup + args.steps
+        for i in range(steps):
+            t0 = time.perf_counter()
+            O.moe_route_qb(logits, None, shape.k, 1, mode)
+            if i >= min(args.warmup, steps - 1):
+                times.append(time.perf_counter() - t0)
+        n_tok = shape.T
+    else:
+        sample = OracleSample(shape, n_tok)
+        for i in range(args.warmup + args.steps):
+            t_route, t_dense = sample.run()
+            if i >= args.warmup:
+                times.append(t_route + t_dense * shape.T / n_tok)
     sec = statistics.mean(times)
     val = shape.T / sec
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "routed tokens/s", "n_gpus": 1,
@@ -285,8 +300,9 @@ def run_reference(args, shape, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": config_of(shape, args),
             "cpu_baseline": {"value": val, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": (f"each step: full routing of {shape.T} tokens + dense layer of {n_tok} "
-                                        f"sampled tokens, scaled to {shape.T} tokens")},
+                             "sample": (f"each step: full routing of {shape.T} tokens" +
+                                        ("" if args.workload in ROUTE_WORKLOADS else
+                                         f" + dense layer of {n_tok} sampled tokens, scaled to {shape.T} tokens"))},
             "e2e": {"value": val, "unit": "routed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -394,6 +410,83 @@ def run_ours(args, shape, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_route(args, shape, world, rank, local):
+    """The QB-routing workload alone: moe_route_qb (one Jacobi sweep) or
+    moe_route_qb_gs (one cyclic sweep) on fp32 logits x W_r^T + o resident
+    in HBM.  Its working set fits in L2, so L2 is flushed (a 512 MB write)
+    between timed steps, outside each step's event pair."""
+    import torch
+    import quantile_balanced_routing_gb300 as Q
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = QI.LayerInputs(shape.with_(seed=shape.seed + rank))
+    x = torch.from_numpy(inp.values("x")).to(dev)
+    wr = torch.from_numpy(inp.values("w_router")).to(dev)
+    o = torch.from_numpy(inp.values("router_offset")).to(dev)
+    logits = (x @ wr.T + o).contiguous()          # input preparation (not timed)
+    del x, wr
+    gs = args.workload == "route_qb_gs"
+    T, n, k = shape.T, shape.n, shape.k
+    scores = torch.empty((T, n), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    loads = torch.empty((n,), dtype=torch.int32, device=dev)
+    bias = torch.empty((n,), dtype=torch.float32, device=dev)
+    lib = Q.load_library()
+    need = lib.qbmoe_route_gs_workspace_bytes(T, n, k) if gs else Q.qbmoe_route_workspace_bytes(T, n, k)
+    ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+    flush = torch.empty((512 << 20,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    p = lambda t: t.data_ptr()
+
+    def step():
+        if gs:
+            rc = lib.moe_route_qb_gs(T, n, k, 1, 0, p(logits), None, p(bias), p(scores), p(idx), p(w), p(loads),
+                                     None, p(ws), ws.numel(), stream.cuda_stream or None)
+            launches = 2 * n + 6
+        else:
+            rc = Q.moe_route_qb(T, n, k, 1, p(logits), None, p(bias), p(scores), p(idx), p(w), p(loads), p(ws),
+                                ws.numel(), stream.cuda_stream or None)
+            launches = lib.qbmoe_route_last_launch_count()
+        if rc:
+            raise Q.QbmoeError(rc, "routing")
+        return launches
+
+    for _ in range(args.warmup):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    launches = 0
+    with ClockSampler(local) as clocks:
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            launches += step()
+            b.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / max(args.steps, 1)
+    value_job, ms_max = replica_throughput(T, ms, world)
+    if rank != 0:
+        return
+    pk, src = peaks()
+    b_alg = T * n * 4 * 2 + T * k * 8 + n * 8       # logits in, scores out, idx/w out, bias/loads
+    achieved = b_alg / (ms_max * 1e-3) / 1e9
+    line = {"metric": "QB routing tokens/s on 1 GB300; % of HBM roofline", "value": value_job,
+            "unit": "routed tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded)",
+            "config": {"workload": shape.name + ("_gauss_seidel" if gs else "_jacobi"), "T": T, "n_experts": n,
+                       "top_k": k, "qb_sweeps": 1, "l2": "flushed between steps (512 MB write)",
+                       "parallelism": f"replicas x{args.gpus}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "traffic": None, "kernel": "routing (all kernels)",
+                         "algorithmic_bytes": b_alg, "peak_source": src},
+            "gpu_launches": launches, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -415,7 +508,10 @@ def main():
         run_reference(args, shape, int(os.environ.get("WORLD_SIZE", "1")), rank)
         return
     world, rank, local = dist_setup()
-    run_ours(args, shape, world, rank, local)
+    if args.workload in ROUTE_WORKLOADS:
+        run_route(args, shape, world, rank, local)
+    else:
+        run_ours(args, shape, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

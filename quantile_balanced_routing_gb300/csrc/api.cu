@@ -342,7 +342,7 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
 
     // 2-3. QB sweeps and biased top-k
     clk.mark("qb_topk");
-    rc = qbh::launch_qb_and_topk(T, n, k, g.qb_sweeps, c->scores, bias_in, bias_out, c->idx, c->wts,
+    rc = qbh::launch_qb_and_topk(T, n, k, g.qb_sweeps, nullptr, c->scores, bias_in, bias_out, c->idx, c->wts,
                                  c->rb.blk_cnt, c->rb, s, &nl);
     if (rc) return rc;
 

@@ -86,13 +86,13 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct RouteBuffers {
     float* margins;      // [n, T]
     float* bias_raw;     // [n]
-    float* bias_cur;     // [n]
-    int* blk_cnt;        // [nblk, n]
+    int* blk_cnt;        // [n, nblk] per-block expert counts (expert-major)
 };
 size_t route_ws_layout(int T, int n, int k, RouteBuffers* rb, void* base);
 int route_tokens_per_warp(int T);
 int launch_scores(const float* logits, float* scores, long long count, cudaStream_t s, int* nl);
-int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* scores, const float* bias_in,
+// logits may be NULL (scores already computed); bias_in may be NULL (zeros).
+int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* logits, float* scores, const float* bias_in,
                        float* bias_out, int32_t* idx, float* w, int* blk_cnt, const RouteBuffers& rb,
                        cudaStream_t s, int* nl);
 int launch_loads_from_counts(int T, int n, int tpw, const int* blk_cnt, int32_t* loads, cudaStream_t s,

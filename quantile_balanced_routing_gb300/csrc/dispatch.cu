@@ -46,7 +46,7 @@ k_expert_offsets(int n, const int32_t* __restrict__ loads, int* __restrict__ off
 }
 
 // Stable scatter: route (t, i) of expert e goes to
-//   pos = offsets[e] + blk_base[blk][e] + #(tokens of this block before t routed to e).
+//   pos = offsets[e] + blk_base[e][blk] + #(tokens of this block before t routed to e).
 // One thread per token of the block (block = 8 * tpw <= 64 tokens).
 __global__ void k_scatter(int T, int n, int k, int tpw, const int32_t* __restrict__ idx,
                           const int* __restrict__ blk_base, const int* __restrict__ offsets,
@@ -61,11 +61,10 @@ __global__ void k_scatter(int T, int n, int k, int tpw, const int32_t* __restric
         for (int i = 0; i < k; ++i) atomicOr(&masks[idx[(size_t)t * k + i]], 1ull << tl);
     __syncthreads();
     if (t >= T) return;
-    const int* base = blk_base + (size_t)blockIdx.x * n;
     const unsigned long long below = (tl == 0) ? 0ull : ((1ull << tl) - 1ull);
     for (int i = 0; i < k; ++i) {
         const int e = idx[(size_t)t * k + i];
-        const int pos = offsets[e] + base[e] + __popcll(masks[e] & below);
+        const int pos = offsets[e] + blk_base[(size_t)e * gridDim.x + blockIdx.x] + __popcll(masks[e] & below);
         perm[pos] = t;
         route_pos[(size_t)t * k + i] = pos;
     }

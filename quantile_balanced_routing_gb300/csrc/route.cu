@@ -8,17 +8,21 @@
 //   Q&A on routing: sigmoid scores, top-k on score + bias, mixture weights =
 //     raw scores renormalised over the chosen k, bias frozen at inference.
 //
-// Kernels (one sweep = token pass + expert select + offset):
-//   k_scores        s = score_of_logit(logit), elementwise
-//   k_token_pass    per token: top-(k+1) of v = s + b by warp argmax rounds;
-//                   margins m = s - tau written transposed [n, T] via SMEM
+// Kernels (one sweep = token pass + expert select):
+//   k_scores        s = score_of_logit(logit), elementwise (only when no sweep
+//                   runs; otherwise the first token pass computes s)
+//   k_token_pass    per token: top-(k+1) of v = s + b (threshold gather and a
+//                   warp sort, or ranking rounds); margins m = s - tau written
+//                   transposed [n, T] via SMEM
 //   k_expert_select per expert: exact r-th and (r+1)-th largest margin by a
 //                   4-pass 8-bit radix select with warp-aggregated SMEM
-//                   histograms; b'_j = -midpoint
-//   k_offset        b = b' - (pairwise-tree sum of b') / n   (one warp)
+//                   histograms (later passes over the first bucket's keys);
+//                   b'_j = -midpoint
 //   k_topk          per token: top-k of s + b, rank-order weights, per-block
 //                   expert counts
 //   k_block_scan    per expert: exclusive prefix of block counts, loads
+// The common offset b = b' - (pairwise-tree sum of b') / n is applied by every
+// CTA of the kernel that reads the biases next (stage_bias).
 #include "common.cuh"
 
 #include <algorithm>
@@ -29,11 +33,12 @@ namespace {
 
 using namespace qb;
 
-constexpr int kTokPassTokens = 32;   // tokens per CTA in the token pass
+constexpr int kTokPassTokens = 16;   // tokens per CTA in the token pass (one per warp)
 constexpr int kTokPassWarps = 16;
 constexpr int kTopkWarps = 8;
 constexpr int kSelectThreads = 512;
-constexpr int kSelectSmemMaxT = 50 * 1024;   // margins staged in SMEM up to this T
+constexpr int kSelectSmemMaxT = 48 * 1024;   // margins staged in SMEM up to this T
+constexpr int kSelectCand = 4096;            // candidate words after the first digit pass
 
 __global__ void k_scores(const float* __restrict__ logits, float* __restrict__ scores, long long count) {
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -41,24 +46,116 @@ __global__ void k_scores(const float* __restrict__ logits, float* __restrict__ s
     for (; i < count; i += stride) scores[i] = score_of_logit(logits[i]);
 }
 
-// Warp-wide argmax under (value desc, index asc).
-QB_DEV void warp_best(float& v, int& j) {
+// Ranking of one token's n values v (lane owns slots j = lane + 32 c) under
+// (value desc, index asc).  Values are compared through order keys
+// (f32_order_key of v with -0 folded into +0, 0 for padding slots), so a
+// warp's next-ranked entry is one max-reduce over the lanes' head keys plus
+// one min-reduce over the indices of the heads that tie with it.  Each lane
+// caches its two best remaining slots and rescans its NPL slots only when a
+// third one is taken.
+QB_DEV uint32_t value_key(float v) { return f32_order_key(v == 0.0f ? 0.0f : v); }
+
+template <int NPL>
+struct WarpRanker {
+    uint32_t removed = 0;   // slots already ranked
+    uint32_t k0 = 0, k1 = 0;
+    int c0 = 0, c1 = 0;
+    bool have1 = false;
+
+    QB_DEV void scan(const uint32_t (&key)[NPL]) {
+        k0 = k1 = 0;
+        c0 = c1 = 0;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-        const int oj = __shfl_xor_sync(0xffffffffu, j, off);
-        if (ranks_before(ov, oj, v, j)) { v = ov; j = oj; }
+        for (int c = 0; c < NPL; ++c) {
+            const uint32_t kc = ((removed >> c) & 1u) ? 0u : key[c];
+            if (kc > k0) { k1 = k0; c1 = c0; k0 = kc; c0 = c; }
+            else if (kc > k1) { k1 = kc; c1 = c; }
+        }
+        have1 = true;
     }
+    // Key and index of the next-ranked entry, which leaves the ranking.
+    QB_DEV void next(const uint32_t (&key)[NPL], int lane, uint32_t& K, int& j) {
+        K = __reduce_max_sync(0xffffffffu, k0);
+        const unsigned mine = (unsigned)(lane + 32 * c0);
+        j = (int)__reduce_min_sync(0xffffffffu, k0 == K ? mine : 0xFFFFFFFFu);
+        if ((unsigned)j == mine) {
+            removed |= 1u << c0;
+            if (have1) { k0 = k1; c0 = c1; have1 = false; }
+            else scan(key);
+        }
+    }
+    // Key of the next-ranked entry, left in the ranking.
+    QB_DEV uint32_t peek() const { return __reduce_max_sync(0xffffffffu, k0); }
+};
+
+// Descending bitonic sort of one value per lane across the warp.
+template <typename U>
+QB_DEV U warp_sort_desc(U x, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const U o = __shfl_xor_sync(0xffffffffu, x, stride);
+            const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+            x = keep_max ? (x > o ? x : o) : (x < o ? x : o);
+        }
+    }
+    return x;
+}
+
+// (key desc, index asc) as one descending 64-bit order.
+QB_DEV unsigned long long rank_word(uint32_t key, int j) {
+    return ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)j;
+}
+QB_DEV uint32_t rank_word_key(unsigned long long w) { return (uint32_t)(w >> 32); }
+QB_DEV int rank_word_index(unsigned long long w) { return (int)~(uint32_t)w; }
+
+// Fast path of a token's ranking: the first `need` (<= 32) ranked entries,
+// lane r ending with the r-th as a rank word.  The need-th largest of the 32
+// lane maxima is a threshold that at least `need` values reach, so every
+// ranked entry up to `need` is among the values at or above it; when those
+// are at most 32 they are gathered one per lane (through buf, 32 words of
+// this warp's shared memory) and sorted.  Returns false (warp-uniform) when
+// more than 32 values reach the threshold; the caller then ranks by rounds.
+template <int NPL>
+QB_DEV bool warp_top_sorted(const uint32_t (&key)[NPL], int need, int lane, unsigned long long* buf,
+                            unsigned long long& mine) {
+    if (need > 32) return false;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int c = 0; c < NPL; ++c) mx = max(mx, key[c]);
+    const uint32_t sorted_max = warp_sort_desc<uint32_t>(mx, lane);
+    const uint32_t theta = __shfl_sync(0xffffffffu, sorted_max, need - 1);
+    int cnt = 0;
+#pragma unroll
+    for (int c = 0; c < NPL; ++c) cnt += (key[c] != 0u && key[c] >= theta) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total > 32) return false;
+    int pos = incl - cnt;
+#pragma unroll
+    for (int c = 0; c < NPL; ++c)
+        if (key[c] != 0u && key[c] >= theta) buf[pos++] = rank_word(key[c], lane + 32 * c);
+    __syncwarp();
+    const unsigned long long w = lane < total ? buf[lane] : 0ull;
+    __syncwarp();
+    mine = warp_sort_desc<unsigned long long>(w, lane);
+    return true;
 }
 
 template <int NPL>
-QB_DEV void lane_best(const float (&v)[NPL], uint32_t removed, int lane, float& bv, int& bj) {
-    bv = -INFINITY;
-    bj = INT_MAX;
+QB_DEV void biased_keys(const float* __restrict__ s_row, const float (&bj)[NPL], int n, int lane,
+                        float (&sv)[NPL], uint32_t (&key)[NPL]) {
 #pragma unroll
     for (int c = 0; c < NPL; ++c) {
         const int j = lane + 32 * c;
-        if (!((removed >> c) & 1u) && ranks_before(v[c], j, bv, bj)) { bv = v[c]; bj = j; }
+        sv[c] = j < n ? s_row[j] : 0.0f;
+        key[c] = j < n ? value_key(__fadd_rn(sv[c], bj[c])) : 0u;
     }
 }
 
@@ -66,168 +163,311 @@ QB_DEV void lane_best(const float (&v)[NPL], uint32_t removed, int lane, float& 
 // the k-th and (k+1)-th ranked experts; mask_k marks this lane's slots that
 // are in the token's top k.
 template <int NPL>
-QB_DEV void rank_rounds(const float (&v)[NPL], int k, int lane, float& Vk, float& Vk1, uint32_t& mask_k) {
-    uint32_t removed = 0;
-    float bv;
-    int bj;
-    lane_best<NPL>(v, removed, lane, bv, bj);
-    for (int r = 0; r <= k; ++r) {
-        float wv = bv;
-        int wj = bj;
-        warp_best(wv, wj);
-        if (r == k - 1) Vk = wv;
-        if (r == k) { Vk1 = wv; break; }
-        if ((wj & 31) == lane) {
-            removed |= 1u << (wj >> 5);
-            lane_best<NPL>(v, removed, lane, bv, bj);
-        }
-        if (r == k - 1) mask_k = removed;
+QB_DEV void rank_rounds(const uint32_t (&key)[NPL], int k, int lane, unsigned long long* buf, float& Vk, float& Vk1,
+                        uint32_t& mask_k) {
+    unsigned long long w;
+    if (warp_top_sorted<NPL>(key, k + 1, lane, buf, w)) {
+        const unsigned long long wk = __shfl_sync(0xffffffffu, w, k - 1);
+        const unsigned long long wk1 = __shfl_sync(0xffffffffu, w, k);
+        Vk = f32_from_order_key(rank_word_key(wk));
+        Vk1 = f32_from_order_key(rank_word_key(wk1));
+        mask_k = 0;
+#pragma unroll
+        for (int c = 0; c < NPL; ++c)
+            if (key[c] != 0u && rank_word(key[c], lane + 32 * c) >= wk) mask_k |= 1u << c;
+        return;
     }
+    WarpRanker<NPL> rk;
+    rk.scan(key);
+    uint32_t K = 0;
+    int j = 0;
+    for (int r = 0; r < k; ++r) rk.next(key, lane, K, j);
+    Vk = f32_from_order_key(K);
+    Vk1 = f32_from_order_key(rk.peek());
+    mask_k = rk.removed;
 }
 
-template <int NPL>
-__global__ void __launch_bounds__(kTokPassWarps * 32)
-k_token_pass(int T, int n, int k, const float* __restrict__ s, const float* __restrict__ b,
+// Common offset of raw coordinate biases b' (one warp): the pairwise-tree sum
+// of b' (zero-padded to a power of two P; each lane reduces P/32 contiguous
+// leaves, then the lanes combine by halving strides) divided by n.
+QB_DEV float common_offset_warp(const float* __restrict__ raw, int n, int lane) {
+    int P = 1;
+    while (P < n) P <<= 1;
+    const int L = P >= 32 ? P / 32 : 1;     // leaves per lane
+    const int A = P / L;                    // lanes holding a subtree
+    float x = 0.0f;
+    if (lane < A) {
+        float a[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int j = lane * L + i;
+            a[i] = (i < L && j < n) ? raw[j] : 0.0f;
+        }
+#pragma unroll
+        for (int w = 32; w > 1; w >>= 1)
+            if (w <= L)
+#pragma unroll
+                for (int i = 0; i < w / 2; ++i) a[i] = __fadd_rn(a[2 * i], a[2 * i + 1]);
+        x = a[0];
+    }
+    for (int off = 1; off < A; off <<= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, x, off);
+        if ((lane % (2 * off)) == 0) x = __fadd_rn(x, o);
+    }
+    return __fdiv_rn(__shfl_sync(0xffffffffu, x, 0), (float)n);
+}
+
+// Where a kernel takes the biases b from: b' - offset(b') when raw is set,
+// else b (NULL = zeros).  Block 0 also stores the biases it used in out
+// (may be NULL).
+struct BiasArg {
+    const float* b;
+    const float* raw;
+    float* out;
+};
+
+// Stage the n biases in shared memory (sb[QBMOE_MAX_EXPERTS]); ends with a
+// block barrier.
+QB_DEV void stage_bias(const BiasArg& ba, int n, float* sb) {
+    __shared__ float s_off;
+    if (ba.raw) {
+        if (threadIdx.x < 32) {
+            const float c = common_offset_warp(ba.raw, n, threadIdx.x);
+            if (threadIdx.x == 0) s_off = c;
+        }
+        __syncthreads();
+        const float c = s_off;
+        for (int j = threadIdx.x; j < n; j += blockDim.x) sb[j] = __fsub_rn(ba.raw[j], c);
+    } else {
+        for (int j = threadIdx.x; j < n; j += blockDim.x) sb[j] = ba.b ? ba.b[j] : 0.0f;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && ba.out)
+        for (int j = threadIdx.x; j < n; j += blockDim.x) ba.out[j] = sb[j];
+}
+
+// Token pass of a QB sweep: per token, tau_j (the k-th best biased score among
+// the experts other than j) and the margin m_tj = s_tj - tau_j, written
+// transposed [n, T] through a shared-memory tile.  With kFromLogits the
+// scores are computed here from the router logits and stored.
+template <int NPL, bool kFromLogits>
+__global__ void __launch_bounds__(kTokPassWarps * 32, 2)
+k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __restrict__ scores, BiasArg ba,
              float* __restrict__ margins) {
     extern __shared__ float tile[];   // [n][kTokPassTokens + 1]
+    __shared__ unsigned long long rank_buf[kTokPassWarps][32];
+    __shared__ float sb[QBMOE_MAX_EXPERTS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * kTokPassTokens;
     constexpr int LD = kTokPassTokens + 1;
-    float bj_[NPL];
-#pragma unroll
-    for (int c = 0; c < NPL; ++c) {
-        const int j = lane + 32 * c;
-        bj_[c] = j < n ? b[j] : 0.0f;
-    }
+    stage_bias(ba, n, sb);
     for (int tl = warp; tl < kTokPassTokens; tl += kTokPassWarps) {
         const int t = t0 + tl;
         if (t >= T) break;
-        float sv[NPL], v[NPL];
+        float* srow = scores + (size_t)t * n;
+        uint32_t key[NPL];
 #pragma unroll
         for (int c = 0; c < NPL; ++c) {
             const int j = lane + 32 * c;
-            sv[c] = j < n ? s[(size_t)t * n + j] : 0.0f;
-            v[c] = j < n ? __fadd_rn(sv[c], bj_[c]) : -INFINITY;
+            float sc = 0.0f;
+            if (j < n) {
+                if (kFromLogits) {
+                    sc = score_of_logit(logits[(size_t)t * n + j]);
+                    srow[j] = sc;
+                } else {
+                    sc = srow[j];
+                }
+            }
+            key[c] = j < n ? value_key(__fadd_rn(sc, sb[j])) : 0u;
         }
         float Vk = 0.0f, Vk1 = 0.0f;
         uint32_t mask_k = 0;
-        rank_rounds<NPL>(v, k, lane, Vk, Vk1, mask_k);
+        rank_rounds<NPL>(key, k, lane, rank_buf[warp], Vk, Vk1, mask_k);
 #pragma unroll
         for (int c = 0; c < NPL; ++c) {
             const int j = lane + 32 * c;
             if (j < n) {
                 const float tau = ((mask_k >> c) & 1u) ? Vk1 : Vk;
-                float m = __fsub_rn(sv[c], tau);
+                float m = __fsub_rn(srow[j], tau);   // this thread's own score (written above if computed)
                 if (m == 0.0f) m = 0.0f;   // canonical +0
                 tile[j * LD + tl] = m;
             }
         }
     }
     __syncthreads();
-    const int tl = threadIdx.x & 31;
+    // transposed write: each half-warp stores 16 consecutive tokens of one expert
+    const int tl = threadIdx.x & (kTokPassTokens - 1);
     const int t = t0 + tl;
-    for (int j = threadIdx.x >> 5; j < n; j += kTokPassWarps) {
+    constexpr int kRowsPerPass = kTokPassWarps * 32 / kTokPassTokens;
+    for (int j = threadIdx.x / kTokPassTokens; j < n; j += kRowsPerPass) {
         if (t < T) margins[(size_t)j * T + t] = tile[j * LD + tl];
     }
 }
 
-// Radix select of the rank-th smallest descending key (rank 1-based) among
-// keys[0..T).  Descending key = ~order_key(margin): the rank-th smallest
-// descending key is the rank-th largest margin.
-template <bool kSmem>
-QB_DEV uint32_t radix_select(const uint32_t* keys_smem, const float* col, int T, int rank,
-                             unsigned* hist, int* shared_digit, int* shared_rank) {
+// Radix select of the rank-th largest margin of one expert's column: the
+// rank-th smallest descending key (~order_key(margin), rank 1-based), four
+// 8-bit digit passes.  With the column staged in shared memory, the keys of
+// the first pass's chosen bucket are compacted (when they fit kSelectCand
+// words) and the later passes run over them alone.
+struct SelectShared {
+    unsigned hist[256];
+    unsigned wsum[8];
+    int digit, rank, cnt, ncand;
+    uint32_t next;
+    float red[kSelectThreads / 32];
+};
+
+// One digit pass over src[0..count) (keys matching prefix under mask):
+// picks the digit holding rank; leaves the digit, the rank within it and the
+// bucket's size in sh.
+// kFromCol: keys come from the margin column (and are stored to stage[] when
+// stage is set), else from src[] in shared memory.
+template <bool kFromCol>
+QB_DEV void radix_pass(const uint32_t* src, const float* col, uint32_t* stage, int count, uint32_t prefix,
+                       uint32_t mask, int shift, int rank, SelectShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t prefix = 0, mask = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < 256; i += blockDim.x) sh.hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < count; base += blockDim.x) {
+        const int i = base + tid;
+        uint32_t key = 0;
+        bool pred = false;
+        if (i < count) {
+            if (kFromCol) {
+                key = ~f32_order_key(col[i]);
+                if (stage) stage[i] = key;
+            } else {
+                key = src[i];
+            }
+            pred = (key & mask) == prefix;
+        }
+        const unsigned active = __ballot_sync(0xffffffffu, pred);
+        if (pred) {
+            const unsigned digit = (key >> shift) & 0xFFu;
+            const unsigned peers = __match_any_sync(active, digit);
+            if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (unsigned)__popc(peers));
+        }
+    }
+    __syncthreads();
+    // inclusive scan of the 256 bins by warps 0..7 (one bin per thread)
+    if (warp < 8) {
+        const int bin = tid;
+        const unsigned c = sh.hist[bin];
+        unsigned incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) sh.wsum[warp] = incl;
+        __syncwarp();
+        asm volatile("bar.sync 1, 256;");
+        unsigned before = 0;
+        for (int w = 0; w < warp; ++w) before += sh.wsum[w];
+        incl += before;
+        const unsigned excl = incl - c;
+        if ((int)excl < rank && rank <= (int)incl) {
+            sh.digit = bin;
+            sh.rank = rank - (int)excl;
+            sh.cnt = (int)c;
+        }
+    }
+    __syncthreads();
+}
+
+// With kSmem the first pass also stages the keys in keys[0..T); returns the
+// selected key and leaves in sh.ncand the number of compacted candidates at
+// keys + T (0 when the later passes ran over all keys).
+template <bool kSmem>
+QB_DEV uint32_t radix_select(uint32_t* keys, uint32_t* cand, const float* col, int T, int rank,
+                             SelectShared& sh) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    radix_pass<true>(nullptr, col, kSmem ? keys : nullptr, T, 0u, 0u, 24, rank, sh);
+    uint32_t prefix = (uint32_t)sh.digit << 24, mask = 0xFF000000u;
+    rank = sh.rank;
+    const uint32_t* src = keys;
+    int count = T;
+    if (tid == 0) sh.ncand = 0;
+    if (kSmem && sh.cnt <= kSelectCand && sh.cnt < T / 2) {
         __syncthreads();
         for (int base = 0; base < T; base += blockDim.x) {
             const int i = base + tid;
-            uint32_t key = 0;
-            bool pred = false;
-            if (i < T) {
-                key = kSmem ? keys_smem[i] : ~f32_order_key(col[i]);
-                pred = (key & mask) == prefix;
-            }
-            const unsigned active = __ballot_sync(0xffffffffu, pred);
-            if (pred) {
-                const unsigned digit = (key >> shift) & 0xFFu;
-                const unsigned peers = __match_any_sync(active, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (unsigned)__popc(peers));
-            }
+            const uint32_t key = i < T ? keys[i] : 0u;
+            const bool pred = i < T && (key & mask) == prefix;
+            const unsigned bal = __ballot_sync(0xffffffffu, pred);
+            int wbase = 0;
+            if (lane == 0 && bal) wbase = atomicAdd(&sh.ncand, __popc(bal));
+            wbase = __shfl_sync(0xffffffffu, wbase, 0);
+            if (pred) cand[wbase + __popc(bal & ((1u << lane) - 1u))] = key;
         }
         __syncthreads();
-        // inclusive scan of the 256 bins by warps 0..7 (one bin per thread)
-        if (warp < 8) {
-            const int bin = tid;
-            const unsigned c = hist[bin];
-            unsigned incl = c;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            // per-warp totals, combined across the 8 scanning warps
-            __shared__ unsigned wsum[8];
-            if (lane == 31) wsum[warp] = incl;
-            __syncwarp();
-            asm volatile("bar.sync 1, 256;");
-            unsigned before = 0;
-            for (int w = 0; w < warp; ++w) before += wsum[w];
-            incl += before;
-            const unsigned excl = incl - c;
-            if ((int)excl < rank && rank <= (int)incl) {
-                *shared_digit = bin;
-                *shared_rank = rank - (int)excl;
-            }
-        }
-        __syncthreads();
-        prefix |= (uint32_t)(*shared_digit) << shift;
+        src = cand;
+        count = sh.ncand;
+    }
+    for (int shift = 16; shift >= 0; shift -= 8) {
+        if (kSmem) radix_pass<false>(src, col, nullptr, count, prefix, mask, shift, rank, sh);
+        else radix_pass<true>(nullptr, col, nullptr, count, prefix, mask, shift, rank, sh);
+        prefix |= (uint32_t)sh.digit << shift;
         mask |= 0xFFu << shift;
-        rank = *shared_rank;
+        rank = sh.rank;
         __syncthreads();
     }
     return prefix;
 }
 
-// Exact coordinate minimiser of one expert from its T margins `col` (keys
-// staged in SMEM when kSmem): returns -q, q the midpoint of the r-th and
-// (r+1)-th largest margins (r = 0: M_1 + 1; r >= T: M_T - 1).  Result valid
-// in thread 0; every thread of the CTA must call it.
+// Coordinate step of expert j (QB): with margins M (descending) and target
+// load r, the bias is minus the midpoint of M_r and M_{r+1}; r = 0 and r >= T
+// step just past the largest / smallest margin.
 template <bool kSmem>
-QB_DEV float coordinate_bias(int T, int r, const float* col, uint32_t* keys, unsigned* hist, int* s_digit,
-                             int* s_rank, float* red) {
+QB_DEV float coordinate_bias(int T, int r, const float* col, uint32_t* keys, SelectShared& sh) {
     const int tid = threadIdx.x;
-    if (kSmem) {
-        for (int i = tid; i < T; i += blockDim.x) keys[i] = ~f32_order_key(col[i]);
-        __syncthreads();
-    }
     float q = 0.0f;
     if (r <= 0 || r >= T) {
         // max margin (r = 0) or min margin (r >= T)
         const bool want_max = r <= 0;
         float acc = want_max ? -INFINITY : INFINITY;
-        for (int i = tid; i < T; i += blockDim.x) {
-            const float m = kSmem ? f32_from_order_key(~keys[i]) : col[i];
-            acc = want_max ? fmaxf(acc, m) : fminf(acc, m);
-        }
+        for (int i = tid; i < T; i += blockDim.x) acc = want_max ? fmaxf(acc, col[i]) : fminf(acc, col[i]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float o = __shfl_xor_sync(0xffffffffu, acc, off);
             acc = want_max ? fmaxf(acc, o) : fminf(acc, o);
         }
-        if ((tid & 31) == 0) red[tid >> 5] = acc;
+        if ((tid & 31) == 0) sh.red[tid >> 5] = acc;
         __syncthreads();
         if (tid == 0) {
-            float a = red[0];
-            for (int w = 1; w < (int)(blockDim.x / 32); ++w) a = want_max ? fmaxf(a, red[w]) : fminf(a, red[w]);
+            float a = sh.red[0];
+            for (int w = 1; w < (int)(blockDim.x / 32); ++w) a = want_max ? fmaxf(a, sh.red[w]) : fminf(a, sh.red[w]);
             q = want_max ? __fadd_rn(a, 1.0f) : __fsub_rn(a, 1.0f);
         }
         return -q;
     }
-    const uint32_t kr = radix_select<kSmem>(keys, col, T, r, hist, s_digit, s_rank);
-    const uint32_t kr1 = radix_select<kSmem>(keys, col, T, r + 1, hist, s_digit, s_rank);
+    uint32_t* cand = keys + (kSmem ? T : 0);
+    const uint32_t kr = radix_select<kSmem>(keys, cand, col, T, r, sh);
+    // (r+1)-th largest: equal to the r-th when its final bucket holds another
+    // copy, else the next larger descending key: the smallest candidate above
+    // kr when the first digit's bucket holds one (every key outside it is
+    // larger than all of them), else a min pass over all keys.
+    uint32_t kr1 = kr;
+    if (sh.cnt - sh.rank < 1) {
+        const int nc = sh.ncand;
+        for (int round = nc > 0 ? 0 : 1; round < 2; ++round) {
+            const uint32_t* src = round == 0 ? cand : keys;
+            const int count = round == 0 ? nc : T;
+            uint32_t mn = 0xFFFFFFFFu;
+            for (int i = tid; i < count; i += blockDim.x) {
+                const uint32_t key = (kSmem || round == 0) ? src[i] : ~f32_order_key(col[i]);
+                if (key > kr && key < mn) mn = key;
+            }
+            mn = __reduce_min_sync(0xffffffffu, mn);
+            if (tid == 0) sh.next = 0xFFFFFFFFu;
+            __syncthreads();
+            if ((tid & 31) == 0) atomicMin(&sh.next, mn);
+            __syncthreads();
+            kr1 = sh.next;
+            __syncthreads();
+            if (kr1 != 0xFFFFFFFFu) break;
+        }
+    }
     if (tid == 0) {
         const float Mr = f32_from_order_key(~kr);
         const float Mr1 = f32_from_order_key(~kr1);
@@ -236,6 +476,8 @@ QB_DEV float coordinate_bias(int T, int r, const float* col, uint32_t* keys, uns
     return -q;
 }
 
+// Target load r_j: T*k routes split as evenly as possible, the first
+// (T*k mod n) experts taking one more.
 QB_DEV int target_load(int T, int n, int k, int j) {
     const long long total = (long long)T * k;
     return (int)(total / n) + (j < (int)(total % n) ? 1 : 0);
@@ -244,96 +486,54 @@ QB_DEV int target_load(int T, int n, int k, int j) {
 template <bool kSmem>
 __global__ void __launch_bounds__(kSelectThreads)
 k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw) {
-    extern __shared__ uint32_t keys[];
-    __shared__ unsigned hist[256];
-    __shared__ int s_digit, s_rank;
-    __shared__ float red[kSelectThreads / 32];
+    extern __shared__ uint32_t keys[];   // [T] keys, then [min(T, kSelectCand)] candidates
+    __shared__ SelectShared sh;
     const int j = blockIdx.x;
-    const float b = coordinate_bias<kSmem>(T, target_load(T, n, k, j), margins + (size_t)j * T, keys, hist,
-                                           &s_digit, &s_rank, red);
+    const float b = coordinate_bias<kSmem>(T, target_load(T, n, k, j), margins + (size_t)j * T, keys, sh);
     if (threadIdx.x == 0) bias_raw[j] = b;
 }
 
-// b = fl(b' - c), c = fl(tree(b') / n); one warp.  Optionally also writes out2.
-__global__ void k_offset(int n, const float* __restrict__ bias_raw, float* __restrict__ bias_cur,
-                         float* __restrict__ out2) {
-    const int lane = threadIdx.x & 31;
-    int P = 1;
-    while (P < n) P <<= 1;
-    const int L = P >= 32 ? P / 32 : 1;     // leaves per lane
-    const int A = P / L;                    // lanes holding a subtree
-    float a[32];
-    float x = 0.0f;
-    if (lane < A) {
-        for (int i = 0; i < L; ++i) {
-            const int j = lane * L + i;
-            a[i] = j < n ? bias_raw[j] : 0.0f;
-        }
-        for (int w = L; w > 1; w >>= 1)
-            for (int i = 0; i < w / 2; ++i) a[i] = __fadd_rn(a[2 * i], a[2 * i + 1]);
-        x = a[0];
-    }
-    for (int off = 1; off < A; off <<= 1) {
-        const float o = __shfl_down_sync(0xffffffffu, x, off);
-        if ((lane % (2 * off)) == 0) x = __fadd_rn(x, o);
-    }
-    const float sum = __shfl_sync(0xffffffffu, x, 0);
-    const float c = __fdiv_rn(sum, (float)n);
-    for (int j = lane; j < n; j += 32) {
-        const float bj = __fsub_rn(bias_raw[j], c);
-        bias_cur[j] = bj;
-        if (out2) out2[j] = bj;
-    }
-}
 
 template <int NPL>
-__global__ void __launch_bounds__(kTopkWarps * 32)
-k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, const float* __restrict__ b,
-       int32_t* __restrict__ idx, float* __restrict__ w, int* __restrict__ blk_cnt) {
+__global__ void __launch_bounds__(kTopkWarps * 32, 3)
+k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, BiasArg ba, int32_t* __restrict__ idx,
+       float* __restrict__ w, int* __restrict__ blk_cnt) {
     extern __shared__ int cnt[];   // [n]
+    __shared__ unsigned long long rank_buf[kTopkWarps][32];
+    __shared__ float sb[QBMOE_MAX_EXPERTS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int j = threadIdx.x; j < n; j += blockDim.x) cnt[j] = 0;
-    __syncthreads();
+    stage_bias(ba, n, sb);
     float bj_[NPL];
 #pragma unroll
     for (int c = 0; c < NPL; ++c) {
         const int j = lane + 32 * c;
-        bj_[c] = j < n ? b[j] : 0.0f;
+        bj_[c] = j < n ? sb[j] : 0.0f;
     }
     const int blk_tokens = kTopkWarps * tpw;
     const int t0 = blockIdx.x * blk_tokens + warp * tpw;
     for (int q = 0; q < tpw; ++q) {
         const int t = t0 + q;
         if (t >= T) break;
-        float sv[NPL], v[NPL];
-#pragma unroll
-        for (int c = 0; c < NPL; ++c) {
-            const int j = lane + 32 * c;
-            sv[c] = j < n ? s[(size_t)t * n + j] : 0.0f;
-            v[c] = j < n ? __fadd_rn(sv[c], bj_[c]) : -INFINITY;
-        }
-        uint32_t removed = 0;
-        float bv;
-        int bjx;
-        lane_best<NPL>(v, removed, lane, bv, bjx);
+        float sv[NPL];
+        uint32_t key[NPL];
+        biased_keys<NPL>(s + (size_t)t * n, bj_, n, lane, sv, key);
         int my_j = 0;
-        float my_s = 0.0f;
-        for (int r = 0; r < k; ++r) {
-            float wv = bv;
-            int wj = bjx;
-            warp_best(wv, wj);
-            const int owner = wj & 31;
-            float ws = 0.0f;
-            if (owner == lane) {
-#pragma unroll
-                for (int c = 0; c < NPL; ++c)
-                    if (c == (wj >> 5)) ws = sv[c];
-                removed |= 1u << (wj >> 5);
-                lane_best<NPL>(v, removed, lane, bv, bjx);
+        unsigned long long wr;
+        if (warp_top_sorted<NPL>(key, k, lane, rank_buf[warp], wr)) {
+            my_j = rank_word_index(wr);
+        } else {
+            WarpRanker<NPL> rk;
+            rk.scan(key);
+            for (int r = 0; r < k; ++r) {
+                uint32_t K;
+                int wj;
+                rk.next(key, lane, K, wj);
+                if (lane == r) my_j = wj;
             }
-            ws = __shfl_sync(0xffffffffu, ws, owner);
-            if (lane == r) { my_j = wj; my_s = ws; }
         }
+        // weights use the raw (unbiased) scores of the chosen experts
+        const float my_s = lane < k ? s[(size_t)t * n + my_j] : 0.0f;
         float sum = 0.0f;
         for (int r = 0; r < k; ++r) {
             const float sr = __shfl_sync(0xffffffffu, my_s, r);
@@ -346,26 +546,40 @@ k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, const float* _
         }
     }
     __syncthreads();
-    for (int j = threadIdx.x; j < n; j += blockDim.x) blk_cnt[(size_t)blockIdx.x * n + j] = cnt[j];
+    // expert-major [n, nblk]: expert j's counts of all blocks are contiguous
+    for (int j = threadIdx.x; j < n; j += blockDim.x) blk_cnt[(size_t)j * gridDim.x + blockIdx.x] = cnt[j];
 }
 
-// Per expert (one warp each): exclusive prefix of per-block counts (in place)
-// and the expert's load.
+// Per expert (one warp each): exclusive prefix over blocks of the expert's
+// per-block counts (in place, expert-major [n, nblk]) and the expert's load.
+// Each lane takes 8 consecutive blocks of a 256-block chunk, so a chunk's
+// loads are issued together and coalesced.
 __global__ void k_block_scan(int nblk, int n, int* __restrict__ blk_cnt, int32_t* __restrict__ loads) {
     const int lane = threadIdx.x & 31;
     const int j = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (j >= n) return;
+    int* row = blk_cnt + (size_t)j * nblk;
     int running = 0;
-    for (int b0 = 0; b0 < nblk; b0 += 32) {
-        const int bb = b0 + lane;
-        const int v = bb < nblk ? blk_cnt[(size_t)bb * n + j] : 0;
-        int incl = v;
+    for (int b0 = 0; b0 < nblk; b0 += 256) {
+        const int first = b0 + lane * 8;
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = first + i < nblk ? row[first + i] : 0;
+        int tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tot += v[i];
+        int incl = tot;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int o = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += o;
         }
-        if (bb < nblk) blk_cnt[(size_t)bb * n + j] = running + incl - v;
+        int acc = running + incl - tot;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (first + i < nblk) row[first + i] = acc;
+            acc += v[i];
+        }
         running += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0 && loads) loads[j] = running;
@@ -381,29 +595,30 @@ __global__ void k_block_scan(int nblk, int n, int* __restrict__ blk_cnt, int32_t
 // Full top-(k1) list of one token (warp): lane r < k1 ends with the r-th
 // ranked (value, index).
 template <int NPL>
-QB_DEV void top_list(const float (&v)[NPL], int k1, int lane, float& my_v, int& my_j) {
-    uint32_t removed = 0;
-    float bv;
-    int bj;
-    lane_best<NPL>(v, removed, lane, bv, bj);
+QB_DEV void top_list(const uint32_t (&key)[NPL], int k1, int lane, unsigned long long* buf, float& my_v,
+                     int& my_j) {
+    unsigned long long w;
+    if (warp_top_sorted<NPL>(key, k1, lane, buf, w)) {
+        if (lane < k1) { my_v = f32_from_order_key(rank_word_key(w)); my_j = rank_word_index(w); }
+        return;
+    }
+    WarpRanker<NPL> rk;
+    rk.scan(key);
     for (int r = 0; r < k1; ++r) {
-        float wv = bv;
-        int wj = bj;
-        warp_best(wv, wj);
-        if (lane == r) { my_v = wv; my_j = wj; }
-        if ((wj & 31) == lane) {
-            removed |= 1u << (wj >> 5);
-            lane_best<NPL>(v, removed, lane, bv, bj);
-        }
+        uint32_t K;
+        int wj;
+        rk.next(key, lane, K, wj);
+        if (lane == r) { my_v = f32_from_order_key(K); my_j = wj; }
     }
 }
 
 template <int NPL>
-QB_DEV void biased_row(const float* __restrict__ s_row, const float* __restrict__ b, int n, int lane, float (&v)[NPL]) {
+QB_DEV void biased_row(const float* __restrict__ s_row, const float* __restrict__ b, int n, int lane,
+                       uint32_t (&key)[NPL]) {
 #pragma unroll
     for (int c = 0; c < NPL; ++c) {
         const int j = lane + 32 * c;
-        v[c] = j < n ? __fadd_rn(s_row[j], b[j]) : -INFINITY;
+        key[c] = j < n ? value_key(__fadd_rn(s_row[j], b[j])) : 0u;
     }
 }
 
@@ -411,16 +626,17 @@ template <int NPL>
 __global__ void __launch_bounds__(256)
 k_gs_lists(int T, int n, int k, const float* __restrict__ s, const float* __restrict__ b, float* __restrict__ lv,
            int* __restrict__ li, const int* __restrict__ done) {
+    __shared__ unsigned long long rank_buf[8][32];
     if (*done) return;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (t >= T) return;
     const int K1 = k + 1;
-    float v[NPL];
-    biased_row<NPL>(s + (size_t)t * n, b, n, lane, v);
+    uint32_t key[NPL];
+    biased_row<NPL>(s + (size_t)t * n, b, n, lane, key);
     float my_v = 0.0f;
     int my_j = 0;
-    top_list<NPL>(v, K1, lane, my_v, my_j);
+    top_list<NPL>(key, K1, lane, rank_buf[threadIdx.x >> 5], my_v, my_j);
     if (lane < K1) {
         lv[(size_t)t * K1 + lane] = my_v;
         li[(size_t)t * K1 + lane] = my_j;
@@ -431,6 +647,7 @@ template <int NPL>
 __global__ void __launch_bounds__(256)
 k_gs_token(int T, int n, int k, int j, int prev, const float* __restrict__ s, const float* __restrict__ b,
            float* __restrict__ lv, int* __restrict__ li, float* __restrict__ mj, const int* __restrict__ done) {
+    __shared__ unsigned long long rank_buf[8][32];
     if (*done) return;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -444,9 +661,9 @@ k_gs_token(int T, int n, int k, int j, int prev, const float* __restrict__ s, co
         const float lastv = __shfl_sync(0xffffffffu, ev, k);
         const int lastj = __shfl_sync(0xffffffffu, ej, k);
         if (in_list || ranks_before(vn, prev, lastv, lastj)) {
-            float v[NPL];
-            biased_row<NPL>(s + (size_t)t * n, b, n, lane, v);
-            top_list<NPL>(v, K1, lane, ev, ej);
+            uint32_t key[NPL];
+            biased_row<NPL>(s + (size_t)t * n, b, n, lane, key);
+            top_list<NPL>(key, K1, lane, rank_buf[threadIdx.x >> 5], ev, ej);
             if (lane < K1) {
                 lv[(size_t)t * K1 + lane] = ev;
                 li[(size_t)t * K1 + lane] = ej;
@@ -468,11 +685,9 @@ __global__ void __launch_bounds__(kSelectThreads)
 k_gs_select(int T, int n, int k, int j, const float* __restrict__ mj, float* __restrict__ b,
             const int* __restrict__ done) {
     if (*done) return;
-    extern __shared__ uint32_t keys[];
-    __shared__ unsigned hist[256];
-    __shared__ int s_digit, s_rank;
-    __shared__ float red[kSelectThreads / 32];
-    const float bj = coordinate_bias<kSmem>(T, target_load(T, n, k, j), mj, keys, hist, &s_digit, &s_rank, red);
+    extern __shared__ uint32_t keys[];   // [T] keys, then [min(T, kSelectCand)] candidates
+    __shared__ SelectShared sh;
+    const float bj = coordinate_bias<kSmem>(T, target_load(T, n, k, j), mj, keys, sh);
     if (threadIdx.x == 0) b[j] = bj;
 }
 
@@ -561,31 +776,37 @@ int dispatch_npl(int npl, Args... args) {
 
 template <int NPL>
 struct TokenPassLaunch {
-    static int run(int T, int n, int k, const float* s, const float* b, float* margins, cudaStream_t st) {
+    static int run(int T, int n, int k, const float* logits, float* scores, BiasArg ba, float* margins,
+                   cudaStream_t st) {
         const size_t smem = (size_t)n * (kTokPassTokens + 1) * sizeof(float);
-        auto kern = k_token_pass<NPL>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        auto kern = logits ? k_token_pass<NPL, true> : k_token_pass<NPL, false>;
+        // the largest shared-memory carveout lets several tiles share an SM
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return QBMOE_ECUDA;
         const int grid = (T + kTokPassTokens - 1) / kTokPassTokens;
-        kern<<<grid, kTokPassWarps * 32, smem, st>>>(T, n, k, s, b, margins);
+        kern<<<grid, kTokPassWarps * 32, smem, st>>>(T, n, k, logits, scores, ba, margins);
         return qbh::cuda_err(cudaGetLastError());
     }
 };
 
 template <int NPL>
 struct TopkLaunch {
-    static int run(int T, int n, int k, int tpw, const float* s, const float* b, int32_t* idx, float* w,
+    static int run(int T, int n, int k, int tpw, const float* s, BiasArg ba, int32_t* idx, float* w,
                    int* blk_cnt, cudaStream_t st) {
         const size_t smem = (size_t)n * sizeof(int);
         const int grid = (T + kTopkWarps * tpw - 1) / (kTopkWarps * tpw);
-        k_topk<NPL><<<grid, kTopkWarps * 32, smem, st>>>(T, n, k, tpw, s, b, idx, w, blk_cnt);
+        k_topk<NPL><<<grid, kTopkWarps * 32, smem, st>>>(T, n, k, tpw, s, ba, idx, w, blk_cnt);
         return qbh::cuda_err(cudaGetLastError());
     }
 };
 
+size_t select_smem_bytes(int T) { return (size_t)(T + std::min(T, kSelectCand)) * sizeof(uint32_t); }
+
 int launch_select(int T, int n, int k, const float* margins, float* bias_raw, cudaStream_t st) {
     if (T <= kSelectSmemMaxT) {
-        const size_t smem = (size_t)T * sizeof(uint32_t);
+        const size_t smem = select_smem_bytes(T);
         if (cudaFuncSetAttribute(k_expert_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)std::max<size_t>(smem, 1)) != cudaSuccess)
             return QBMOE_ECUDA;
@@ -601,16 +822,17 @@ int launch_select(int T, int n, int k, const float* margins, float* bias_raw, cu
 namespace qbh {
 
 int route_tokens_per_warp(int T) {
-    const int per = (T + kTopkWarps * 304 - 1) / (kTopkWarps * 304);
+    // about four 8-warp CTAs per SM before a warp takes a second token
+    const int per = (T + kTopkWarps * 608 - 1) / (kTopkWarps * 608);
     return std::min(8, std::max(1, per));
 }
 
 size_t route_ws_layout(int T, int n, int k, RouteBuffers* rb, void* base) {
     (void)k;
     // Per-block count rows for any T' <= T: tokens_per_warp(T') is 1 while
-    // T' <= 8*304 (then at most ceil(T'/8) blocks, never more than 304),
-    // between 2 and 7 (at most 304 blocks), or 8 (ceil(T'/64) blocks).
-    const int nblk = std::max(std::min((T + 7) / 8, 304), (T + 63) / 64);
+    // T' <= 8*608 (then at most ceil(T'/8) blocks, never more than 608),
+    // between 2 and 7 (at most 608 blocks), or 8 (ceil(T'/64) blocks).
+    const int nblk = std::max(std::min((T + 7) / 8, 608), (T + 63) / 64);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -619,13 +841,11 @@ size_t route_ws_layout(int T, int n, int k, RouteBuffers* rb, void* base) {
     };
     const size_t o_m = take((size_t)n * T * sizeof(float));
     const size_t o_raw = take((size_t)n * sizeof(float));
-    const size_t o_cur = take((size_t)n * sizeof(float));
     const size_t o_cnt = take((size_t)nblk * n * sizeof(int));
     if (rb && base) {
         char* p = static_cast<char*>(base);
         rb->margins = reinterpret_cast<float*>(p + o_m);
         rb->bias_raw = reinterpret_cast<float*>(p + o_raw);
-        rb->bias_cur = reinterpret_cast<float*>(p + o_cur);
         rb->blk_cnt = reinterpret_cast<int*>(p + o_cnt);
     }
     return off;
@@ -641,34 +861,27 @@ int launch_scores(const float* logits, float* scores, long long count, cudaStrea
 }
 
 // QB sweeps (if any) then the final top-k.  bias_in may be NULL (zeros).
-int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* scores, const float* bias_in,
+// With logits set, the scores are computed from them first (inside the first
+// token pass when there is a sweep).
+int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* logits, float* scores, const float* bias_in,
                        float* bias_out, int32_t* idx, float* w, int* blk_cnt, const RouteBuffers& rb,
                        cudaStream_t s, int* nl) {
     const int npl = npl_for(n);
     if (npl < 0) return QBMOE_EINVAL;
-    const float* b = bias_in;
-    if (!b) {
-        if (cudaMemsetAsync(rb.bias_cur, 0, (size_t)n * sizeof(float), s) != cudaSuccess) return QBMOE_ECUDA;
-        b = rb.bias_cur;
-    }
     int rc;
+    if (logits && sweeps == 0 && (rc = launch_scores(logits, scores, (long long)T * n, s, nl))) return rc;
+    BiasArg ba{bias_in, nullptr, nullptr};
     for (int it = 0; it < sweeps; ++it) {
-        rc = dispatch_npl<TokenPassLaunch>(npl, T, n, k, scores, b, rb.margins, s);
+        rc = dispatch_npl<TokenPassLaunch>(npl, T, n, k, it == 0 ? logits : nullptr, scores, ba, rb.margins, s);
         if (rc) return rc;
         rc = launch_select(T, n, k, rb.margins, rb.bias_raw, s);
         if (rc) return rc;
-        const bool last = it == sweeps - 1;
-        k_offset<<<1, 32, 0, s>>>(n, rb.bias_raw, rb.bias_cur, last ? bias_out : nullptr);
-        if ((rc = cuda_err(cudaGetLastError()))) return rc;
-        b = rb.bias_cur;
-        if (nl) *nl += 3;
+        ba = BiasArg{nullptr, rb.bias_raw, nullptr};
+        if (nl) *nl += 2;
     }
-    if (sweeps == 0 && bias_out && bias_out != b) {
-        if (cudaMemcpyAsync(bias_out, b, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-            return QBMOE_ECUDA;
-    }
+    ba.out = bias_out;
     const int tpw = route_tokens_per_warp(T);
-    rc = dispatch_npl<TopkLaunch>(npl, T, n, k, tpw, scores, b, idx, w, blk_cnt, s);
+    rc = dispatch_npl<TopkLaunch>(npl, T, n, k, tpw, scores, ba, idx, w, blk_cnt, s);
     if (nl) ++*nl;
     return rc;
 }
@@ -715,9 +928,8 @@ extern "C" int moe_route_qb(int T, int n, int k, int qb_sweeps, const float* log
     qbh::RouteBuffers rb;
     qbh::route_ws_layout(T, n, k, &rb, workspace);
     int nl = 0;
-    rc = qbh::launch_scores(logits, scores, (long long)T * n, s, &nl);
-    if (!rc) rc = qbh::launch_qb_and_topk(T, n, k, qb_sweeps, scores, bias_in, bias_out, topk_idx, topk_w,
-                                          rb.blk_cnt, rb, s, &nl);
+    rc = qbh::launch_qb_and_topk(T, n, k, qb_sweeps, logits, scores, bias_in, bias_out, topk_idx, topk_w,
+                                 rb.blk_cnt, rb, s, &nl);
     if (!rc) rc = qbh::launch_loads_from_counts(T, n, qbh::route_tokens_per_warp(T), rb.blk_cnt, loads, s, &nl);
     g_route_launches = nl;
     return rc;
@@ -797,7 +1009,7 @@ extern "C" int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_whe
     if (cudaMemsetAsync(gb.done, 0, sizeof(int), s) != cudaSuccess) return QBMOE_ECUDA;
     if (sweeps_done && cudaMemsetAsync(sweeps_done, 0, sizeof(int32_t), s) != cudaSuccess) return QBMOE_ECUDA;
     const bool smem_sel = T <= kSelectSmemMaxT;
-    const size_t sel_smem = smem_sel ? (size_t)T * sizeof(uint32_t) : 0;
+    const size_t sel_smem = smem_sel ? select_smem_bytes(T) : 0;
     if (smem_sel && cudaFuncSetAttribute(k_gs_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)std::max<size_t>(sel_smem, 1)) != cudaSuccess)
         return QBMOE_ECUDA;
@@ -817,7 +1029,7 @@ extern "C" int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_whe
         k_gs_offset<<<1, 32, 0, s>>>(n, gb.b, gb.done);
         if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
         // loads under the new biases, for the sweep count and the balance test
-        if ((rc = qbh::launch_qb_and_topk(T, n, k, 0, scores, gb.b, nullptr, topk_idx, topk_w, rb.blk_cnt, rb, s,
+        if ((rc = qbh::launch_qb_and_topk(T, n, k, 0, nullptr, scores, gb.b, nullptr, topk_idx, topk_w, rb.blk_cnt, rb, s,
                                           &nl)))
             return rc;
         if ((rc = qbh::launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, &nl))) return rc;
@@ -825,7 +1037,7 @@ extern "C" int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_whe
         if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
     }
     // final routing with the final biases
-    rc = qbh::launch_qb_and_topk(T, n, k, 0, scores, gb.b, bias_out, topk_idx, topk_w, rb.blk_cnt, rb, s, &nl);
+    rc = qbh::launch_qb_and_topk(T, n, k, 0, nullptr, scores, gb.b, bias_out, topk_idx, topk_w, rb.blk_cnt, rb, s, &nl);
     if (!rc) rc = qbh::launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, &nl);
     return rc;
 }

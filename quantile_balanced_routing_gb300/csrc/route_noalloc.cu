@@ -67,14 +67,11 @@ extern "C" int moe_route_qb_noalloc(int T, int n, int k, int qb_sweeps, const fl
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     qbh::RouteBuffers rb;
     qbh::route_ws_layout(T, n, k, &rb, scratch);
-    // Every scratch region is fully written before it is read (bias_cur is
-    // cleared below when bias_in is NULL), so stale contents from an earlier
-    // call cannot leak into this one.
+    // Every scratch region is fully written before it is read, so stale
+    // contents from an earlier call cannot leak into this one.
     int nl = 0;
-    rc = qbh::launch_scores(logits, scores, (long long)T * n, s, &nl);
-    if (!rc)
-        rc = qbh::launch_qb_and_topk(T, n, k, qb_sweeps, scores, bias_in, bias_out, topk_idx, topk_w, rb.blk_cnt, rb,
-                                     s, &nl);
+    rc = qbh::launch_qb_and_topk(T, n, k, qb_sweeps, logits, scores, bias_in, bias_out, topk_idx, topk_w,
+                                 rb.blk_cnt, rb, s, &nl);
     if (!rc) rc = qbh::launch_loads_from_counts(T, n, qbh::route_tokens_per_warp(T), rb.blk_cnt, loads, s, &nl);
     return rc;
 }
