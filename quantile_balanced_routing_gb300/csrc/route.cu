@@ -33,8 +33,8 @@ namespace {
 
 using namespace qb;
 
-constexpr int kTokPassTokens = 16;   // tokens per CTA in the token pass (one per warp)
-constexpr int kTokPassWarps = 16;
+constexpr int kTokPassTokens = 8;    // tokens per CTA in the token pass (one per warp)
+constexpr int kTokPassWarps = 8;
 constexpr int kTopkWarps = 8;
 constexpr int kSelectThreads = 512;
 constexpr int kSelectSmemMaxT = 48 * 1024;   // margins staged in SMEM up to this T
@@ -148,17 +148,6 @@ QB_DEV bool warp_top_sorted(const uint32_t (&key)[NPL], int need, int lane, unsi
     return true;
 }
 
-template <int NPL>
-QB_DEV void biased_keys(const float* __restrict__ s_row, const float (&bj)[NPL], int n, int lane,
-                        float (&sv)[NPL], uint32_t (&key)[NPL]) {
-#pragma unroll
-    for (int c = 0; c < NPL; ++c) {
-        const int j = lane + 32 * c;
-        sv[c] = j < n ? s_row[j] : 0.0f;
-        key[c] = j < n ? value_key(__fadd_rn(sv[c], bj[c])) : 0u;
-    }
-}
-
 // One token's ranking rounds (warp-uniform): V_k and V_{k+1} are the values of
 // the k-th and (k+1)-th ranked experts; mask_k marks this lane's slots that
 // are in the token's top k.
@@ -251,34 +240,39 @@ QB_DEV void stage_bias(const BiasArg& ba, int n, float* sb) {
 // transposed [n, T] through a shared-memory tile.  With kFromLogits the
 // scores are computed here from the router logits and stored.
 template <int NPL, bool kFromLogits>
-__global__ void __launch_bounds__(kTokPassWarps * 32, 2)
+__global__ void __launch_bounds__(kTokPassWarps * 32, 4)
 k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __restrict__ scores, BiasArg ba,
              float* __restrict__ margins) {
-    extern __shared__ float tile[];   // [n][kTokPassTokens + 1]
+    extern __shared__ float tile[];   // [n][kTokPassTokens + 1]: scores, then margins
     __shared__ unsigned long long rank_buf[kTokPassWarps][32];
     __shared__ float sb[QBMOE_MAX_EXPERTS];
+    static_assert(kTokPassTokens == kTokPassWarps, "one token per warp");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * kTokPassTokens;
     constexpr int LD = kTokPassTokens + 1;
+    const int tl = warp;
+    const int t = t0 + tl;
+    // the token's row is requested before the biases are staged
+    const float* src = kFromLogits ? logits + (size_t)t * n : scores + (size_t)t * n;
+    float x[NPL];
+#pragma unroll
+    for (int c = 0; c < NPL; ++c) {
+        const int j = lane + 32 * c;
+        x[c] = (t < T && j < n) ? src[j] : 0.0f;
+    }
     stage_bias(ba, n, sb);
-    for (int tl = warp; tl < kTokPassTokens; tl += kTokPassWarps) {
-        const int t = t0 + tl;
-        if (t >= T) break;
-        float* srow = scores + (size_t)t * n;
+    if (t < T) {
         uint32_t key[NPL];
 #pragma unroll
         for (int c = 0; c < NPL; ++c) {
             const int j = lane + 32 * c;
-            float sc = 0.0f;
+            key[c] = 0u;
             if (j < n) {
-                if (kFromLogits) {
-                    sc = score_of_logit(logits[(size_t)t * n + j]);
-                    srow[j] = sc;
-                } else {
-                    sc = srow[j];
-                }
+                const float sc = kFromLogits ? score_of_logit(x[c]) : x[c];
+                if (kFromLogits) scores[(size_t)t * n + j] = sc;
+                tile[j * LD + tl] = sc;   // kept for the margin below
+                key[c] = value_key(__fadd_rn(sc, sb[j]));
             }
-            key[c] = j < n ? value_key(__fadd_rn(sc, sb[j])) : 0u;
         }
         float Vk = 0.0f, Vk1 = 0.0f;
         uint32_t mask_k = 0;
@@ -288,19 +282,20 @@ k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __res
             const int j = lane + 32 * c;
             if (j < n) {
                 const float tau = ((mask_k >> c) & 1u) ? Vk1 : Vk;
-                float m = __fsub_rn(srow[j], tau);   // this thread's own score (written above if computed)
+                float m = __fsub_rn(tile[j * LD + tl], tau);
                 if (m == 0.0f) m = 0.0f;   // canonical +0
                 tile[j * LD + tl] = m;
             }
         }
     }
     __syncthreads();
-    // transposed write: each half-warp stores 16 consecutive tokens of one expert
-    const int tl = threadIdx.x & (kTokPassTokens - 1);
-    const int t = t0 + tl;
+    // transposed write: each group of kTokPassTokens threads stores one
+    // expert's consecutive tokens
+    const int wl = threadIdx.x % kTokPassTokens;
+    const int wt = t0 + wl;
     constexpr int kRowsPerPass = kTokPassWarps * 32 / kTokPassTokens;
     for (int j = threadIdx.x / kTokPassTokens; j < n; j += kRowsPerPass) {
-        if (t < T) margins[(size_t)j * T + t] = tile[j * LD + tl];
+        if (wt < T) margins[(size_t)j * T + wt] = tile[j * LD + wl];
     }
 }
 
@@ -503,21 +498,32 @@ k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, BiasArg ba, in
     __shared__ float sb[QBMOE_MAX_EXPERTS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int j = threadIdx.x; j < n; j += blockDim.x) cnt[j] = 0;
-    stage_bias(ba, n, sb);
-    float bj_[NPL];
+    const int blk_tokens = kTopkWarps * tpw;
+    const int t0 = blockIdx.x * blk_tokens + warp * tpw;
+    // the first token's row is requested before the biases are staged
+    float x[NPL];
 #pragma unroll
     for (int c = 0; c < NPL; ++c) {
         const int j = lane + 32 * c;
-        bj_[c] = j < n ? sb[j] : 0.0f;
+        x[c] = (t0 < T && j < n) ? s[(size_t)t0 * n + j] : 0.0f;
     }
-    const int blk_tokens = kTopkWarps * tpw;
-    const int t0 = blockIdx.x * blk_tokens + warp * tpw;
+    stage_bias(ba, n, sb);
     for (int q = 0; q < tpw; ++q) {
         const int t = t0 + q;
         if (t >= T) break;
-        float sv[NPL];
+        if (q > 0) {
+#pragma unroll
+            for (int c = 0; c < NPL; ++c) {
+                const int j = lane + 32 * c;
+                x[c] = j < n ? s[(size_t)t * n + j] : 0.0f;
+            }
+        }
         uint32_t key[NPL];
-        biased_keys<NPL>(s + (size_t)t * n, bj_, n, lane, sv, key);
+#pragma unroll
+        for (int c = 0; c < NPL; ++c) {
+            const int j = lane + 32 * c;
+            key[c] = j < n ? value_key(__fadd_rn(x[c], sb[j])) : 0u;
+        }
         int my_j = 0;
         unsigned long long wr;
         if (warp_top_sorted<NPL>(key, k, lane, rank_buf[warp], wr)) {
