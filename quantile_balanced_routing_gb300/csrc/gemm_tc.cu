@@ -33,6 +33,7 @@
 #include "tc_ptx.cuh"
 
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 #include <cstring>
@@ -46,6 +47,10 @@ constexpr int kProdAWarp = 0, kProdBWarp = 1, kMmaWarp = 2, kEpiFirstWarp = 3, k
 constexpr int kThreads = (kEpiFirstWarp + 4) * 32;     // 224
 constexpr int kConvWarps = 8;                          // MXFP4 converter warps (two threads per weight row)
 constexpr int kThreadsMx = (kConvFirstWarp + kConvWarps) * 32;  // 480
+constexpr int kSfWarps = 4;                            // block-scaled MXFP4: scale writers, one per TMEM lane quarter
+constexpr int kThreadsMxS = (kConvFirstWarp + kSfWarps) * 32;   // 352
+constexpr int kBKS = 128;                      // block-scaled: K elements per stage (128 bytes of E4M3 per row)
+constexpr int kScaleGroupS = 4;                // block-scaled: stages per E8M0 scale load (16 scale bytes per row)
 constexpr int kBK = 64;                        // K elements per block (128 bytes of bf16)
 constexpr int kATileBytes = 128 * kBK * 2;     // 16 KB
 constexpr int kPackBytes = 128 * kBK / 2;              // packed E2M1 bytes of one 128 x 64 weight block
@@ -58,13 +63,31 @@ constexpr long long kDrainWait = 1LL << 12;    // polls per stage when draining 
 
 enum { SUB_STORE = 0, SUB_ROUTER = 1, SUB_SITU = 2 };
 
+// Kernel modes: bf16 weights; MXFP4 weights decoded to bf16 in SMEM by
+// converter warps (kind::f16 MMA); MXFP4 weights fed to the block-scaled MMA
+// (kind::mxf8f6f4) with E4M3 tokens.
+enum { MODE_BF16 = 0, MODE_MX_DECODE = 1, MODE_MX_SCALED = 2 };
+
+// Block-scaled MMAs take fp8 tokens, so a bf16 activation a enters as two
+// E4M3 terms, a = hi + lo / 16 with hi = e4m3(a) and lo = e4m3(16 (a - hi)),
+// multiplied with the token scales 2^0 and 2^-4.  For bf16 a with
+// 2^-6 <= |a| <= 448 both terms are exact (the residual has at most four
+// significant bits), so the product is that of the bf16 activation; smaller
+// magnitudes keep an absolute error below 2^-14 and larger ones saturate.
+constexpr int kLoShift = 4;
+__device__ __forceinline__ void e4m3_pair(float a, uint8_t& hi, uint8_t& lo) {
+    hi = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
+    const float h = __half2float(__half(__nv_cvt_fp8_to_halfraw(hi, __NV_E4M3)));
+    lo = __nv_cvt_float_to_fp8(__fmul_rn(__fsub_rn(a, h), float(1 << kLoShift)), __NV_SATFINITE, __NV_E4M3);
+}
+
 struct SubGemm {
     int epi;
     int F;              // output features (rows of W per group)
     int m_tiles;        // tiles over F (128 rows, or 64 features for SITU)
     int m_begin;        // first global m index of this sub-GEMM
     int k_split;        // K blocks read from a0; the rest from a1 (ignored for SITU)
-    int pad;
+    int out_e4m3;       // SITU output stored as an E4M3 pair (hi bytes at column f, lo at F + f)
     void* out;
     long long ldo;
     const float* col_bias;
@@ -188,19 +211,33 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
             }
         } else {
             // SITU: 16 tokens x 8 groups of 8 features, gate rows 0..63, up rows 64..127
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
             const int j = et >> 3, fg = et & 7;
             const int f = f_base + fg * 8;
             if (j < tok_left && f < sg.F) {
-                __align__(16) __nv_bfloat16 o[8];
+                float a[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const float g = st[(fg * 8 + u) * kStLd + j];
                     const float up = st[(64 + fg * 8 + u) * kStLd + j];
-                    o[u] = __float2bfloat16_rn(situ_glu(g, up, p.beta1, p.beta2));
+                    a[u] = situ_glu(g, up, p.beta1, p.beta2);
                 }
-                *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
-                    *reinterpret_cast<const uint4*>(o);
+                const long long off = (long long)(ti.row0 + c0 + j) * sg.ldo + f;
+                if (sg.out_e4m3) {
+                    // the bf16 activation as an E4M3 pair: hi plane, then lo plane F bytes on
+                    __align__(8) uint8_t oh[8];
+                    __align__(8) uint8_t ol[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) e4m3_pair(__bfloat162float(__float2bfloat16_rn(a[u])), oh[u], ol[u]);
+                    uint8_t* o8 = static_cast<uint8_t*>(sg.out) + off;
+                    *reinterpret_cast<uint2*>(o8) = *reinterpret_cast<const uint2*>(oh);
+                    *reinterpret_cast<uint2*>(o8 + sg.F) = *reinterpret_cast<const uint2*>(ol);
+                } else {
+                    __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(a[u]);
+                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sg.out) + off) =
+                        *reinterpret_cast<const uint4*>(o);
+                }
             }
         }
     }
@@ -244,10 +281,25 @@ __device__ __forceinline__ void mx_decode_word(uint32_t w, const uint32_t (&h)[2
     for (int q = 0; q < 4; ++q) o[q] |= __byte_perm(w, w4, (q << 12) | ((4 + q) << 4)) & 0x80008000u;
 }
 
-template <int BN, int S, bool MX>
-__global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const __grid_constant__ TcParams p) {
-    constexpr int kBBytes = BN * kBK * 2;
-    constexpr uint32_t kCols = (2 * BN <= 32) ? 32 : (2 * BN <= 128 ? 128 : 512);   // two accumulators, power of two
+template <int MODE>
+constexpr int threads_of() {
+    return MODE == MODE_MX_DECODE ? kThreadsMx : (MODE == MODE_MX_SCALED ? kThreadsMxS : kThreads);
+}
+constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
+
+template <int BN, int S, int MODE>
+__global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_constant__ TcParams p) {
+    constexpr bool MX = MODE == MODE_MX_DECODE;    // MXFP4 decoded to bf16 by converter warps
+    constexpr bool MXS = MODE == MODE_MX_SCALED;   // MXFP4 on the block-scaled MMA, E4M3 tokens
+    constexpr int kKS = MXS ? kBKS : kBK;          // K elements per stage
+    constexpr int kPlane = BN * 128;               // token tile: BN rows of 128 bytes
+    constexpr int kBBytes = MXS ? 2 * kPlane : kPlane;   // block-scaled: hi and lo planes
+    // TMEM columns: two accumulators (2 x BN); block-scaled adds the token
+    // scales (8 columns of 2^0 for hi, 8 of 2^-4 for lo) and a 4-column
+    // weight-scale slot per stage.
+    constexpr int kSfbCol = 2 * BN, kSfaCol = 2 * BN + 16;
+    constexpr uint32_t kCols = MXS ? pow2_cols(kSfaCol + 4 * S) : pow2_cols(2 * BN);
+    static_assert(!MXS || kSfaCol + 4 * S <= 512, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // S stages, each a 16 KB weight tile and a BN-row token tile that share
@@ -259,12 +311,12 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
     uint8_t* b_ring = smem + S * kATileBytes;
     uint8_t* p_ring = b_ring + S * kBBytes;
     uint8_t* sc_ring = p_ring + (MX ? S * kPackBytes : 0);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sc_ring + (MX ? 2 * kScaleBytes : 0));
+    uint64_t* full = reinterpret_cast<uint64_t*>(sc_ring + (MX || MXS ? 2 * kScaleBytes : 0));
     uint64_t* empty = full + S;
-    uint64_t* fullP = empty + S;                 // MX: packed block landed
-    uint64_t* fullS = fullP + (MX ? S : 0);      // MX: scale group landed
-    uint64_t* emptyS = fullS + (MX ? 2 : 0);     // MX: scale group consumed
-    uint64_t* accf = emptyS + (MX ? 2 : 0);
+    uint64_t* fullP = empty + S;                       // MX: packed block landed
+    uint64_t* fullS = fullP + (MX ? S : 0);            // MX, MXS: scale group landed
+    uint64_t* emptyS = fullS + (MX || MXS ? 2 : 0);    // MX, MXS: scale group consumed
+    uint64_t* accf = emptyS + (MX || MXS ? 2 : 0);
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -284,15 +336,16 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            // token producer + weight producer (bf16) or + the converter warps (MXFP4)
-            tc::mbar_init(&full[s], MX ? 1 + kConvWarps : 2);
+            // token producer + weight producer (bf16), + the converter warps
+            // (MXFP4 decode) or + the scale writers (block-scaled)
+            tc::mbar_init(&full[s], MX ? 1 + kConvWarps : (MXS ? 2 + kSfWarps : 2));
             tc::mbar_init(&empty[s], 1);   // one MMA commit per stage
             if (MX) tc::mbar_init(&fullP[s], 1);
         }
-        if (MX) {
+        if (MX || MXS) {
             for (int g = 0; g < 2; ++g) {
                 tc::mbar_init(&fullS[g], 1);
-                tc::mbar_init(&emptyS[g], kConvWarps);
+                tc::mbar_init(&emptyS[g], MX ? kConvWarps : kSfWarps);
             }
         }
         for (int a = 0; a < 2; ++a) {
@@ -341,11 +394,14 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
                         *abort_flag = 1;
                         break;
                     }
-                    if (MX && is_a) {
-                        // packed E2M1 block (and, every kScaleGroup blocks, the scales) for the converters
+                    if ((MX || MXS) && is_a) {
+                        // MX: packed E2M1 block for the converters; MXS: E2M1
+                        // tile unpacked by TMA into the stage.  Every sgrp K
+                        // blocks also the E8M0 scales (16 bytes per row).
                         const bool situ = sg.epi == SUB_SITU;
                         const int y = ti.g * sg.F + ti.mt * (situ ? 64 : 128);
-                        if (kb % kScaleGroup == 0) {
+                        constexpr int sgrp = MX ? kScaleGroup : kScaleGroupS;
+                        if (kb % sgrp == 0) {
                             const int slot = gidx & 1;
                             if (!tc::mbar_wait(&emptyS[slot], ((gidx >> 1) & 1) ^ 1u, lim)) {
                                 set_status(p.status, QBMOE_ETIMEOUT);
@@ -354,7 +410,7 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
                             }
                             uint8_t* SC = sc_ring + slot * kScaleBytes;
                             tc::mbar_expect_tx(&fullS[slot], kScaleBytes);
-                            const int xs = (kb / kScaleGroup) * 16;
+                            const int xs = (kb / sgrp) * 16;
                             if (situ) {
                                 tc::tma_load_2d(SC, &p.sc0, &fullS[slot], xs, y);
                                 tc::tma_load_2d(SC + kScaleBytes / 2, &p.sc1, &fullS[slot], xs, y);
@@ -365,13 +421,26 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
                             sc_par = (sc_par & ~(1u << slot)) | (((gidx >> 1) & 1u) << slot);
                             ++gidx;
                         }
-                        uint8_t* PK = p_ring + s * kPackBytes;
-                        tc::mbar_expect_tx(&fullP[s], kPackBytes);
-                        if (situ) {
-                            tc::tma_load_2d(PK, &p.a0[ti.sub], &fullP[s], kb * (kBK / 2), y);
-                            tc::tma_load_2d(PK + kPackBytes / 2, &p.a1[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                        if (MX) {
+                            uint8_t* PK = p_ring + s * kPackBytes;
+                            tc::mbar_expect_tx(&fullP[s], kPackBytes);
+                            if (situ) {
+                                tc::tma_load_2d(PK, &p.a0[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                                tc::tma_load_2d(PK + kPackBytes / 2, &p.a1[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                            } else {
+                                tc::tma_load_2d(PK, &p.a0[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                            }
                         } else {
-                            tc::tma_load_2d(PK, &p.a0[ti.sub], &fullP[s], kb * (kBK / 2), y);
+                            // 128 rows x 128 codes, each 16-code chunk landing as 8 bytes + 8 unused;
+                            // the transaction counts the 8 KB of packed codes read
+                            uint8_t* A = a_ring + s * kATileBytes;
+                            tc::mbar_expect_tx(&full[s], kATileBytes / 2);
+                            if (situ) {
+                                tc::tma_load_2d(A, &p.a0[ti.sub], &full[s], kb * kBKS, y);
+                                tc::tma_load_2d(A + kATileBytes / 2, &p.a1[ti.sub], &full[s], kb * kBKS, y);
+                            } else {
+                                tc::tma_load_2d(A, &p.a0[ti.sub], &full[s], kb * kBKS, y);
+                            }
                         }
                     } else if (is_a) {
                         uint8_t* A = a_ring + s * kATileBytes;
@@ -389,14 +458,18 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
                         }
                     } else {
                         uint8_t* B = b_ring + s * kBBytes;
-                        tc::mbar_expect_tx(&fullx[s], n_eff * kBK * 2);
+                        tc::mbar_expect_tx(&fullx[s], (MXS ? 2 : 1) * n_eff * 128);
                         // n_eff rows as a sum of power-of-two boxes (largest first): <= 5 TMA issues
+                        // per plane (block-scaled: hi columns kb * 128, lo columns K + kb * 128)
                         int r = 0;
 #pragma unroll
                         for (int i = 5; i >= 1; --i) {
                             const int h = 8 << i;
                             if (h <= BN && (n_eff - r) >= h) {
-                                tc::tma_load_2d(B + r * kBK * 2, &p.bx[i], &fullx[s], kb * kBK, ti.row0 + r);
+                                tc::tma_load_2d(B + r * 128, &p.bx[i], &fullx[s], kb * kKS, ti.row0 + r);
+                                if (MXS)
+                                    tc::tma_load_2d(B + kPlane + r * 128, &p.bx[i], &fullx[s], (p.nkb + kb) * kKS,
+                                                    ti.row0 + r);
                                 r += h;
                             }
                         }
@@ -484,6 +557,59 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
             if (!ok || stop) break;
         }
         __syncthreads();
+    } else if (MXS && warp >= kConvFirstWarp) {
+        // ------------------------------------------------- weight scales -> TMEM
+        // Warp w writes TMEM lane quarter w % 4.  A stage's scale words (four
+        // E8M0 bytes per weight row, one per 32-wide K slice) go to its
+        // 4-column slot in the layout the block-scaled MMA reads for M = 128:
+        // in every lane quarter, lane i column j holds row i + 32 j.  The
+        // token scales are constant, written once: 8 columns of 0x7F bytes
+        // (2^0, hi plane) and 8 of 0x7B bytes (2^-4, lo plane).
+        const int q = warp & 3;
+        const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
+        constexpr uint32_t kSfHi = 0x7F7F7F7Fu, kSfLo = 0x01010101u * (127 - kLoShift);
+        tc::tmem_st4(tbase + lanes + kSfbCol, kSfHi, kSfHi, kSfHi, kSfHi);
+        tc::tmem_st4(tbase + lanes + kSfbCol + 4, kSfHi, kSfHi, kSfHi, kSfHi);
+        tc::tmem_st4(tbase + lanes + kSfbCol + 8, kSfLo, kSfLo, kSfLo, kSfLo);
+        tc::tmem_st4(tbase + lanes + kSfbCol + 12, kSfLo, kSfLo, kSfLo, kSfLo);
+        tc::tmem_wait_st();
+        int s = 0, gidx = 0;
+        uint32_t ph = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            bool ok = true;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                const int slot = gidx & 1;
+                int w = 1;
+                if (lane == 0) {
+                    if (kb % kScaleGroupS == 0) w = tc::mbar_wait(&fullS[slot], (gidx >> 1) & 1u, lim);
+                    // the slot is free once the MMAs of the stage's last use completed
+                    if (w) w = tc::mbar_wait(&empty[s], ph ^ 1u, lim);
+                    if (!w) {
+                        set_status(p.status, QBMOE_ETIMEOUT);
+                        *abort_flag = 1;
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint8_t* SC = sc_ring + slot * kScaleBytes + (kb % kScaleGroupS) * 4;
+                uint32_t v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint32_t*>(SC + (lane + 32 * j) * 16);
+                tc::tmem_st4(tbase + lanes + kSfaCol + 4 * s, v[0], v[1], v[2], v[3]);
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&full[s]);
+                if (kb % kScaleGroupS == kScaleGroupS - 1 || kb == p.nkb - 1) {
+                    if (lane == 0) tc::mbar_arrive(&emptyS[slot]);
+                    ++gidx;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            const int stop = __shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0);
+            if (!ok || stop) break;
+        }
+        __syncthreads();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -514,10 +640,24 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
                     tc::tc_fence_after();
                     const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
                     const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
+                    if (MXS) {
+                        // four 32-wide K slices (slice kk uses byte kk of the weight
+                        // scale words), each against the hi and the lo token plane
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc::tc_mma_bf16(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32), idesc,
-                                        (kb | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t id = tc::idesc_mx_e2m1_e4m3_m128(n_eff, kk, 0);
+                            const uint64_t ad = tc::desc_sw128(a_addr + kk * 32);
+                            tc::tc_mma_mxf8f6f4(d, ad, tc::desc_sw128(b_addr + kk * 32), id, tbase + kSfaCol + 4 * sa,
+                                                tbase + kSfbCol, (kb | kk) != 0);
+                            tc::tc_mma_mxf8f6f4(d, ad, tc::desc_sw128(b_addr + kPlane + kk * 32), id,
+                                                tbase + kSfaCol + 4 * sa, tbase + kSfbCol + 8, 1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc::tc_mma_bf16(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
+                                            idesc, (kb | kk) != 0);
+                    }
                     tc::tc_commit(&empty[sa]);
                     if (++sa == S) { sa = 0; pha ^= 1u; }
                 }
@@ -543,7 +683,6 @@ __global__ void __launch_bounds__(MX ? kThreadsMx : kThreads, 1) k_tc_gemm(const
             TileInfo ti;
             decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
             const SubGemm& sg = p.sub[ti.sub];
-            const int n_eff = (ti.nrows + 15) & ~15;
             // one thread waits; the verdict is shared so the 128 threads stay uniform
             if (et == 0) {
                 const bool ok = tc::mbar_wait(&accf[ab], aph, lim);
@@ -800,6 +939,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm2(const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
+// Row gather into E4M3 pairs: row r of dst holds the hi bytes of
+// src[rows[r]] in its first vec_per_row * 8 columns and the lo bytes after
+// them (e4m3_pair); 8 bf16 in, 2 x 8 bytes out per step.
+__global__ void k_gather_rows_e4m3(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ rows,
+                                   int n_rows, uint2* __restrict__ dst) {
+    const long long total = (long long)n_rows * vec_per_row;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / vec_per_row;
+        const int c = (int)(i - r * vec_per_row);
+        const uint4 v = src[(long long)__ldg(rows + r) * vec_per_row + c];
+        const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&v);
+        __align__(8) uint8_t oh[8];
+        __align__(8) uint8_t ol[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) e4m3_pair(__bfloat162float(b[u]), oh[u], ol[u]);
+        uint2* row = dst + r * 2 * vec_per_row;
+        row[c] = *reinterpret_cast<const uint2*>(oh);
+        row[vec_per_row + c] = *reinterpret_cast<const uint2*>(ol);
+    }
+}
+
 // Row gather: dst[r] = src[rows[r]] (16-byte vectors), r < n_rows.
 __global__ void k_gather_rows(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ rows,
                               int n_rows, uint4* __restrict__ dst) {
@@ -835,13 +996,27 @@ template <int BN> struct StagesMx;
 template <> struct StagesMx<16> { static constexpr int S = 9; };
 template <> struct StagesMx<64> { static constexpr int S = 7; };
 template <> struct StagesMx<160> { static constexpr int S = 5; };
-template <> struct StagesMx<256> { static constexpr int S = 3; };
 
-template <int BN, bool MX>
+// Block-scaled MXFP4: stages as for bf16 (a 16 KB E2M1 tile and a token tile
+// of BN x 128 E4M3 bytes) plus two 2 KB scale slots.
+template <int BN> struct StagesMxS;
+template <> struct StagesMxS<16> { static constexpr int S = 10; };
+template <> struct StagesMxS<64> { static constexpr int S = 6; };
+template <> struct StagesMxS<128> { static constexpr int S = 4; };
+
+template <int BN, int MODE> struct StagesOf { static constexpr int S = Stages<BN>::S; };
+template <int BN> struct StagesOf<BN, MODE_MX_DECODE> { static constexpr int S = StagesMx<BN>::S; };
+template <int BN> struct StagesOf<BN, MODE_MX_SCALED> { static constexpr int S = StagesMxS<BN>::S; };
+
+template <int BN, int MODE>
+constexpr int stages_of() { return StagesOf<BN, MODE>::S; }
+
+template <int BN, int MODE>
 constexpr size_t smem_for() {
-    constexpr int S = MX ? StagesMx<BN>::S : Stages<BN>::S;
-    return 1024 + (size_t)S * (kATileBytes + BN * kBK * 2 + (MX ? kPackBytes : 0)) +
-           (MX ? 2 * kScaleBytes : 0) + 768 + 128 * kStLd * 4 + 2 * (QBMOE_MAX_EXPERTS + 1) * 4;
+    constexpr int S = stages_of<BN, MODE>();
+    constexpr bool MX = MODE == MODE_MX_DECODE, MXS = MODE == MODE_MX_SCALED;
+    return 1024 + (size_t)S * (kATileBytes + (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
+           (MX || MXS ? 2 * kScaleBytes : 0) + 768 + 128 * kStLd * 4 + 2 * (QBMOE_MAX_EXPERTS + 1) * 4;
 }
 
 }  // namespace
@@ -857,6 +1032,7 @@ struct TcPlan {
     long long wait_limit = 0;
     int stall = 0;
     bool pair_ok = false;  // 2-SM kernel enabled (QBMOE_ENABLE_2SM=1)
+    bool mx_scaled = false;  // MXFP4 experts on the block-scaled MMA (else decoded to bf16 in SMEM)
     int pair_clusters[2] = {0, 0};   // co-resident clusters of the 160 / 256 variants (0 = not queried)
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
@@ -900,6 +1076,45 @@ bool make_token_maps(TcPlan* P, TcParams& prm, const void* x, long long rows, lo
     return true;
 }
 
+// 2-D E4M3 tensor [rows, cols] (row stride ld bytes), box {128, box_rows}, 128-byte swizzle.
+bool make_map_e4m3(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long long cols, long long ld,
+                   int box_rows) {
+    if (!P->encode || rows <= 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {(cuuint32_t)kBKS, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = P->encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_token_maps_e4m3(TcPlan* P, TcParams& prm, const void* x, long long rows, long long K, int BN) {
+    for (int i = 0; i < 6; ++i) {
+        const int h = std::min(8 << i, BN);
+        if (!make_map_e4m3(P, &prm.bx[i], x, rows, K, K, h)) return false;
+    }
+    return true;
+}
+
+// Packed E2M1 weights [rows, K] (K codes per row, two per byte, row stride
+// K/2 bytes), box {128 codes, box_rows}: each 16-code chunk lands in SMEM as
+// 8 bytes followed by 8 unused bytes, the operand layout of the block-scaled
+// MMA, with the 128-byte swizzle.  Needs K % 128 == 0, a row stride that is a
+// multiple of 32 bytes and a 32-byte aligned base.
+bool make_map_e2m1(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long long K, int box_rows) {
+    if (!P->encode || rows <= 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    cuuint32_t box[2] = {(cuuint32_t)kBKS, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = P->encode(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box,
+                           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 2-D uint8 tensor [rows, cols] (row stride ld bytes), box {box_x, box_rows}, no swizzle.
 bool make_map_u8(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_x,
                  int box_rows) {
@@ -914,19 +1129,19 @@ bool make_map_u8(TcPlan* P, CUtensorMap* m, const void* base, long long rows, lo
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool MX>
+template <int BN, int MODE>
 int launch_bn(TcParams& prm, int grid, cudaStream_t s) {
-    constexpr size_t smem = smem_for<BN, MX>();
+    constexpr size_t smem = smem_for<BN, MODE>();
     static_assert(smem <= 232448, "shared memory per CTA");
-    constexpr int S = MX ? StagesMx<BN>::S : Stages<BN>::S;
-    auto kern = k_tc_gemm<BN, S, MX>;
+    constexpr int S = stages_of<BN, MODE>();
+    auto kern = k_tc_gemm<BN, S, MODE>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
     if (attr_err != cudaSuccess) return QBMOE_ECUDA;
-    kern<<<grid, MX ? kThreadsMx : kThreads, smem, s>>>(prm);
+    kern<<<grid, threads_of<MODE>(), smem, s>>>(prm);
     return cuda_err(cudaGetLastError());
 }
 
@@ -968,21 +1183,30 @@ int launch_bn2(TcPlan* P, TcParams& prm, int tiles, cudaStream_t s) {
     return cuda_err(cudaGetLastError());
 }
 
-int launch_mx(int BN, TcParams& prm, int grid, cudaStream_t s) {
+int launch_mx_decode(int BN, TcParams& prm, int grid, cudaStream_t s) {
     switch (BN) {
-        case 16: return launch_bn<16, true>(prm, grid, s);
-        case 64: return launch_bn<64, true>(prm, grid, s);
-        case 160: return launch_bn<160, true>(prm, grid, s);
+        case 16: return launch_bn<16, MODE_MX_DECODE>(prm, grid, s);
+        case 64: return launch_bn<64, MODE_MX_DECODE>(prm, grid, s);
+        case 160: return launch_bn<160, MODE_MX_DECODE>(prm, grid, s);
+        default: return QBMOE_EINVAL;
+    }
+}
+
+int launch_mx_scaled(int BN, TcParams& prm, int grid, cudaStream_t s) {
+    switch (BN) {
+        case 16: return launch_bn<16, MODE_MX_SCALED>(prm, grid, s);
+        case 64: return launch_bn<64, MODE_MX_SCALED>(prm, grid, s);
+        case 128: return launch_bn<128, MODE_MX_SCALED>(prm, grid, s);
         default: return QBMOE_EINVAL;
     }
 }
 
 int launch_any(int BN, TcParams& prm, int grid, cudaStream_t s) {
     switch (BN) {
-        case 16: return launch_bn<16, false>(prm, grid, s);
-        case 64: return launch_bn<64, false>(prm, grid, s);
-        case 160: return launch_bn<160, false>(prm, grid, s);
-        case 256: return launch_bn<256, false>(prm, grid, s);
+        case 16: return launch_bn<16, MODE_BF16>(prm, grid, s);
+        case 64: return launch_bn<64, MODE_BF16>(prm, grid, s);
+        case 160: return launch_bn<160, MODE_BF16>(prm, grid, s);
+        case 256: return launch_bn<256, MODE_BF16>(prm, grid, s);
         default: return QBMOE_EINVAL;
     }
 }
@@ -1041,6 +1265,10 @@ TcPlan* tc_plan_create(const qbmoe_config& cfg) {
     // the prefill shape, so it is opt-in (QBMOE_ENABLE_2SM=1).
     const char* env2 = getenv("QBMOE_ENABLE_2SM");
     P->pair_ok = env2 && env2[0] == '1';
+    // MXFP4 experts use the block-scaled MMA unless QBMOE_MX_DECODE=1 asks for
+    // the in-SMEM decode to bf16.
+    const char* env3 = getenv("QBMOE_MX_DECODE");
+    P->mx_scaled = cfg.expert_wfmt == QBMOE_W_MXFP4 && !(env3 && env3[0] == '1');
     return P;
 }
 
@@ -1055,6 +1283,8 @@ int tc_plan_set_weights(TcPlan* P, const qbmoe_config&, const qbmoe_weights& w) 
 
 bool tc_enabled(const TcPlan* p) { return p && p->enabled; }
 
+bool tc_mx_scaled(const TcPlan* p) { return p && p->enabled && p->mx_scaled; }
+
 void tc_set_wait_limit(TcPlan* p, long long lim) {
     if (p) p->wait_limit = lim;
 }
@@ -1067,7 +1297,10 @@ int tc_token_tile(const TcPlan* P, int T) {
     // Token rows per grouped tile: each expert's rows are split into equal
     // tiles of at most this many rows (e.g. 293 -> 160 + 133).
     const long long avg = (long long)T * P->cfg.top_k / P->cfg.n_experts;
-    return avg <= 16 ? 16 : (avg <= 64 ? 64 : 160);
+    // the block-scaled MXFP4 kernel holds two token planes per stage, so its
+    // largest tile is 128 rows
+    const int big = tc_mx_scaled(P) ? 128 : 160;
+    return avg <= 16 ? 16 : (avg <= 64 ? 64 : big);
 }
 
 // m-tiles of a sub-GEMM over F outputs: the one-CTA kernel covers 128 weight
@@ -1122,6 +1355,17 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, v
     return launch_dense(P, prm, BN, pair, T, x, c.d, c.d, s, nl);
 }
 
+int tc_gather_e4m3(const void* src, int cols, const int* perm, int n_rows, void* dst, cudaStream_t s, int* nl) {
+    // dst rows are 2 * cols bytes: hi plane, then lo plane
+    const int vpr = cols / 8;
+    const long long total = (long long)n_rows * vpr;
+    const int grid = (int)std::min<long long>((total + 255) / 256, 152LL * 8);
+    k_gather_rows_e4m3<<<std::max(grid, 1), 256, 0, s>>>(static_cast<const uint4*>(src), vpr, perm, n_rows,
+                                                         static_cast<uint2*>(dst));
+    if (nl) ++*nl;
+    return cuda_err(cudaGetLastError());
+}
+
 int tc_gather(const void* src, int cols, const int* perm, int n_rows, void* dst, cudaStream_t s, int* nl) {
     const int vpr = cols * 2 / 16;
     const long long total = (long long)n_rows * vpr;
@@ -1133,16 +1377,24 @@ int tc_gather(const void* src, int cols, const int* perm, int n_rows, void* dst,
 }
 
 static int launch_grouped(TcPlan* P, TcParams& prm, bool pair, const void* act, long long routes, long long K,
-                          const int* offsets, const int* tile_off, int BN, cudaStream_t s, int* nl, bool mx = false) {
-    if (!make_token_maps(P, prm, act, routes, K, K, BN)) return QBMOE_ECUDA;
-    prm.nkb = (int)((K + kBK - 1) / kBK);
+                          const int* offsets, const int* tile_off, int BN, cudaStream_t s, int* nl,
+                          int mode = MODE_BF16) {
+    if (mode == MODE_MX_SCALED) {
+        // E4M3 pairs: rows of 2K bytes (hi plane, then lo plane)
+        if (!make_token_maps_e4m3(P, prm, act, routes, 2 * K, BN)) return QBMOE_ECUDA;
+        prm.nkb = (int)(K / kBKS);
+    } else {
+        if (!make_token_maps(P, prm, act, routes, K, K, BN)) return QBMOE_ECUDA;
+        prm.nkb = (int)((K + kBK - 1) / kBK);
+    }
     prm.n_groups = P->cfg.n_experts;
     prm.seg_off = offsets;
     prm.tile_off = tile_off;
     prm.rows = 0;
     prm.raster_g = 1;
     if (nl) ++*nl;
-    if (mx) return launch_mx(BN, prm, P->num_sms, s);
+    if (mode == MODE_MX_SCALED) return launch_mx_scaled(BN, prm, P->num_sms, s);
+    if (mode == MODE_MX_DECODE) return launch_mx_decode(BN, prm, P->num_sms, s);
     if (pair) return BN == 160 ? launch_bn2<160>(P, prm, 1 << 30, s) : launch_bn2<256>(P, prm, 1 << 30, s);
     return launch_any(BN, prm, P->num_sms, s);
 }
@@ -1161,7 +1413,19 @@ int tc_expert_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets, 
     g.epi = SUB_SITU; g.F = c.expert_inter; g.m_tiles = m_tiles_of(c.expert_inter, true, pair); g.m_begin = 0;
     g.k_split = 1 << 30; g.out = act; g.ldo = c.expert_inter;
     const long long wrows = (long long)c.n_experts * c.expert_inter;
-    if (mx) {
+    const int mode = !mx ? MODE_BF16 : (P->mx_scaled ? MODE_MX_SCALED : MODE_MX_DECODE);
+    if (mode == MODE_MX_SCALED) {
+        // E2M1 tiles unpacked by TMA (box 128 codes x 64 rows), E8M0 scales
+        // [rows, K/32] (box 16 x 64); the output act is E4M3 for the down GEMM
+        const long long K = c.latent;
+        g.out_e4m3 = 1;
+        g.ldo = 2LL * c.expert_inter;   // act as E4M3 pairs: hi plane, then lo plane
+        if (!make_map_e2m1(P, &prm.a0[0], P->w.w_gate, wrows, K, 64) ||
+            !make_map_e2m1(P, &prm.a1[0], P->w.w_up, wrows, K, 64) ||
+            !make_map_u8(P, &prm.sc0, P->w.s_gate, wrows, K / 32, K / 32, 16, 64) ||
+            !make_map_u8(P, &prm.sc1, P->w.s_up, wrows, K / 32, K / 32, 16, 64))
+            return QBMOE_ECUDA;
+    } else if (mx) {
         // packed E2M1 [rows, K/2] (box 32 bytes x 64 rows) and E8M0 scales [rows, K/32] (box 16 x 64)
         const long long K = c.latent;
         if (!make_map_u8(P, &prm.a0[0], P->w.w_gate, wrows, K / 2, K / 2, kBK / 2, 64) ||
@@ -1174,7 +1438,7 @@ int tc_expert_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets, 
         return QBMOE_ECUDA;
     }
     prm.m_total = g.m_tiles;
-    return launch_grouped(P, prm, pair, h_perm, routes, c.latent, offsets, tile_off, BN, s, nl, mx);
+    return launch_grouped(P, prm, pair, h_perm, routes, c.latent, offsets, tile_off, BN, s, nl, mode);
 }
 
 int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const int* tile_off, void* e,
@@ -1191,7 +1455,13 @@ int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const 
     g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = m_tiles_of(c.latent, false, pair); g.m_begin = 0;
     g.k_split = 1 << 30; g.out = e; g.ldo = c.latent;
     const long long wrows = (long long)c.n_experts * c.latent;
-    if (mx) {
+    const int mode = !mx ? MODE_BF16 : (P->mx_scaled ? MODE_MX_SCALED : MODE_MX_DECODE);
+    if (mode == MODE_MX_SCALED) {
+        const long long K = c.expert_inter;
+        if (!make_map_e2m1(P, &prm.a0[0], P->w.w_out, wrows, K, 128) ||
+            !make_map_u8(P, &prm.sc0, P->w.s_out, wrows, K / 32, K / 32, 16, 128))
+            return QBMOE_ECUDA;
+    } else if (mx) {
         const long long K = c.expert_inter;
         if (!make_map_u8(P, &prm.a0[0], P->w.w_out, wrows, K / 2, K / 2, kBK / 2, 128) ||
             !make_map_u8(P, &prm.sc0, P->w.s_out, wrows, K / 32, K / 32, 16, 128))
@@ -1201,7 +1471,7 @@ int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const 
     }
     prm.a1[0] = prm.a0[0];
     prm.m_total = g.m_tiles;
-    return launch_grouped(P, prm, pair, act, routes, c.expert_inter, offsets, tile_off, BN, s, nl, mx);
+    return launch_grouped(P, prm, pair, act, routes, c.expert_inter, offsets, tile_off, BN, s, nl, mode);
 }
 
 int tc_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, int* status, cudaStream_t s,

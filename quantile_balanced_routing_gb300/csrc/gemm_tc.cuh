@@ -22,6 +22,12 @@ int tc_xside(TcPlan* p, int T, const void* x, bool with_router, float* scores, v
              int* status, cudaStream_t s, int* nl);
 // dst[r] = src[rows[r]] for r < n_rows (bf16 rows of `cols` elements).
 int tc_gather(const void* src, int cols, const int* rows, int n_rows, void* dst, cudaStream_t s, int* nl);
+// The same gather converted to E4M3 bytes (the token operand of the
+// block-scaled MXFP4 expert GEMMs; cols % 8 == 0).
+int tc_gather_e4m3(const void* src, int cols, const int* rows, int n_rows, void* dst, cudaStream_t s, int* nl);
+// Whether the MXFP4 expert GEMMs run on the block-scaled MMA: their token
+// inputs (h_perm, act) are then E4M3 bytes.
+bool tc_mx_scaled(const TcPlan* p);
 int tc_expert_gate_up(TcPlan* p, int T, const void* h_perm, const int* offsets, const int* tile_off, void* act,
                       int* status, cudaStream_t s, int* nl);
 int tc_expert_down(TcPlan* p, int T, const void* act, const int* offsets, const int* tile_off, void* e,

@@ -163,6 +163,38 @@ __device__ __forceinline__ uint32_t idesc_bf16_m128(uint32_t n) {
            | ((128u >> 4) << 24);  // M >> 4
 }
 
+// ---- block-scaled MMA (OCP MX) ----------------------------------------------
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with one E8M0 scale per 32 K
+// elements of each operand row, read from TMEM (scale_vec::1X): K = 32 per
+// instruction, operands in 8-bit containers in SMEM (E2M1 as 16 packed
+// codes per 16-byte chunk, the second 8 bytes unused), fp32 accumulate.
+__device__ __forceinline__ void tc_mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+// Instruction descriptor of kind::mxf8f6f4 with A = E2M1 (weights) and
+// B = E4M3 (tokens), both K-major, E8M0 scales, M = 128, N = n.  Bits: B
+// scale byte [4,6), A format [7,10) (E2M1 = 5), B format [10,13) (E4M3 = 0),
+// N >> 3 [17,23), scale type [23] (1 = E8M0), M >> 4 [24,29), A scale byte
+// [29,31).  The scale byte selects which byte of each 32-bit TMEM scale
+// word this instruction's 32-wide K slice uses.
+__device__ __forceinline__ uint32_t idesc_mx_e2m1_e4m3_m128(uint32_t n, uint32_t a_sf_byte, uint32_t b_sf_byte) {
+    return (b_sf_byte << 4) | (5u << 7) | (0u << 10) | ((n >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) |
+           (a_sf_byte << 29);
+}
+// This warp's 32 TMEM lanes x 4 consecutive 32-bit columns from registers.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

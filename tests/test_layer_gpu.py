@@ -66,6 +66,14 @@ def test_layer_cuda_core_path_matches_oracle(shape, monkeypatch):
     compare_fed(shape)
 
 
+@pytest.mark.parametrize("shape", [TC_MXFP4_DECODE_LIKE, TC_MXFP4_PREFILL_LIKE], ids=lambda s: s.name)
+def test_mxfp4_decode_to_bf16_path_matches_oracle(shape, monkeypatch):
+    """MXFP4 experts on the alternative tensor-core path: converter warps
+    decode E2M1 x E8M0 to bf16 in SMEM for the kind::f16 MMA (bf16 tokens)."""
+    monkeypatch.setenv("QBMOE_MX_DECODE", "1")
+    compare_fed(shape)
+
+
 def test_two_sm_kernel_on_prefill_tiles_matches_oracle(monkeypatch):
     """The prefill-size GEMMs on the opt-in 2-SM (cta_group::2) kernel: 256-row
     weight tiles across a CTA pair, 160- and 256-row token tiles."""
