@@ -162,12 +162,21 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_t
 // quarter q of this warp, 16-column chunks staged through SMEM, epilogue
 // math, 16-byte global stores.  f_base is the output feature of TMEM lane 0;
 // tacc the accumulator's TMEM column base.
+// lo_col > 0 (block-scaled, stacked token planes): the accumulator holds
+// W * hi in columns [0, n) and W * lo in [lo_col, lo_col + n); the result is
+// hi + lo * 2^-kLoShift.
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo& ti, const SubGemm& sg, int f_base,
-                                              uint32_t tacc, int q, int lane, int et, float* st) {
+                                              uint32_t tacc, int lo_col, int q, int lane, int et, float* st) {
     const int n_eff = (ti.nrows + 15) & ~15;
     for (int c0 = 0; c0 < n_eff; c0 += 16) {
         float v[16];
         tc::tmem_ld16(tacc + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+        if (lo_col > 0) {
+            float lo[16];
+            tc::tmem_ld16(tacc + (static_cast<uint32_t>(32 * q) << 16) + lo_col + c0, lo);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = fmaf(lo[j], 1.0f / float(1 << kLoShift), v[j]);
+        }
         tc::named_bar_sync(1, 128);   // previous chunk's readers are done
 #pragma unroll
         for (int j = 0; j < 16; ++j) st[(32 * q + lane) * kStLd + j] = v[j];
@@ -294,10 +303,15 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     constexpr int kKS = MXS ? kBKS : kBK;          // K elements per stage
     constexpr int kPlane = BN * 128;               // token tile: BN rows of 128 bytes
     constexpr int kBBytes = MXS ? 2 * kPlane : kPlane;   // block-scaled: hi and lo planes
-    // TMEM columns: two accumulators (2 x BN); block-scaled adds the token
-    // scales (8 columns of 2^0 for hi, 8 of 2^-4 for lo) and a 4-column
-    // weight-scale slot per stage.
-    constexpr int kSfbCol = 2 * BN, kSfaCol = 2 * BN + 16;
+    // Block-scaled: the lo rows of a token tile are stacked under its hi rows
+    // so one MMA (N = 2 n) serves both planes; the epilogue adds lo * 2^-4.
+    // (The MMA's cost per instruction is mostly reading the weight tile from
+    // SMEM, so one N = 2n MMA is much cheaper than two N = n ones.)
+    static_assert(!MXS || 2 * BN <= 256, "stacked token planes need N = 2 BN <= 256");
+    constexpr int kAccCols = MXS ? 2 * BN : BN;   // TMEM columns per accumulator
+    // TMEM columns: two accumulators; block-scaled adds the token scales
+    // (8 columns of 2^0) and a 4-column weight-scale slot per stage.
+    constexpr int kSfbCol = 2 * kAccCols, kSfaCol = 2 * kAccCols + 8;
     constexpr uint32_t kCols = MXS ? pow2_cols(kSfaCol + 4 * S) : pow2_cols(2 * BN);
     static_assert(!MXS || kSfaCol + 4 * S <= 512, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
@@ -460,7 +474,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         uint8_t* B = b_ring + s * kBBytes;
                         tc::mbar_expect_tx(&fullx[s], (MXS ? 2 : 1) * n_eff * 128);
                         // n_eff rows as a sum of power-of-two boxes (largest first): <= 5 TMA issues
-                        // per plane (block-scaled: hi columns kb * 128, lo columns K + kb * 128)
+                        // per plane (block-scaled: hi columns kb * 128, lo columns K + kb * 128,
+                        // the lo rows stacked under the hi rows)
                         int r = 0;
 #pragma unroll
                         for (int i = 5; i >= 1; --i) {
@@ -468,7 +483,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                             if (h <= BN && (n_eff - r) >= h) {
                                 tc::tma_load_2d(B + r * 128, &p.bx[i], &fullx[s], kb * kKS, ti.row0 + r);
                                 if (MXS)
-                                    tc::tma_load_2d(B + kPlane + r * 128, &p.bx[i], &fullx[s], (p.nkb + kb) * kKS,
+                                    tc::tma_load_2d(B + (n_eff + r) * 128, &p.bx[i], &fullx[s], (p.nkb + kb) * kKS,
                                                     ti.row0 + r);
                                 r += h;
                             }
@@ -563,15 +578,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         // E8M0 bytes per weight row, one per 32-wide K slice) go to its
         // 4-column slot in the layout the block-scaled MMA reads for M = 128:
         // in every lane quarter, lane i column j holds row i + 32 j.  The
-        // token scales are constant, written once: 8 columns of 0x7F bytes
-        // (2^0, hi plane) and 8 of 0x7B bytes (2^-4, lo plane).
+        // token scales are all 2^0 (the lo plane's 2^-4 is applied in the
+        // epilogue): 8 columns of 0x7F bytes, written once.
         const int q = warp & 3;
         const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
-        constexpr uint32_t kSfHi = 0x7F7F7F7Fu, kSfLo = 0x01010101u * (127 - kLoShift);
-        tc::tmem_st4(tbase + lanes + kSfbCol, kSfHi, kSfHi, kSfHi, kSfHi);
-        tc::tmem_st4(tbase + lanes + kSfbCol + 4, kSfHi, kSfHi, kSfHi, kSfHi);
-        tc::tmem_st4(tbase + lanes + kSfbCol + 8, kSfLo, kSfLo, kSfLo, kSfLo);
-        tc::tmem_st4(tbase + lanes + kSfbCol + 12, kSfLo, kSfLo, kSfLo, kSfLo);
+        constexpr uint32_t kSf1 = 0x7F7F7F7Fu;
+        tc::tmem_st4(tbase + lanes + kSfbCol, kSf1, kSf1, kSf1, kSf1);
+        tc::tmem_st4(tbase + lanes + kSfbCol + 4, kSf1, kSf1, kSf1, kSf1);
         tc::tmem_wait_st();
         int s = 0, gidx = 0;
         uint32_t ph = 0;
@@ -628,7 +641,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t d = tbase + ab * BN;
+                const uint32_t d = tbase + ab * kAccCols;
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
                     if (!tc::mbar_wait(&full[sa], pha, lim)) {
@@ -642,16 +655,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                     const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
                     if (MXS) {
                         // four 32-wide K slices (slice kk uses byte kk of the weight
-                        // scale words), each against the hi and the lo token plane
+                        // scale words) against the stacked hi and lo rows
+                        const uint32_t id0 = tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, 0, 0);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t id = tc::idesc_mx_e2m1_e4m3_m128(n_eff, kk, 0);
-                            const uint64_t ad = tc::desc_sw128(a_addr + kk * 32);
-                            tc::tc_mma_mxf8f6f4(d, ad, tc::desc_sw128(b_addr + kk * 32), id, tbase + kSfaCol + 4 * sa,
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::tc_mma_mxf8f6f4(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
+                                                id0 | (uint32_t(kk) << 29), tbase + kSfaCol + 4 * sa,
                                                 tbase + kSfbCol, (kb | kk) != 0);
-                            tc::tc_mma_mxf8f6f4(d, ad, tc::desc_sw128(b_addr + kPlane + kk * 32), id,
-                                                tbase + kSfaCol + 4 * sa, tbase + kSfbCol + 8, 1);
-                        }
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -697,7 +707,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             tc::named_bar_sync(1, 128);
             if (!ok) break;
             tc::tc_fence_after();
-            epilogue_tile(p, ti, sg, sg.epi == SUB_SITU ? ti.mt * 64 : ti.mt * 128, tbase + ab * BN, q, lane, et, st);
+            epilogue_tile(p, ti, sg, sg.epi == SUB_SITU ? ti.mt * 64 : ti.mt * 128, tbase + ab * kAccCols,
+                          MXS ? (ti.nrows + 15) & ~15 : 0, q, lane, et, st);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acce[ab]);
@@ -917,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm2(const __grid_constant_
             if (!ok) break;
             tc::tc_fence_after();
             const int f_base = sg.epi == SUB_SITU ? ti.mt * 128 + (int)rank * 64 : ti.mt * 256 + (int)rank * 128;
-            epilogue_tile(p, ti, sg, f_base, tbase + ab * BN, q, lane, et, st);
+            epilogue_tile(p, ti, sg, f_base, tbase + ab * BN, 0, q, lane, et, st);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -1002,7 +1013,7 @@ template <> struct StagesMx<160> { static constexpr int S = 5; };
 template <int BN> struct StagesMxS;
 template <> struct StagesMxS<16> { static constexpr int S = 10; };
 template <> struct StagesMxS<64> { static constexpr int S = 6; };
-template <> struct StagesMxS<128> { static constexpr int S = 4; };
+template <> struct StagesMxS<112> { static constexpr int S = 4; };
 
 template <int BN, int MODE> struct StagesOf { static constexpr int S = Stages<BN>::S; };
 template <int BN> struct StagesOf<BN, MODE_MX_DECODE> { static constexpr int S = StagesMx<BN>::S; };
@@ -1196,7 +1207,7 @@ int launch_mx_scaled(int BN, TcParams& prm, int grid, cudaStream_t s) {
     switch (BN) {
         case 16: return launch_bn<16, MODE_MX_SCALED>(prm, grid, s);
         case 64: return launch_bn<64, MODE_MX_SCALED>(prm, grid, s);
-        case 128: return launch_bn<128, MODE_MX_SCALED>(prm, grid, s);
+        case 112: return launch_bn<112, MODE_MX_SCALED>(prm, grid, s);
         default: return QBMOE_EINVAL;
     }
 }
@@ -1297,9 +1308,10 @@ int tc_token_tile(const TcPlan* P, int T) {
     // Token rows per grouped tile: each expert's rows are split into equal
     // tiles of at most this many rows (e.g. 293 -> 160 + 133).
     const long long avg = (long long)T * P->cfg.top_k / P->cfg.n_experts;
-    // the block-scaled MXFP4 kernel holds two token planes per stage, so its
-    // largest tile is 128 rows
-    const int big = tc_mx_scaled(P) ? 128 : 160;
+    // the block-scaled MXFP4 kernel stacks two token planes in one MMA
+    // (N = 2 x rows <= 256) and keeps two accumulators plus the scale slots
+    // in TMEM, so its largest tile is 112 rows
+    const int big = tc_mx_scaled(P) ? 112 : 160;
     return avg <= 16 ? 16 : (avg <= 64 ? 64 : big);
 }
 
