@@ -1,25 +1,33 @@
 // Tensor-core GEMMs of the layer on sm_103a: TMA -> SMEM (128-byte swizzle)
-// -> tcgen05.mma (bf16, fp32 accumulator in TMEM) -> tcgen05.ld epilogue.
+// -> tcgen05.mma (fp32 accumulator in TMEM) -> tcgen05.ld epilogue.
 //
 // [K3-width] = "Kimi K3 模型结构（5）：宽度维度，Stable LatentMoE" (xhh.club).
 // The contractions are the layer's: full-width router (Q&A on routing), the
 // latent down-projection (延伸解读 "half-width latent space"), the per-expert
 // SiTU-GLU experts in latent space (Q&A on SiTU-GLU), the up-projection and
-// the merged shared expert (Q&A on the shared expert).
+// the merged shared expert (Q&A on the shared expert); MXFP4 expert weights
+// follow 延伸解读 on deployment (OCP MX: E2M1 codes, an E8M0 scale per 32).
 //
 // Orientation: every GEMM is out[t, f] = sum_k W[f, k] X[t, k] with the
 // weights as the MMA's A operand (M = 128 weight rows) and the tokens as its
 // B operand (N = 16..256 token rows), so a decode step with ~5 tokens per
 // expert still issues full-height MMAs while streaming the weights.
 //
-// One persistent, warp-specialised kernel (192 threads, one CTA per SM):
-//   warp 0      TMA producer (one lane): A (weights) and B (tokens) tiles
-//               into a STAGES-deep ring, mbarrier complete_tx
-//   warp 1      TMEM owner and MMA issuer (one lane): 4 x (128 x N x 16)
-//               MMAs per 64-wide K block, commit frees the stage; a tile's
-//               last commit hands the accumulator to the epilogue
-//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 16 columns, stage through
+// One persistent, warp-specialised kernel (one CTA per SM):
+//   warp 0      weight producer (one lane): TMA of A tiles into a
+//               STAGES-deep ring (and the E8M0 scales for MXFP4)
+//   warp 1      token producer (one lane): TMA of B tiles into the same stage
+//   warp 2      TMEM owner and MMA issuer (one lane); one commit per stage
+//               frees it, a tile's last commit hands the accumulator over
+//   warps 3-6   epilogue: tcgen05.ld 32 lanes x 16 columns, stage through
 //               SMEM, epilogue math, 16-byte stores
+//   warps 7+    MXFP4 only: converter warps (decode E2M1 to bf16 in SMEM for
+//               the kind::f16 MMA) or scale writers (E8M0 scale words into
+//               TMEM for the block-scaled kind::mxf8f6f4 MMA)
+// Modes: bf16 weights (kind::f16, 4 x K=16 MMAs per 64-wide K stage);
+// MXFP4 decoded to bf16; MXFP4 block-scaled (E2M1 unpacked by TMA, tokens
+// as exact E4M3 hi/lo pairs stacked in one N = 2n MMA, 4 x K=32 MMAs per
+// 128-wide K stage).
 // Two TMEM accumulators alternate so a tile's epilogue overlaps the next
 // tile's main loop.  Every mbarrier wait is bounded: on expiry the kernel
 // records QBMOE_ETIMEOUT, stops, drains its own TMA/MMA work (bounded) and
@@ -27,7 +35,7 @@
 //
 // Epilogues per sub-GEMM: STORE (bf16), ROUTER (fp32 score of logit + offset)
 // and SITU (A tile = 64 gate rows over 64 up rows of the same features;
-// act = SiTU-GLU(gate, up)).
+// act = SiTU-GLU(gate, up), stored as bf16 or as E4M3 pairs).
 #include "gemm_tc.cuh"
 #include "dispatch.cuh"
 #include "tc_ptx.cuh"
