@@ -52,11 +52,16 @@ namespace {
 using namespace qb;
 
 constexpr int kProdAWarp = 0, kProdBWarp = 1, kMmaWarp = 2, kEpiFirstWarp = 3, kConvFirstWarp = 7;
-constexpr int kThreads = (kEpiFirstWarp + 4) * 32;     // 224
+// Second producer pair (bf16 and block-scaled modes, and the 2-SM kernel):
+// producer pair p issues the weight and token tiles of the K blocks with
+// kb % 2 == p, so twice as many threads issue TMA copies.
+constexpr int kProdA1Warp = 7, kProdB1Warp = 8;
 constexpr int kConvWarps = 8;                          // MXFP4 converter warps (two threads per weight row)
 constexpr int kThreadsMx = (kConvFirstWarp + kConvWarps) * 32;  // 480
 constexpr int kSfWarps = 4;                            // block-scaled MXFP4: scale writers, one per TMEM lane quarter
-constexpr int kThreadsMxS = (kConvFirstWarp + kSfWarps) * 32;   // 352
+constexpr int kSfFirstWarp = kProdB1Warp + 1;          // 9
+constexpr int kThreadsMxS = (kSfFirstWarp + kSfWarps) * 32;     // 416
+constexpr int kThreadsBf16 = (kProdB1Warp + 1) * 32;   // 288
 constexpr int kBKS = 128;                      // block-scaled: K elements per stage (128 bytes of E4M3 per row)
 constexpr int kScaleGroupS = 4;                // block-scaled: stages per E8M0 scale load (16 scale bytes per row)
 constexpr int kBK = 64;                        // K elements per block (128 bytes of bf16)
@@ -300,7 +305,7 @@ __device__ __forceinline__ void mx_decode_word(uint32_t w, const uint32_t (&h)[2
 
 template <int MODE>
 constexpr int threads_of() {
-    return MODE == MODE_MX_DECODE ? kThreadsMx : (MODE == MODE_MX_SCALED ? kThreadsMxS : kThreads);
+    return MODE == MODE_MX_DECODE ? kThreadsMx : (MODE == MODE_MX_SCALED ? kThreadsMxS : kThreadsBf16);
 }
 constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
@@ -392,11 +397,16 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     const int n_tiles_dense = p.n_groups > 0 ? 0 : (p.rows + BN - 1) / BN;
     const int n_tiles = p.n_groups > 0 ? s_toff[p.n_groups] * p.m_total : n_tiles_dense * p.m_total;
 
-    if (warp == kProdAWarp || warp == kProdBWarp) {
+    constexpr int kNProd = MX ? 1 : 2;   // producer pairs
+    const bool is_prod = warp == kProdAWarp || warp == kProdBWarp ||
+                         (kNProd == 2 && (warp == kProdA1Warp || warp == kProdB1Warp));
+    if (is_prod) {
         // ------------------------------------------------- producers (one lane each)
-        // Warp kProdAWarp loads the weight tiles, warp kProdBWarp the token
-        // tiles (up to 5 TMA issues each), in parallel into the same stage.
-        const bool is_a = warp == kProdAWarp;
+        // A weight producer and a token producer per pair load into the same
+        // stage in parallel (up to 5 TMA issues each); pair p takes the K
+        // blocks with kb % kNProd == p.
+        const bool is_a = warp == kProdAWarp || warp == kProdA1Warp;
+        const int pair = (warp == kProdAWarp || warp == kProdBWarp) ? 0 : 1;
         uint64_t* fullx = (MX && is_a) ? fullP : full;
         uint64_t* emptyx = empty;
         uint32_t issued = 0, last_par = 0;
@@ -411,6 +421,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 const SubGemm& sg = p.sub[ti.sub];
                 const int n_eff = (ti.nrows + 15) & ~15;
                 for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (kNProd == 2 && (kb & 1) != pair) {   // the other pair's K block
+                        if (++s == S) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
                     if (!tc::mbar_wait(&emptyx[s], ph ^ 1u, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
@@ -580,7 +594,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             if (!ok || stop) break;
         }
         __syncthreads();
-    } else if (MXS && warp >= kConvFirstWarp) {
+    } else if (MXS && warp >= kSfFirstWarp) {
         // ------------------------------------------------- weight scales -> TMEM
         // Warp w writes TMEM lane quarter w % 4.  A stage's scale words (four
         // E8M0 bytes per weight row, one per 32-wide K slice) go to its
@@ -661,20 +675,18 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                     tc::tc_fence_after();
                     const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
                     const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
-                    if (MXS) {
-                        // four 32-wide K slices (slice kk uses byte kk of the weight
-                        // scale words) against the stacked hi and lo rows
-                        const uint32_t id0 = tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, 0, 0);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (MXS) {
+                            // 32-wide K slice kk (byte kk of the weight scale words)
+                            // against the stacked hi and lo rows
+                            const uint32_t id = tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, kk, 0);
                             tc::tc_mma_mxf8f6f4(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
-                                                id0 | (uint32_t(kk) << 29), tbase + kSfaCol + 4 * sa,
-                                                tbase + kSfbCol, (kb | kk) != 0);
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)
+                                                id, tbase + kSfaCol + 4 * sa, tbase + kSfbCol, (kb | kk) != 0);
+                        } else {
                             tc::tc_mma_bf16(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
                                             idesc, (kb | kk) != 0);
+                        }
                     }
                     tc::tc_commit(&empty[sa]);
                     if (++sa == S) { sa = 0; pha ^= 1u; }
@@ -743,7 +755,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
 // epilogue drains its own TMEM lanes (weight rows) and arrives on the
 // leader's accumulator-free barrier.
 template <int BN, int S>
-__global__ void __launch_bounds__(kThreads, 1) k_tc_gemm2(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_constant__ TcParams p) {
     constexpr int kHalf = BN / 2;                            // token rows per CTA per stage
     constexpr int kBBytes = kHalf * kBK * 2;
     constexpr uint32_t kCols = (2 * BN <= 128) ? 128 : 512;  // two accumulators of BN columns
@@ -801,8 +813,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm2(const __grid_constant_
     const int n_tiles_dense = p.n_groups > 0 ? 0 : (p.rows + BN - 1) / BN;
     const int n_tiles = p.n_groups > 0 ? s_toff[p.n_groups] * p.m_total : n_tiles_dense * p.m_total;
 
-    if (warp == kProdAWarp || warp == kProdBWarp) {
-        const bool is_a = warp == kProdAWarp;
+    const bool is_prod = warp == kProdAWarp || warp == kProdBWarp || warp == kProdA1Warp || warp == kProdB1Warp;
+    if (is_prod) {
+        // two producer pairs per CTA, pair p taking the K blocks with kb % 2 == p
+        const bool is_a = warp == kProdAWarp || warp == kProdA1Warp;
+        const int pair = (warp == kProdAWarp || warp == kProdBWarp) ? 0 : 1;
         uint64_t* fullx = full;
         uint64_t* emptyx = empty;
         uint32_t issued = 0, last_par = 0;
@@ -816,6 +831,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm2(const __grid_constant_
                 const int n_eff = (ti.nrows + 15) & ~15;
                 const int half = n_eff >> 1;
                 for (int kb = 0; kb < p.nkb; ++kb) {
+                    if ((kb & 1) != pair) {   // the other pair's K block
+                        if (++s == S) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
                     if (!tc::mbar_wait(&emptyx[s], ph ^ 1u, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
@@ -896,9 +915,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_gemm2(const __grid_constant_
                     const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
                     const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
                         tc::tc_mma_bf16_pair(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
                                              idesc, (kb | kk) != 0);
+                    }
                     tc::tc_commit_pair(&empty[sa], 0x3);
                     if (++sa == S) { sa = 0; pha ^= 1u; }
                 }
@@ -1050,7 +1070,8 @@ struct TcPlan {
     int num_sms = 0;
     long long wait_limit = 0;
     int stall = 0;
-    bool pair_ok = false;  // 2-SM kernel enabled (QBMOE_ENABLE_2SM=1)
+    bool pair_dense = false;     // dense 256-row launches on the 2-SM kernel (default; QBMOE_DISABLE_2SM=1 turns off)
+    bool pair_grouped = false;   // grouped launches on the 2-SM kernel (QBMOE_ENABLE_2SM=1)
     bool mx_scaled = false;  // MXFP4 experts on the block-scaled MMA (else decoded to bf16 in SMEM)
     int pair_clusters[2] = {0, 0};   // co-resident clusters of the 160 / 256 variants (0 = not queried)
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -1181,7 +1202,7 @@ int launch_bn2(TcPlan* P, TcParams& prm, int tiles, cudaStream_t s) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kThreadsBf16, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -1246,7 +1267,9 @@ int dense_bn(long long m_tiles_128, int T) {
 }
 
 // Whether a launch with token tile BN runs on the 2-SM kernel.
-bool use_pair(const TcPlan* P, int BN) { return P->pair_ok && (BN == 256 || BN == 160); }
+bool use_pair(const TcPlan* P, int BN, bool grouped) {
+    return grouped ? P->pair_grouped && (BN == 256 || BN == 160) : P->pair_dense && BN == 256;
+}
 
 // Dense launch over T token rows; n_tiles x m_total tiles.
 int launch_dense(TcPlan* P, TcParams& prm, int BN, bool pair, int T, const void* x, long long ldx, long long K,
@@ -1280,10 +1303,14 @@ TcPlan* tc_plan_create(const qbmoe_config& cfg) {
                            cfg.n_experts % 4 == 0 && cfg.latent % 128 == 0 && cfg.d % 128 == 0;
     const char* env = getenv("QBMOE_DISABLE_TC");
     P->enabled = shapes_ok && P->encode != nullptr && !(env && env[0] == '1');
-    // The 2-SM kernel is measured slower than the one-CTA kernel on GB300 at
-    // the prefill shape, so it is opt-in (QBMOE_ENABLE_2SM=1).
+    // Measured on GB300 at the prefill shape: the 2-SM kernel runs the dense
+    // 256-row GEMMs 7-13% faster than the one-CTA kernel (each SM stages half
+    // the token tile) and the grouped expert GEMMs no faster, so dense
+    // launches use it by default and grouped ones only on request.
     const char* env2 = getenv("QBMOE_ENABLE_2SM");
-    P->pair_ok = env2 && env2[0] == '1';
+    const char* env4 = getenv("QBMOE_DISABLE_2SM");
+    P->pair_grouped = env2 && env2[0] == '1';
+    P->pair_dense = !(env4 && env4[0] == '1');
     // MXFP4 experts use the block-scaled MMA unless QBMOE_MX_DECODE=1 asks for
     // the in-SMEM decode to bf16.
     const char* env3 = getenv("QBMOE_MX_DECODE");
@@ -1337,7 +1364,7 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, v
     const long long m128 = (with_router ? (c.n_experts + 127) / 128 : 0) + (c.latent + 127) / 128 +
                            (c.shared_inter + 63) / 64;
     const int BN = dense_bn(m128, T);
-    const bool pair = use_pair(P, BN);
+    const bool pair = use_pair(P, BN, false);
     TcParams prm;
     base_params(P, prm, status);
     int m = 0, ns = 0;
@@ -1425,7 +1452,7 @@ int tc_expert_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets, 
     const long long routes = (long long)T * c.top_k;
     const int BN = tc_token_tile(P, T);
     const bool mx = c.expert_wfmt == QBMOE_W_MXFP4;
-    const bool pair = !mx && use_pair(P, BN);
+    const bool pair = !mx && use_pair(P, BN, true);
     TcParams prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
@@ -1467,7 +1494,7 @@ int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const 
     const long long routes = (long long)T * c.top_k;
     const int BN = tc_token_tile(P, T);
     const bool mx = c.expert_wfmt == QBMOE_W_MXFP4;
-    const bool pair = !mx && use_pair(P, BN);
+    const bool pair = !mx && use_pair(P, BN, true);
     TcParams prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
@@ -1498,7 +1525,7 @@ int tc_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, i
                  int* nl) {
     const qbmoe_config& c = P->cfg;
     const int BN = dense_bn((c.d + 127) / 128, T);
-    const bool pair = use_pair(P, BN);
+    const bool pair = use_pair(P, BN, false);
     TcParams prm;
     base_params(P, prm, status);
     prm.n_sub = 1;

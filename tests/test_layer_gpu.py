@@ -75,9 +75,17 @@ def test_mxfp4_decode_to_bf16_path_matches_oracle(shape, monkeypatch):
 
 
 def test_two_sm_kernel_on_prefill_tiles_matches_oracle(monkeypatch):
-    """The prefill-size GEMMs on the opt-in 2-SM (cta_group::2) kernel: 256-row
-    weight tiles across a CTA pair, 160- and 256-row token tiles."""
+    """The prefill-size GEMMs on the 2-SM (cta_group::2) kernel, grouped ones
+    included (opt-in): 256-row weight tiles across a CTA pair, 160- and
+    256-row token tiles."""
     monkeypatch.setenv("QBMOE_ENABLE_2SM", "1")
+    compare_fed(TC_PREFILL_LIKE)
+
+
+def test_one_cta_kernel_on_dense_prefill_tiles_matches_oracle(monkeypatch):
+    """The dense 256-row GEMMs on the one-CTA kernel (the 2-SM kernel runs
+    them by default)."""
+    monkeypatch.setenv("QBMOE_DISABLE_2SM", "1")
     compare_fed(TC_PREFILL_LIKE)
 
 
