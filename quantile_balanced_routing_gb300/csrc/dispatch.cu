@@ -71,43 +71,59 @@ __global__ void k_scatter(int T, int n, int k, int tpw, const int32_t* __restric
 }
 
 // y = sum_i w[t,i] * e[route_pos[t,i]] (fp32); z = y / sqrt(mean(y^2) + eps) * gamma.
-// One CTA of 128 threads per token; 16-byte vector loads and stores.
-constexpr int kCombThreads = 128;
-constexpr int kCombMaxVec = 8;   // vectors per thread: latent <= 128 * 8 * (16 / sizeof(TA))
+// One CTA per token; each thread owns VPT 16-byte vectors of the row and
+// reads its k expert rows eight at a time, so that many loads are in flight
+// (the kernel streams the T*k expert rows once).
+constexpr int kCombMaxThreads = 1024;
+constexpr int kCombUnroll = 8;
 
-template <typename TA>
-__global__ void __launch_bounds__(kCombThreads)
+template <typename TA, int VPT>
+__global__ void __launch_bounds__(kCombMaxThreads)
 k_combine_rmsnorm(int T, int k, int latent, const TA* __restrict__ e, const float* __restrict__ w,
                   const int* __restrict__ route_pos, const float* __restrict__ gamma, float eps,
                   TA* __restrict__ z, long long ldz) {
     constexpr int V = 16 / sizeof(TA);             // elements per vector
-    __shared__ float red[kCombThreads / 32];
+    __shared__ float s_w[QBMOE_MAX_TOPK];
+    __shared__ int s_pos[QBMOE_MAX_TOPK];
+    __shared__ float red[kCombMaxThreads / 32];
     const int t = blockIdx.x;
     const int tid = threadIdx.x;
     const int nvec = latent / V;
-    float y[kCombMaxVec][V];
+    if (tid < k) {
+        s_w[tid] = w[(size_t)t * k + tid];
+        s_pos[tid] = route_pos[(size_t)t * k + tid];
+    }
+    __syncthreads();
+    float y[VPT][V];
 #pragma unroll
-    for (int q = 0; q < kCombMaxVec; ++q)
+    for (int q = 0; q < VPT; ++q)
 #pragma unroll
         for (int u = 0; u < V; ++u) y[q][u] = 0.0f;
-    for (int i = 0; i < k; ++i) {
-        const float wi = w[(size_t)t * k + i];
-        const uint4* row = reinterpret_cast<const uint4*>(e + (size_t)route_pos[(size_t)t * k + i] * latent);
 #pragma unroll
-        for (int q = 0; q < kCombMaxVec; ++q) {
-            const int c = tid + q * kCombThreads;
-            if (c < nvec) {
-                const uint4 raw = __ldg(row + c);
-                const TA* vals = reinterpret_cast<const TA*>(&raw);
+    for (int q = 0; q < VPT; ++q) {
+        const int c = tid + q * blockDim.x;
+        if (c >= nvec) break;
+        for (int i0 = 0; i0 < k; i0 += kCombUnroll) {
+            uint4 raw[kCombUnroll];
 #pragma unroll
-                for (int u = 0; u < V; ++u) y[q][u] = fmaf(wi, to_f32(vals[u]), y[q][u]);
+            for (int u = 0; u < kCombUnroll; ++u)
+                if (i0 + u < k)
+                    raw[u] = __ldg(reinterpret_cast<const uint4*>(e + (size_t)s_pos[i0 + u] * latent) + c);
+#pragma unroll
+            for (int u = 0; u < kCombUnroll; ++u) {
+                if (i0 + u < k) {
+                    const float wi = s_w[i0 + u];
+                    const TA* vals = reinterpret_cast<const TA*>(&raw[u]);
+#pragma unroll
+                    for (int x = 0; x < V; ++x) y[q][x] = fmaf(wi, to_f32(vals[x]), y[q][x]);
+                }
             }
         }
     }
     float ss = 0.0f;
 #pragma unroll
-    for (int q = 0; q < kCombMaxVec; ++q)
-        if (tid + q * kCombThreads < nvec)
+    for (int q = 0; q < VPT; ++q)
+        if (tid + q * (int)blockDim.x < nvec)
 #pragma unroll
             for (int u = 0; u < V; ++u) ss = fmaf(y[q][u], y[q][u], ss);
 #pragma unroll
@@ -115,14 +131,13 @@ k_combine_rmsnorm(int T, int k, int latent, const TA* __restrict__ e, const floa
     if ((tid & 31) == 0) red[tid >> 5] = ss;
     __syncthreads();
     float tot = 0.0f;
-#pragma unroll
-    for (int q = 0; q < kCombThreads / 32; ++q) tot += red[q];
+    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) tot += red[q];
     const float inv = 1.0f / sqrtf(tot / (float)latent + eps);
     uint4* zr = reinterpret_cast<uint4*>(z + (size_t)t * ldz);
     const float4* g4 = reinterpret_cast<const float4*>(gamma);
 #pragma unroll
-    for (int q = 0; q < kCombMaxVec; ++q) {
-        const int c = tid + q * kCombThreads;
+    for (int q = 0; q < VPT; ++q) {
+        const int c = tid + q * blockDim.x;
         if (c < nvec) {
             __align__(16) TA o[V];
 #pragma unroll
@@ -136,6 +151,23 @@ k_combine_rmsnorm(int T, int k, int latent, const TA* __restrict__ e, const floa
             zr[c] = *reinterpret_cast<const uint4*>(o);
         }
     }
+}
+
+template <typename TA>
+int launch_combine_t(int T, int k, int latent, const TA* e, const float* w, const int* route_pos,
+                     const float* gamma, float eps, TA* z, long long ldz, cudaStream_t s) {
+    constexpr int V = 16 / sizeof(TA);
+    const int nvec = latent / V;
+    const int vpt = nvec <= kCombMaxThreads ? 1 : (nvec <= 2 * kCombMaxThreads ? 2 : 4);
+    if (nvec > 4 * kCombMaxThreads) return QBMOE_EINVAL;
+    const int threads = std::min(kCombMaxThreads, ((nvec + vpt - 1) / vpt + 31) & ~31);
+    if (vpt == 1)
+        k_combine_rmsnorm<TA, 1><<<T, threads, 0, s>>>(T, k, latent, e, w, route_pos, gamma, eps, z, ldz);
+    else if (vpt == 2)
+        k_combine_rmsnorm<TA, 2><<<T, threads, 0, s>>>(T, k, latent, e, w, route_pos, gamma, eps, z, ldz);
+    else
+        k_combine_rmsnorm<TA, 4><<<T, threads, 0, s>>>(T, k, latent, e, w, route_pos, gamma, eps, z, ldz);
+    return QBMOE_OK;
 }
 
 }  // namespace
@@ -163,13 +195,14 @@ int launch_combine_rmsnorm(int act_dtype, int T, int k, int latent, const void* 
                            const int* route_pos, const float* gamma, float eps, void* z, long long ldz,
                            cudaStream_t s, int* nl) {
     const int V = act_dtype == QBMOE_BF16 ? 8 : 4;
-    if (latent % V || latent / V > kCombThreads * kCombMaxVec || !aligned16(gamma)) return QBMOE_EINVAL;
+    if (latent % V || k > QBMOE_MAX_TOPK || !aligned16(gamma)) return QBMOE_EINVAL;
+    int rc;
     if (act_dtype == QBMOE_BF16)
-        k_combine_rmsnorm<__nv_bfloat16><<<T, kCombThreads, 0, s>>>(T, k, latent, (const __nv_bfloat16*)e, w,
-                                                                     route_pos, gamma, eps, (__nv_bfloat16*)z, ldz);
+        rc = launch_combine_t<__nv_bfloat16>(T, k, latent, (const __nv_bfloat16*)e, w, route_pos, gamma, eps,
+                                             (__nv_bfloat16*)z, ldz, s);
     else
-        k_combine_rmsnorm<float><<<T, kCombThreads, 0, s>>>(T, k, latent, (const float*)e, w, route_pos, gamma, eps,
-                                                             (float*)z, ldz);
+        rc = launch_combine_t<float>(T, k, latent, (const float*)e, w, route_pos, gamma, eps, (float*)z, ldz, s);
+    if (rc) return rc;
     if (nl) ++*nl;
     return cuda_err(cudaGetLastError());
 }
