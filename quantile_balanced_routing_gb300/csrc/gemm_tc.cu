@@ -175,6 +175,22 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_t
 // quarter q of this warp, 16-column chunks staged through SMEM, epilogue
 // math, 16-byte global stores.  f_base is the output feature of TMEM lane 0;
 // tacc the accumulator's TMEM column base.
+// SiTU-GLU for the tensor-core epilogues, whose results are stored as bf16
+// (or E4M3 pairs of bf16): a = b1 tanh(g / b1), b = b2 tanh(u / b2),
+// out = a sigmoid(a) b with sigmoid(a) = (1 + tanh(a / 2)) / 2, the three
+// tanh on the hardware approximation (tanh.approx.f32, relative error about
+// 2^-11, below the bf16 rounding that follows).
+__device__ __forceinline__ float tanh_hw(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float situ_glu_hw(float g, float u, float b1, float inv_b1, float b2, float inv_b2) {
+    const float a = b1 * tanh_hw(g * inv_b1);
+    const float b = b2 * tanh_hw(u * inv_b2);
+    return a * fmaf(0.5f, tanh_hw(0.5f * a), 0.5f) * b;
+}
+
 // lo_col > 0 (block-scaled, stacked token planes): the accumulator holds
 // W * hi in columns [0, n) and W * lo in [lo_col, lo_col + n); the result is
 // hi + lo * 2^-kLoShift.
@@ -236,12 +252,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
             const int j = et >> 3, fg = et & 7;
             const int f = f_base + fg * 8;
             if (j < tok_left && f < sg.F) {
+                const float inv_b1 = 1.0f / p.beta1, inv_b2 = 1.0f / p.beta2;
                 float a[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const float g = st[(fg * 8 + u) * kStLd + j];
                     const float up = st[(64 + fg * 8 + u) * kStLd + j];
-                    a[u] = situ_glu(g, up, p.beta1, p.beta2);
+                    a[u] = situ_glu_hw(g, up, p.beta1, inv_b1, p.beta2, inv_b2);
                 }
                 const long long off = (long long)(ti.row0 + c0 + j) * sg.ldo + f;
                 if (sg.out_e4m3) {
