@@ -1034,6 +1034,7 @@ __global__ void k_gather_rows(const uint4* __restrict__ src, int vec_per_row, co
 template <int BN> struct Stages;
 template <> struct Stages<16> { static constexpr int S = 11; };
 template <> struct Stages<64> { static constexpr int S = 8; };
+template <> struct Stages<128> { static constexpr int S = 6; };
 template <> struct Stages<160> { static constexpr int S = 5; };
 template <> struct Stages<256> { static constexpr int S = 4; };
 
@@ -1262,6 +1263,7 @@ int launch_any(int BN, TcParams& prm, int grid, cudaStream_t s) {
     switch (BN) {
         case 16: return launch_bn<16, MODE_BF16>(prm, grid, s);
         case 64: return launch_bn<64, MODE_BF16>(prm, grid, s);
+        case 128: return launch_bn<128, MODE_BF16>(prm, grid, s);
         case 160: return launch_bn<160, MODE_BF16>(prm, grid, s);
         case 256: return launch_bn<256, MODE_BF16>(prm, grid, s);
         default: return QBMOE_EINVAL;
@@ -1277,10 +1279,18 @@ void base_params(TcPlan* P, TcParams& prm, int* status) {
     prm.stall_first_tile = P->stall;
 }
 
-// Token tile of a dense launch: 256 rows unless that leaves too few tiles.
-int dense_bn(long long m_tiles_128, int T) {
-    if (m_tiles_128 * ((T + 255) / 256) < 64) return T <= 16 ? 16 : 64;
-    return 256;
+// Token tile of a dense launch.  With many waves of tiles (prefill) 256 rows
+// move the fewest bytes per flop.  Otherwise the launch is a weight stream
+// (decode): take the tile that still fits one wave with the most tiles, so
+// that as many SMs as possible stream weights.
+int dense_bn(long long m_tiles_128, int T, int num_sms) {
+    const auto tiles = [&](int bn) { return m_tiles_128 * ((T + bn - 1) / bn); };
+    if (tiles(256) >= 2LL * num_sms) return 256;
+    int best = 256;
+    for (int bn : {128, 64})
+        if (tiles(bn) <= num_sms && tiles(bn) > tiles(best)) best = bn;
+    if (T <= 16) return 16;
+    return best;
 }
 
 // Whether a launch with token tile BN runs on the 2-SM kernel.
@@ -1380,7 +1390,7 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, v
     const qbmoe_config& c = P->cfg;
     const long long m128 = (with_router ? (c.n_experts + 127) / 128 : 0) + (c.latent + 127) / 128 +
                            (c.shared_inter + 63) / 64;
-    const int BN = dense_bn(m128, T);
+    const int BN = dense_bn(m128, T, P->num_sms);
     const bool pair = use_pair(P, BN, false);
     TcParams prm;
     base_params(P, prm, status);
@@ -1541,7 +1551,7 @@ int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const 
 int tc_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, int* status, cudaStream_t s,
                  int* nl) {
     const qbmoe_config& c = P->cfg;
-    const int BN = dense_bn((c.d + 127) / 128, T);
+    const int BN = dense_bn((c.d + 127) / 128, T, P->num_sms);
     const bool pair = use_pair(P, BN, false);
     TcParams prm;
     base_params(P, prm, status);
