@@ -182,7 +182,8 @@ typedef struct {
  *   w_down [latent, d]
  *   w_gate, w_up [n, m, latent]; w_out [n, latent, m]    (expert_wfmt)
  *     MXFP4: values packed two per byte (element 2i in the low nibble) as
- *     [rows, K/2] u8, scales E8M0 [rows, K/32] u8 in s_gate/s_up/s_out.
+ *     [rows, K/2] u8 with 32-byte aligned bases, scales E8M0 [rows, K/32]
+ *     u8 in s_gate/s_up/s_out (tensor-core path: K a multiple of 512).
  *   rms_gamma [latent] fp32
  *   w_proj_up [d, latent]
  *   w_shared_gate, w_shared_up [m_s, d]; w_shared_out [d, m_s]  (m_s > 0)
@@ -228,7 +229,12 @@ int qbmoe_destroy(qbmoe_ctx* ctx);
  *   z   = round(RMSNorm(sum_i w_i e_i) * gamma)                   [K3-width] Q&A RMSNorm
  *   out = round(z W_proj_up^T + act_s W_shared_out^T),
  *         act_s = round(SiTU-GLU(x W_shared_gate^T, x W_shared_up^T))   Q&A shared expert
- * ("round" = to act_dtype; accumulation is fp32.)
+ * ("round" = to act_dtype; accumulation is fp32.  With bf16 activations the
+ * tensor-core SiTU epilogues use the hardware tanh approximation, relative
+ * error about 2^-11, below the bf16 rounding.  MXFP4 experts run on the
+ * block-scaled MMA: each bf16 activation a enters as e4m3(a) + e4m3(16 (a -
+ * e4m3(a))) / 16, which is exact for 2^-6 <= |a| <= 448; magnitudes above
+ * 448 saturate.)
  *
  * x [T, d] act_dtype device; out [T, d] act_dtype device.
  * logits_in: NULL, or [T, n] fp32 device router logits used instead of the

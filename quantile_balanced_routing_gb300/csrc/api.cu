@@ -218,6 +218,11 @@ extern "C" int qbmoe_set_weights(qbmoe_ctx* c, const qbmoe_weights* w) {
                           w->rms_gamma, w->w_proj_up, w->w_shared_gate, w->w_shared_up, w->w_shared_out};
     for (const void* p : ptrs)
         if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
+    // Packed E2M1 weights are read by TMA copies that unpack 4-bit codes,
+    // which need 32-byte aligned bases.
+    if (g.expert_wfmt == QBMOE_W_MXFP4)
+        for (const void* p : {w->w_gate, w->w_up, w->w_out})
+            if ((reinterpret_cast<uintptr_t>(p) & 31u) != 0) return QBMOE_EINVAL;
     c->w = *w;
     c->have_weights = true;
     int rc = qbh::tc_plan_set_weights(c->tc, c->cfg, *w);

@@ -94,3 +94,4 @@ def test_null_context_calls(lib):
     assert lib.moe_latent_forward(None, 4, FAKE, None, None, None, FAKE, None, None, None, None, None) == Q.QBMOE_EINVAL
     assert lib.qbmoe_set_weights(None, None) == Q.QBMOE_EINVAL
     assert lib.qbmoe_set_timing(None, 1) == Q.QBMOE_EINVAL
+

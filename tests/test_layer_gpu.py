@@ -45,6 +45,23 @@ def test_mxfp4_layers_run_on_tensor_cores():
     lay.close()
 
 
+def test_mxfp4_weights_need_32_byte_alignment():
+    """Packed E2M1 weights are read by unpacking TMA copies that need 32-byte
+    aligned bases: qbmoe_set_weights refuses a base that is only 16-byte
+    aligned (a host-side check; the layer is not run)."""
+    import quantile_balanced_routing_gb300 as Q
+    from qb_inputs.device import layer_for, upload
+    d = upload(QI.LayerInputs(TC_MXFP4), "cuda:0")
+    w = {k: v for k, v in d.items() if k != "x"}
+    lay = layer_for(TC_MXFP4)
+    lay.set_weights(**w)
+    w["w_up"] = w["w_up"].view(torch.uint8).flatten()[16:]    # base 16 bytes past a 32-byte boundary
+    with pytest.raises(Q.QbmoeError) as err:
+        lay.set_weights(**w)
+    assert err.value.code == Q.QBMOE_EINVAL
+    lay.close()
+
+
 def test_bf16_layers_run_on_tensor_cores(monkeypatch):
     from qb_inputs.device import layer_for
     lay = layer_for(SMALL_BF16)
