@@ -45,6 +45,7 @@ struct qbmoe_ctx {
     size_t ws_bytes = 0;
     // workspace views
     float* scores = nullptr;
+    float* logits = nullptr;   // router GEMM output (logit + offset) [T, n] fp32
     qbh::RouteBuffers rb{};
     int32_t* idx = nullptr;
     float* wts = nullptr;
@@ -86,6 +87,7 @@ size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
     const size_t routes = (size_t)T * k;
     const size_t a = elt(c.act_dtype);
     char* p_scores = take((size_t)T * n * 4);
+    char* p_logits = take((size_t)T * n * 4);
     const size_t rbytes = qbh::route_ws_layout(T, n, k, nullptr, nullptr);
     char* p_route = take(rbytes);
     char* p_idx = take(routes * 4);
@@ -104,6 +106,7 @@ size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
     char* p_status = take(256);
     if (x && base) {
         x->scores = (float*)p_scores;
+        x->logits = (float*)p_logits;
         qbh::route_ws_layout(T, n, k, &x->rb, p_route);
         x->idx = (int32_t*)p_idx;
         x->wts = (float*)p_w;
@@ -327,27 +330,24 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     StageClock clk{c, s};
     const bool use_tc = qbh::tc_enabled(c->tc);
 
-    // 1. router scores (tensor-core path: fused with the other x-side GEMMs)
+    // 1. router logits x W_r^T + o (tensor-core path: fused with the other
+    //    x-side GEMMs), unless the caller gives them
+    const float* logits = logits_in ? logits_in : c->logits;
     if (use_tc) {
         clk.mark("xside_gemm");
-        if (logits_in) rc = qbh::launch_scores(logits_in, c->scores, (long long)T * n, s, &nl);
-        if (!rc) rc = qbh::tc_xside(c->tc, T, x, logits_in == nullptr, c->scores, c->h, c->zcat, ldz, c->status, s, &nl);
-    } else {
+        rc = qbh::tc_xside(c->tc, T, x, logits_in == nullptr, c->logits, c->h, c->zcat, ldz, c->status, s, &nl);
+    } else if (!logits_in) {
         clk.mark("router");
-        if (logits_in) {
-            rc = qbh::launch_scores(logits_in, c->scores, (long long)T * n, s, &nl);
-        } else {
-            qbh::GemmArgs ga;
-            ga.A = x; ga.lda = d; ga.rows = T; ga.K1 = d; ga.W1 = c->w.w_router; ga.F = n;
-            ga.out = c->scores; ga.ldo = n; ga.col_bias = c->w.router_offset;
-            rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_ROUTER, ga, s, &nl);
-        }
+        qbh::GemmArgs ga;
+        ga.A = x; ga.lda = d; ga.rows = T; ga.K1 = d; ga.W1 = c->w.w_router; ga.F = n;
+        ga.out = c->logits; ga.ldo = n; ga.col_bias = c->w.router_offset;
+        rc = qbh::launch_gemm_simt(ad, dense_wf, qbh::EPI_ROUTER, ga, s, &nl);
     }
     if (rc) return rc;
 
-    // 2-3. QB sweeps and biased top-k
+    // 2-3. scores (in the first QB token pass), QB sweeps and biased top-k
     clk.mark("qb_topk");
-    rc = qbh::launch_qb_and_topk(T, n, k, g.qb_sweeps, nullptr, c->scores, bias_in, bias_out, c->idx, c->wts,
+    rc = qbh::launch_qb_and_topk(T, n, k, g.qb_sweeps, logits, c->scores, bias_in, bias_out, c->idx, c->wts,
                                  c->rb.blk_cnt, c->rb, s, &nl);
     if (rc) return rc;
 

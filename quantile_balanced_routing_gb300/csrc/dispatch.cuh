@@ -23,7 +23,8 @@ enum GemmEpi { EPI_STORE = 0, EPI_ROUTER = 1, EPI_SITU = 2 };
 //   W: for k < K1 from W1 [F, K1], for k >= K1 from W2 [F, K2] (dense, act
 //      dtype).  Grouped: expert g's weights start at W1 + g * F * K1 (wfmt);
 //      MXFP4 weights use S1 (scales).  EPI_SITU also reads Wu/Su (up branch).
-//   out: row r at out + r * ldo (act dtype; fp32 for EPI_ROUTER).
+//   out: row r at out + r * ldo (act dtype; for EPI_ROUTER the fp32 logit
+//        plus col_bias, from which the QB token pass takes the score).
 struct GemmArgs {
     const void* A = nullptr;
     long long lda = 0;

@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(GemmArgs p) {
             if (f >= p.F) continue;
             float v;
             if (EPI == qbh::EPI_ROUTER) {
-                const float logit = p.col_bias ? __fadd_rn(acc[i][j], p.col_bias[f]) : acc[i][j];
-                v = score_of_logit(logit);
+                // router logit + offset; the QB token pass takes the score from it
+                v = p.col_bias ? __fadd_rn(acc[i][j], p.col_bias[f]) : acc[i][j];
             } else if (EPI == qbh::EPI_SITU) {
                 v = situ_glu(acc[i][j], accu[i][j], p.beta1, p.beta2);
             } else {

@@ -33,7 +33,7 @@
 // records QBMOE_ETIMEOUT, stops, drains its own TMA/MMA work (bounded) and
 // frees TMEM.
 //
-// Epilogues per sub-GEMM: STORE (bf16), ROUTER (fp32 score of logit + offset)
+// Epilogues per sub-GEMM: STORE (bf16), ROUTER (fp32 logit + offset)
 // and SITU (A tile = 64 gate rows over 64 up rows of the same features;
 // act = SiTU-GLU(gate, up), stored as bf16 or as E4M3 pairs).
 #include "gemm_tc.cuh"
@@ -242,7 +242,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
                     for (int u = 0; u < 4; ++u) {
                         float lg = st[(fg * 4 + u) * kStLd + j];
                         if (sg.col_bias) lg = __fadd_rn(lg, sg.col_bias[f + u]);
-                        op[u] = score_of_logit(lg);
+                        op[u] = lg;   // the score is taken from this logit by the QB token pass
                     }
                     *reinterpret_cast<float4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) = o;
                 }
@@ -1385,7 +1385,7 @@ static int m_tiles_of(int F, bool situ, bool pair) {
     return (F + rows - 1) / rows;
 }
 
-int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, void* h, void* zcat, long long ldz,
+int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, void* h, void* zcat, long long ldz,
              int* status, cudaStream_t s, int* nl) {
     const qbmoe_config& c = P->cfg;
     const long long m128 = (with_router ? (c.n_experts + 127) / 128 : 0) + (c.latent + 127) / 128 +
@@ -1398,7 +1398,7 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* scores, v
     if (with_router) {
         SubGemm& r = prm.sub[ns];
         r.epi = SUB_ROUTER; r.F = c.n_experts; r.m_tiles = m_tiles_of(c.n_experts, false, pair); r.m_begin = m;
-        r.k_split = 1 << 30; r.out = scores; r.ldo = c.n_experts; r.col_bias = P->w.router_offset;
+        r.k_split = 1 << 30; r.out = logits; r.ldo = c.n_experts; r.col_bias = P->w.router_offset;
         if (!make_map(P, &prm.a0[ns], P->w.w_router, c.n_experts, c.d, c.d, 128)) return QBMOE_ECUDA;
         prm.a1[ns] = prm.a0[ns];
         m += r.m_tiles;

@@ -17,8 +17,9 @@ int tc_token_tile(const TcPlan* p, int T);
 void tc_set_wait_limit(TcPlan* p, long long iterations);
 void tc_set_stall(TcPlan* p, int on);
 
-// Router (optional) + latent down-projection + shared gate/up in one launch.
-int tc_xside(TcPlan* p, int T, const void* x, bool with_router, float* scores, void* h, void* zcat, long long ldz,
+// Router logits (optional; fp32 x W_r^T + o) + latent down-projection +
+// shared gate/up in one launch.
+int tc_xside(TcPlan* p, int T, const void* x, bool with_router, float* logits, void* h, void* zcat, long long ldz,
              int* status, cudaStream_t s, int* nl);
 // dst[r] = src[rows[r]] for r < n_rows (bf16 rows of `cols` elements).
 int tc_gather(const void* src, int cols, const int* rows, int n_rows, void* dst, cudaStream_t s, int* nl);
