@@ -330,6 +330,7 @@ template <int BN, int S, int MODE>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_constant__ TcParams p) {
     constexpr bool MX = MODE == MODE_MX_DECODE;    // MXFP4 decoded to bf16 by converter warps
     constexpr bool MXS = MODE == MODE_MX_SCALED;   // MXFP4 on the block-scaled MMA, E4M3 tokens
+    constexpr bool kTestFirst = MODE == MODE_BF16;  // waits start with a non-blocking test
     constexpr int kKS = MXS ? kBKS : kBK;          // K elements per stage
     constexpr int kPlane = BN * 128;               // token tile: BN rows of 128 bytes
     constexpr int kBBytes = MXS ? 2 * kPlane : kPlane;   // block-scaled: hi and lo planes
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         if (++s == S) { s = 0; ph ^= 1u; }
                         continue;
                     }
-                    if (!tc::mbar_wait(&emptyx[s], ph ^ 1u, lim)) {
+                    if (!tc::mbar_wait<kTestFirst>(&emptyx[s], ph ^ 1u, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         break;
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         constexpr int sgrp = MX ? kScaleGroup : kScaleGroupS;
                         if (kb % sgrp == 0) {
                             const int slot = gidx & 1;
-                            if (!tc::mbar_wait(&emptyS[slot], ((gidx >> 1) & 1) ^ 1u, lim)) {
+                            if (!tc::mbar_wait<kTestFirst>(&emptyS[slot], ((gidx >> 1) & 1) ^ 1u, lim)) {
                                 set_status(p.status, QBMOE_ETIMEOUT);
                                 *abort_flag = 1;
                                 break;
@@ -538,9 +539,9 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         // drain: every TMA this thread issued has landed before SMEM is released
         if (lane == 0 && *abort_flag) {
             for (int s = 0; s < S; ++s)
-                if ((issued >> s) & 1u) tc::mbar_wait(&fullx[s], (last_par >> s) & 1u, kDrainWait);
+                if ((issued >> s) & 1u) tc::mbar_wait<kTestFirst>(&fullx[s], (last_par >> s) & 1u, kDrainWait);
             for (int g = 0; g < 2; ++g)
-                if ((sc_issued >> g) & 1u) tc::mbar_wait(&fullS[g], (sc_par >> g) & 1u, kDrainWait);
+                if ((sc_issued >> g) & 1u) tc::mbar_wait<kTestFirst>(&fullS[g], (sc_par >> g) & 1u, kDrainWait);
         }
     } else if (MX && warp >= kConvFirstWarp) {
         // ------------------------------------------------- MXFP4 converters
@@ -557,8 +558,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 const int slot = gidx & 1;
                 int w = 1;
                 if (lane == 0) {
-                    if (kb % kScaleGroup == 0) w = tc::mbar_wait(&fullS[slot], (gidx >> 1) & 1u, lim);
-                    if (w) w = tc::mbar_wait(&fullP[s], ph, lim);
+                    if (kb % kScaleGroup == 0) w = tc::mbar_wait<kTestFirst>(&fullS[slot], (gidx >> 1) & 1u, lim);
+                    if (w) w = tc::mbar_wait<kTestFirst>(&fullP[s], ph, lim);
                     if (!w) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
@@ -633,9 +634,9 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 const int slot = gidx & 1;
                 int w = 1;
                 if (lane == 0) {
-                    if (kb % kScaleGroupS == 0) w = tc::mbar_wait(&fullS[slot], (gidx >> 1) & 1u, lim);
+                    if (kb % kScaleGroupS == 0) w = tc::mbar_wait<kTestFirst>(&fullS[slot], (gidx >> 1) & 1u, lim);
                     // the slot is free once the MMAs of the stage's last use completed
-                    if (w) w = tc::mbar_wait(&empty[s], ph ^ 1u, lim);
+                    if (w) w = tc::mbar_wait<kTestFirst>(&empty[s], ph ^ 1u, lim);
                     if (!w) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
@@ -674,7 +675,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
                 const uint32_t n_eff = (ti.nrows + 15) & ~15;
                 const uint32_t idesc = tc::idesc_bf16_m128(n_eff);
-                if (!tc::mbar_wait(&acce[ab], aph ^ 1u, lim)) {
+                if (!tc::mbar_wait<kTestFirst>(&acce[ab], aph ^ 1u, lim)) {
                     set_status(p.status, QBMOE_ETIMEOUT);
                     *abort_flag = 1;
                     break;
@@ -683,7 +684,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 const uint32_t d = tbase + ab * kAccCols;
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait(&full[sa], pha, lim)) {
+                    if (!tc::mbar_wait<kTestFirst>(&full[sa], pha, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         ok = false;
@@ -715,7 +716,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             }
             // all MMAs issued by this thread complete before TMEM is freed
             tc::tc_commit(drain);
-            tc::mbar_wait(drain, 0, kDefaultWait);
+            tc::mbar_wait<kTestFirst>(drain, 0, kDefaultWait);
         }
         __syncwarp();
         __syncthreads();
@@ -732,7 +733,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             const SubGemm& sg = p.sub[ti.sub];
             // one thread waits; the verdict is shared so the 128 threads stay uniform
             if (et == 0) {
-                const bool ok = tc::mbar_wait(&accf[ab], aph, lim);
+                const bool ok = tc::mbar_wait<kTestFirst>(&accf[ab], aph, lim);
                 if (!ok) {
                     set_status(p.status, QBMOE_ETIMEOUT);
                     *abort_flag = 1;
@@ -852,7 +853,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
                         if (++s == S) { s = 0; ph ^= 1u; }
                         continue;
                     }
-                    if (!tc::mbar_wait(&emptyx[s], ph ^ 1u, lim)) {
+                    if (!tc::mbar_wait<true>(&emptyx[s], ph ^ 1u, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         break;
@@ -896,7 +897,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
         if (lane == 0 && *abort_flag) {
             if (leader) {
                 for (int s = 0; s < S; ++s)
-                    if ((issued >> s) & 1u) tc::mbar_wait(&fullx[s], (last_par >> s) & 1u, kDrainWait);
+                    if ((issued >> s) & 1u) tc::mbar_wait<true>(&fullx[s], (last_par >> s) & 1u, kDrainWait);
             } else {
                 // this CTA's copies signal the leader's barriers: give them time to land
                 for (int i = 0; i < 200; ++i) __nanosleep(10000);
@@ -913,7 +914,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
                 decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
                 const uint32_t n_eff = (ti.nrows + 15) & ~15;
                 const uint32_t idesc = tc::idesc_bf16_m256(n_eff);
-                if (!tc::mbar_wait(&acce[ab], aph ^ 1u, lim)) {
+                if (!tc::mbar_wait<true>(&acce[ab], aph ^ 1u, lim)) {
                     set_status(p.status, QBMOE_ETIMEOUT);
                     *abort_flag = 1;
                     break;
@@ -922,7 +923,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
                 const uint32_t d = tbase + ab * BN;
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait(&full[sa], pha, lim)) {
+                    if (!tc::mbar_wait<true>(&full[sa], pha, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         ok = false;
@@ -945,7 +946,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
                 if (ab == 0) aph ^= 1u;
             }
             tc::tc_commit_pair(drain, 0x1);
-            tc::mbar_wait(drain, 0, kDefaultWait);
+            tc::mbar_wait<true>(drain, 0, kDefaultWait);
         }
         __syncwarp();
         __syncthreads();
@@ -960,7 +961,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
             decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
             const SubGemm& sg = p.sub[ti.sub];
             if (et == 0) {
-                const bool ok = tc::mbar_wait(&accf[ab], aph, lim);
+                const bool ok = tc::mbar_wait<true>(&accf[ab], aph, lim);
                 if (!ok) {
                     set_status(p.status, QBMOE_ETIMEOUT);
                     *abort_flag = 1;

@@ -42,9 +42,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false after `limit` unsuccessful polls (at most limit * kSuspendNs).
+// Non-blocking test of the phase with `parity`.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete: with
+// kTestFirst one non-blocking test, then suspending polls.  Returns false
+// after `limit` unsuccessful polls (at most limit * kSuspendNs).  (Measured:
+// the test first helps the bf16 weight-streaming GEMMs and slows the
+// block-scaled ones.)
+template <bool kTestFirst = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
+    if (kTestFirst && mbar_test(bar, parity)) return true;
     for (long long i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
