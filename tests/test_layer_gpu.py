@@ -26,11 +26,16 @@ TC_MXFP4 = QI.LayerShape("tc_mxfp4", T=300, d=1024, latent=512, n=64, k=8, m=512
                          dtype="bf16", wfmt="mxfp4", offset_var=1.0)
 TC_MXFP4_DECODE_LIKE = TC_MXFP4.with_(name="tc_mxfp4_decode_like", T=64)
 TC_MXFP4_PREFILL_LIKE = TC_MXFP4.with_(name="tc_mxfp4_prefill_like", T=1200, n=32, offset_var=2.0)
+# edge cases of the tensor-core tilings: one token (a 1-row tile through the
+# stacked block-scaled MMA), two tokens on bf16 weights
+TC_MXFP4_ONE_TOKEN = TC_MXFP4.with_(name="tc_mxfp4_one_token", T=1)
+TC_TWO_TOKENS = TC_DECODE_LIKE.with_(name="tc_two_tokens", T=2)
 
 
 @pytest.mark.parametrize("shape", [QI.TINY_F32, RAGGED_F32, SMALL_BF16, SMALL_MXFP4, FROZEN_BF16, ONE_TOKEN,
                                    TC_DECODE_LIKE, TC_PREFILL_LIKE, TC_MXFP4, TC_MXFP4_DECODE_LIKE,
-                                   TC_MXFP4_PREFILL_LIKE], ids=lambda s: s.name)
+                                   TC_MXFP4_PREFILL_LIKE, TC_MXFP4_ONE_TOKEN, TC_TWO_TOKENS],
+                         ids=lambda s: s.name)
 def test_layer_fed_logits(shape):
     compare_fed(shape)
 
