@@ -171,6 +171,56 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_t
     ti.mt = m - p.sub[s].m_begin;
 }
 
+// Walks a grouped launch's tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// without a division or a search per tile: the (token tile, m-tile) pair
+// steps by gridDim.x and the expert of a token tile is found by scanning
+// forward from the previous one, since a CTA's tiles only move forward.
+// (decode_tile's division and binary search sat on the MMA thread's path
+// between tiles.)  Dense launches fall back to decode_tile.
+template <int BN>
+struct TileWalker {
+    int ntg = 0, m = 0, g = 0;
+    __device__ __forceinline__ void seek(const TcParams& p, const int* s_toff) {
+        while (g + 8 < p.n_groups && s_toff[g + 8] <= ntg) g += 8;
+        while (g + 1 < p.n_groups && s_toff[g + 1] <= ntg) ++g;
+    }
+    __device__ __forceinline__ void start(const TcParams& p, const int* s_toff) {
+        if (p.n_groups > 0) {
+            ntg = blockIdx.x / p.m_total;
+            m = blockIdx.x - ntg * p.m_total;
+            g = 0;
+            seek(p, s_toff);
+        }
+    }
+    __device__ __forceinline__ void next(const TcParams& p, const int* s_toff) {
+        if (p.n_groups > 0) {
+            m += gridDim.x;
+            while (m >= p.m_total) { m -= p.m_total; ++ntg; }
+            seek(p, s_toff);
+        }
+    }
+    __device__ __forceinline__ void get(const TcParams& p, int tile, int n_tiles_dense, const int* s_toff,
+                                        const int* s_seg, TileInfo& ti) const {
+        if (p.n_groups == 0) {
+            decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+            return;
+        }
+        // the expert's rows split into equal tiles (multiples of 16 rows), as in decode_tile
+        ti.g = g;
+        const int nt = ntg - s_toff[g];
+        const int ntiles = s_toff[g + 1] - s_toff[g];
+        const int seg0 = s_seg[g], seg1 = s_seg[g + 1];
+        const int len = seg1 - seg0;
+        const int per = ((ntiles == 1 ? len : (len + ntiles - 1) / ntiles) + 15) & ~15;
+        ti.row0 = seg0 + nt * per;
+        ti.nrows = min(per, seg1 - ti.row0);
+        int sb = 0;
+        while (sb + 1 < p.n_sub && m >= p.sub[sb + 1].m_begin) ++sb;
+        ti.sub = sb;
+        ti.mt = m - p.sub[sb].m_begin;
+    }
+};
+
 // Epilogue of one accumulator tile by the 128 epilogue threads: TMEM lane
 // quarter q of this warp, 16-column chunks staged through SMEM, epilogue
 // math, 16-byte global stores.  f_base is the output feature of TMEM lane 0;
@@ -433,9 +483,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+            TileWalker<BN> tw;
+            tw.start(p, s_toff);
+            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p, s_toff)) {
                 TileInfo ti;
-                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                tw.get(p, tile, n_tiles_dense, s_toff, s_seg, ti);
                 const SubGemm& sg = p.sub[ti.sub];
                 const int n_eff = (ti.nrows + 15) & ~15;
                 for (int kb = 0; kb < p.nkb; ++kb) {
@@ -670,9 +722,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             uint32_t pha = 0;
             int ab = 0;
             uint32_t aph = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+            TileWalker<BN> tw;
+            tw.start(p, s_toff);
+            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p, s_toff)) {
                 TileInfo ti;
-                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                tw.get(p, tile, n_tiles_dense, s_toff, s_seg, ti);
                 const uint32_t n_eff = (ti.nrows + 15) & ~15;
                 const uint32_t idesc = tc::idesc_bf16_m128(n_eff);
                 if (!tc::mbar_wait<kTestFirst>(&acce[ab], aph ^ 1u, lim)) {
@@ -727,9 +781,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         int ab = 0;
         uint32_t aph = 0;
         volatile int* ok_slot = abort_flag + 1;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        TileWalker<BN> tw;
+        tw.start(p, s_toff);
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, tw.next(p, s_toff)) {
             TileInfo ti;
-            decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+            tw.get(p, tile, n_tiles_dense, s_toff, s_seg, ti);
             const SubGemm& sg = p.sub[ti.sub];
             // one thread waits; the verdict is shared so the 128 threads stay uniform
             if (et == 0) {
