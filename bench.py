@@ -48,11 +48,17 @@ def peaks():
 
 
 def kernel_source_sha256():
+    """Hash of the tensor-core kernel's code (comments and whitespace removed,
+    so that a recorded traffic figure survives edits of comments only)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("gemm_tc.cu", "tc_ptx.cuh"):
-        with open(os.path.join(ROOT, "quantile_balanced_routing_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "quantile_balanced_routing_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()
 
 

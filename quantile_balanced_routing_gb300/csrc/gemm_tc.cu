@@ -51,6 +51,7 @@ namespace {
 
 using namespace qb;
 
+// (MXFP4-decode mode has one producer pair; its converter warps start at 7.)
 constexpr int kProdAWarp = 0, kProdBWarp = 1, kMmaWarp = 2, kEpiFirstWarp = 3, kConvFirstWarp = 7;
 // Second producer pair (bf16 and block-scaled modes, and the 2-SM kernel):
 // producer pair p issues the weight and token tiles of the K blocks with
@@ -82,8 +83,9 @@ enum { SUB_STORE = 0, SUB_ROUTER = 1, SUB_SITU = 2 };
 enum { MODE_BF16 = 0, MODE_MX_DECODE = 1, MODE_MX_SCALED = 2 };
 
 // Block-scaled MMAs take fp8 tokens, so a bf16 activation a enters as two
-// E4M3 terms, a = hi + lo / 16 with hi = e4m3(a) and lo = e4m3(16 (a - hi)),
-// multiplied with the token scales 2^0 and 2^-4.  For bf16 a with
+// E4M3 terms, a = hi + lo / 16 with hi = e4m3(a) and lo = e4m3(16 (a - hi));
+// the lo rows are stacked under the hi rows in one MMA and the epilogue
+// combines the two accumulators as hi + lo / 16.  For bf16 a with
 // 2^-6 <= |a| <= 448 both terms are exact (the residual has at most four
 // significant bits), so the product is that of the bf16 activation; smaller
 // magnitudes keep an absolute error below 2^-14 and larger ones saturate.
