@@ -738,6 +738,17 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 }
                 tc::tc_fence_after();
                 const uint32_t d = tbase + ab * kAccCols;
+                // Descriptors step by plain adds: the start-address field holds
+                // address / 16, so a 32-byte K step is +2 and a stage is
+                // +stage_bytes / 16 (addresses stay below 256 KB, inside the
+                // 14-bit field).  At small N the issuing thread, not the tensor
+                // pipe, sets the pace, so the loop keeps its arithmetic minimal.
+                const uint64_t a_desc0 = tc::desc_sw128(tc::smem_u32(a_ring));
+                const uint64_t b_desc0 = tc::desc_sw128(tc::smem_u32(b_ring));
+                uint32_t id_k[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    id_k[kk] = MXS ? tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, kk, 0) : idesc;
                 bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
                     if (!tc::mbar_wait<kTestFirst>(&full[sa], pha, lim)) {
@@ -747,19 +758,18 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
-                    const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
+                    const uint64_t ad = a_desc0 + (uint64_t)(sa * (kATileBytes >> 4));
+                    const uint64_t bd = b_desc0 + (uint64_t)(sa * (kBBytes >> 4));
+                    const uint32_t sfa = tbase + kSfaCol + 4 * sa;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         if (MXS) {
                             // 32-wide K slice kk (byte kk of the weight scale words)
                             // against the stacked hi and lo rows
-                            const uint32_t id = tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, kk, 0);
-                            tc::tc_mma_mxf8f6f4(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
-                                                id, tbase + kSfaCol + 4 * sa, tbase + kSfbCol, (kb | kk) != 0);
+                            tc::tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], sfa, tbase + kSfbCol,
+                                                (kb | kk) != 0);
                         } else {
-                            tc::tc_mma_bf16(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
-                                            idesc, (kb | kk) != 0);
+                            tc::tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], (kb | kk) != 0);
                         }
                     }
                     tc::tc_commit(&empty[sa]);
