@@ -363,11 +363,8 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     const size_t routes = (size_t)T * k;
     const int max_tiles = (int)((routes + tile_rows - 1) / tile_rows) + n;
     if (use_tc) {
-        if (qbh::tc_mx_scaled(c->tc))
-            rc = qbh::tc_gather_e4m3(c->h, L, c->perm, (int)routes, c->h_perm, s, &nl);
-        else
-            rc = qbh::tc_gather(c->h, L, c->perm, (int)routes, c->h_perm, s, &nl);
-        if (rc) return rc;
+        // h rows are bf16, or E4M3 pairs of the same width for block-scaled experts
+        if ((rc = qbh::tc_gather(c->h, L, c->perm, (int)routes, c->h_perm, s, &nl))) return rc;
         clk.mark("expert_gate_up");
         rc = qbh::tc_expert_gate_up(c->tc, T, c->h_perm, c->offsets, c->tile_off_simt, c->act, c->status, s, &nl);
         if (rc) return rc;

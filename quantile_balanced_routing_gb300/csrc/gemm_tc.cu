@@ -102,7 +102,7 @@ struct SubGemm {
     int m_tiles;        // tiles over F (128 rows, or 64 features for SITU)
     int m_begin;        // first global m index of this sub-GEMM
     int k_split;        // K blocks read from a0; the rest from a1 (ignored for SITU)
-    int out_e4m3;       // SITU output stored as an E4M3 pair (hi bytes at column f, lo at F + f)
+    int out_e4m3;       // STORE/SITU output stored as an E4M3 pair (hi bytes at column f, lo at F + f)
     void* out;
     long long ldo;
     const float* col_bias;
@@ -272,11 +272,24 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
                 const int j = item >> 4, fg = item & 15;
                 const int f = f_base + fg * 8;
                 if (j < tok_left && f < sg.F) {
-                    __align__(16) __nv_bfloat16 o[8];
+                    if (sg.out_e4m3) {
+                        // the bf16 value as an E4M3 pair: hi plane, then lo plane F bytes on
+                        __align__(8) uint8_t oh[8];
+                        __align__(8) uint8_t ol[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(st[(fg * 8 + u) * kStLd + j]);
-                    *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
-                        *reinterpret_cast<const uint4*>(o);
+                        for (int u = 0; u < 8; ++u)
+                            e4m3_pair(__bfloat162float(__float2bfloat16_rn(st[(fg * 8 + u) * kStLd + j])), oh[u],
+                                      ol[u]);
+                        uint8_t* o8 = static_cast<uint8_t*>(sg.out) + (long long)(ti.row0 + c0 + j) * sg.ldo + f;
+                        *reinterpret_cast<uint2*>(o8) = *reinterpret_cast<const uint2*>(oh);
+                        *reinterpret_cast<uint2*>(o8 + sg.F) = *reinterpret_cast<const uint2*>(ol);
+                    } else {
+                        __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(st[(fg * 8 + u) * kStLd + j]);
+                        *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
+                            *reinterpret_cast<const uint4*>(o);
+                    }
                 }
             }
         } else if (sg.epi == SUB_ROUTER) {
@@ -1064,28 +1077,6 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Row gather into E4M3 pairs: row r of dst holds the hi bytes of
-// src[rows[r]] in its first vec_per_row * 8 columns and the lo bytes after
-// them (e4m3_pair); 8 bf16 in, 2 x 8 bytes out per step.
-__global__ void k_gather_rows_e4m3(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ rows,
-                                   int n_rows, uint2* __restrict__ dst) {
-    const long long total = (long long)n_rows * vec_per_row;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long r = i / vec_per_row;
-        const int c = (int)(i - r * vec_per_row);
-        const uint4 v = src[(long long)__ldg(rows + r) * vec_per_row + c];
-        const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&v);
-        __align__(8) uint8_t oh[8];
-        __align__(8) uint8_t ol[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) e4m3_pair(__bfloat162float(b[u]), oh[u], ol[u]);
-        uint2* row = dst + r * 2 * vec_per_row;
-        row[c] = *reinterpret_cast<const uint2*>(oh);
-        row[vec_per_row + c] = *reinterpret_cast<const uint2*>(ol);
-    }
-}
-
 // Row gather: dst[r] = src[rows[r]] (16-byte vectors), r < n_rows.
 __global__ void k_gather_rows(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ rows,
                               int n_rows, uint4* __restrict__ dst) {
@@ -1477,6 +1468,12 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, v
         SubGemm& g = prm.sub[ns];
         g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = m_tiles_of(c.latent, false, pair); g.m_begin = m;
         g.k_split = 1 << 30; g.out = h; g.ldo = c.latent;
+        if (tc_mx_scaled(P)) {
+            // block-scaled experts read h as E4M3 pairs, converted once here
+            // rather than once per route in the dispatch gather
+            g.out_e4m3 = 1;
+            g.ldo = 2LL * c.latent;
+        }
         if (!make_map(P, &prm.a0[ns], P->w.w_down, c.latent, c.d, c.d, 128)) return QBMOE_ECUDA;
         prm.a1[ns] = prm.a0[ns];
         m += g.m_tiles;
@@ -1496,17 +1493,6 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, v
     prm.n_sub = ns;
     prm.m_total = m;
     return launch_dense(P, prm, BN, pair, T, x, c.d, c.d, s, nl);
-}
-
-int tc_gather_e4m3(const void* src, int cols, const int* perm, int n_rows, void* dst, cudaStream_t s, int* nl) {
-    // dst rows are 2 * cols bytes: hi plane, then lo plane
-    const int vpr = cols / 8;
-    const long long total = (long long)n_rows * vpr;
-    const int grid = (int)std::min<long long>((total + 255) / 256, 152LL * 8);
-    k_gather_rows_e4m3<<<std::max(grid, 1), 256, 0, s>>>(static_cast<const uint4*>(src), vpr, perm, n_rows,
-                                                         static_cast<uint2*>(dst));
-    if (nl) ++*nl;
-    return cuda_err(cudaGetLastError());
 }
 
 int tc_gather(const void* src, int cols, const int* perm, int n_rows, void* dst, cudaStream_t s, int* nl) {

@@ -18,14 +18,13 @@ void tc_set_wait_limit(TcPlan* p, long long iterations);
 void tc_set_stall(TcPlan* p, int on);
 
 // Router logits (optional; fp32 x W_r^T + o) + latent down-projection +
-// shared gate/up in one launch.
+// shared gate/up in one launch.  h is bf16 [T, latent], or E4M3 pairs (hi
+// plane, then lo plane: 2 x latent bytes a row) when the expert GEMMs run on
+// the block-scaled MMA.
 int tc_xside(TcPlan* p, int T, const void* x, bool with_router, float* logits, void* h, void* zcat, long long ldz,
              int* status, cudaStream_t s, int* nl);
-// dst[r] = src[rows[r]] for r < n_rows (bf16 rows of `cols` elements).
+// dst[r] = src[rows[r]] for r < n_rows (rows of 2 x `cols` bytes).
 int tc_gather(const void* src, int cols, const int* rows, int n_rows, void* dst, cudaStream_t s, int* nl);
-// The same gather converted to E4M3 bytes (the token operand of the
-// block-scaled MXFP4 expert GEMMs; cols % 8 == 0).
-int tc_gather_e4m3(const void* src, int cols, const int* rows, int n_rows, void* dst, cudaStream_t s, int* nl);
 // Whether the MXFP4 expert GEMMs run on the block-scaled MMA: their token
 // inputs (h_perm, act) are then E4M3 bytes.
 bool tc_mx_scaled(const TcPlan* p);
