@@ -1077,15 +1077,20 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Row gather: dst[r] = src[rows[r]] (16-byte vectors), r < n_rows.
-__global__ void k_gather_rows(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ rows,
-                              int n_rows, uint4* __restrict__ dst) {
-    const long long total = (long long)n_rows * vec_per_row;
+// Row copy in token order: dst[route_pos[t * k + i]] = src[t] for each of
+// token t's k routes (16-byte vectors).  Each source row is read once and
+// written k times; walking the destination rows instead re-reads every source
+// row k times, from DRAM once the rows have left L2.
+__global__ void k_scatter_rows(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ route_pos,
+                               int T, int k, uint4* __restrict__ dst) {
+    const long long total = (long long)T * vec_per_row;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
-        const long long r = i / vec_per_row;
-        const int c = (int)(i - r * vec_per_row);
-        dst[i] = src[(long long)__ldg(rows + r) * vec_per_row + c];
+        const long long t = i / vec_per_row;
+        const int c = (int)(i - t * vec_per_row);
+        const uint4 v = src[i];
+        const int* rp = route_pos + t * k;
+        for (int r = 0; r < k; ++r) dst[(long long)__ldg(rp + r) * vec_per_row + c] = v;
     }
 }
 
@@ -1495,12 +1500,13 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, v
     return launch_dense(P, prm, BN, pair, T, x, c.d, c.d, s, nl);
 }
 
-int tc_gather(const void* src, int cols, const int* perm, int n_rows, void* dst, cudaStream_t s, int* nl) {
+int tc_scatter_rows(const void* src, int cols, const int* route_pos, int T, int k, void* dst, cudaStream_t s,
+                    int* nl) {
     const int vpr = cols * 2 / 16;
-    const long long total = (long long)n_rows * vpr;
+    const long long total = (long long)T * vpr;
     const int grid = (int)std::min<long long>((total + 255) / 256, 152LL * 8);
-    k_gather_rows<<<std::max(grid, 1), 256, 0, s>>>(static_cast<const uint4*>(src), vpr, perm, n_rows,
-                                                    static_cast<uint4*>(dst));
+    k_scatter_rows<<<std::max(grid, 1), 256, 0, s>>>(static_cast<const uint4*>(src), vpr, route_pos, T, k,
+                                                     static_cast<uint4*>(dst));
     if (nl) ++*nl;
     return cuda_err(cudaGetLastError());
 }
