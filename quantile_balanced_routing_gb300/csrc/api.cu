@@ -364,7 +364,7 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     const int max_tiles = (int)((routes + tile_rows - 1) / tile_rows) + n;
     if (use_tc) {
         // h rows are bf16, or E4M3 pairs of the same width for block-scaled experts
-        if ((rc = qbh::tc_scatter_rows(c->h, L, c->route_pos, T, k, c->h_perm, s, &nl))) return rc;
+        if ((rc = qbh::launch_scatter_rows(c->h, 2 * L, c->route_pos, T, k, c->h_perm, s, &nl))) return rc;
         clk.mark("expert_gate_up");
         rc = qbh::tc_expert_gate_up(c->tc, T, c->h_perm, c->offsets, c->tile_off_simt, c->act, c->status, s, &nl);
         if (rc) return rc;

@@ -70,6 +70,23 @@ __global__ void k_scatter(int T, int n, int k, int tpw, const int32_t* __restric
     }
 }
 
+// Row copy in token order: dst[route_pos[t * k + i]] = src[t] for each of
+// token t's k routes (16-byte vectors).  Each source row is read once and
+// written k times; walking the destination rows instead re-reads every source
+// row k times, from DRAM once the rows have left L2.
+__global__ void k_scatter_rows(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ route_pos,
+                               int T, int k, uint4* __restrict__ dst) {
+    const long long total = (long long)T * vec_per_row;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / vec_per_row;
+        const int c = (int)(i - t * vec_per_row);
+        const uint4 v = src[i];
+        const int* rp = route_pos + t * k;
+        for (int r = 0; r < k; ++r) dst[(long long)__ldg(rp + r) * vec_per_row + c] = v;
+    }
+}
+
 // y = sum_i w[t,i] * e[route_pos[t,i]] (fp32); z = y / sqrt(mean(y^2) + eps) * gamma.
 // One CTA per token; each thread owns VPT 16-byte vectors of the row and
 // reads its k expert rows eight at a time, so that many loads are in flight
@@ -187,6 +204,18 @@ int launch_scatter(int T, int n, int k, int tpw, const int32_t* idx, const int* 
     const int nblk = (T + bt - 1) / bt;
     k_scatter<<<nblk, bt, (size_t)n * sizeof(unsigned long long), s>>>(T, n, k, tpw, idx, blk_base, offsets,
                                                                         perm, route_pos);
+    if (nl) ++*nl;
+    return cuda_err(cudaGetLastError());
+}
+
+int launch_scatter_rows(const void* src, int row_bytes, const int* route_pos, int T, int k, void* dst,
+                        cudaStream_t s, int* nl) {
+    if (row_bytes % 16 || !aligned16(src) || !aligned16(dst)) return QBMOE_EINVAL;
+    const int vpr = row_bytes / 16;
+    const long long total = (long long)T * vpr;
+    const int grid = (int)std::min<long long>((total + 255) / 256, 152LL * 8);
+    k_scatter_rows<<<std::max(grid, 1), 256, 0, s>>>(static_cast<const uint4*>(src), vpr, route_pos, T, k,
+                                                     static_cast<uint4*>(dst));
     if (nl) ++*nl;
     return cuda_err(cudaGetLastError());
 }

@@ -9,6 +9,10 @@ int launch_expert_offsets(int n, const int32_t* loads, int* offsets, int tile_ro
                           cudaStream_t s, int* nl);
 int launch_scatter(int T, int n, int k, int tpw, const int32_t* idx, const int* blk_base, const int* offsets,
                    int* perm, int* route_pos, cudaStream_t s, int* nl);
+// Token rows into expert order: dst[route_pos[t * k + i]] = src[t] for
+// t < T, i < k (rows of row_bytes, a multiple of 16; 16-byte aligned bases).
+int launch_scatter_rows(const void* src, int row_bytes, const int* route_pos, int T, int k, void* dst,
+                        cudaStream_t s, int* nl);
 int launch_combine_rmsnorm(int act_dtype, int T, int k, int latent, const void* e, const float* w,
                            const int* route_pos, const float* gamma, float eps, void* z, long long ldz,
                            cudaStream_t s, int* nl);

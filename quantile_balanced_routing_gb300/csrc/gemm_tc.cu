@@ -1076,24 +1076,6 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
     }
 }
 
-// ---------------------------------------------------------------------------
-// Row copy in token order: dst[route_pos[t * k + i]] = src[t] for each of
-// token t's k routes (16-byte vectors).  Each source row is read once and
-// written k times; walking the destination rows instead re-reads every source
-// row k times, from DRAM once the rows have left L2.
-__global__ void k_scatter_rows(const uint4* __restrict__ src, int vec_per_row, const int* __restrict__ route_pos,
-                               int T, int k, uint4* __restrict__ dst) {
-    const long long total = (long long)T * vec_per_row;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long t = i / vec_per_row;
-        const int c = (int)(i - t * vec_per_row);
-        const uint4 v = src[i];
-        const int* rp = route_pos + t * k;
-        for (int r = 0; r < k; ++r) dst[(long long)__ldg(rp + r) * vec_per_row + c] = v;
-    }
-}
-
 // Pipeline depths (stages of one weight tile + one token tile), chosen by
 // measurement on GB300 within the 227 KB of shared memory per CTA.
 template <int BN> struct Stages;
@@ -1498,17 +1480,6 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, v
     prm.n_sub = ns;
     prm.m_total = m;
     return launch_dense(P, prm, BN, pair, T, x, c.d, c.d, s, nl);
-}
-
-int tc_scatter_rows(const void* src, int cols, const int* route_pos, int T, int k, void* dst, cudaStream_t s,
-                    int* nl) {
-    const int vpr = cols * 2 / 16;
-    const long long total = (long long)T * vpr;
-    const int grid = (int)std::min<long long>((total + 255) / 256, 152LL * 8);
-    k_scatter_rows<<<std::max(grid, 1), 256, 0, s>>>(static_cast<const uint4*>(src), vpr, route_pos, T, k,
-                                                     static_cast<uint4*>(dst));
-    if (nl) ++*nl;
-    return cuda_err(cudaGetLastError());
 }
 
 static int launch_grouped(TcPlan* P, TcParams& prm, bool pair, const void* act, long long routes, long long K,

@@ -23,10 +23,6 @@ void tc_set_stall(TcPlan* p, int on);
 // the block-scaled MMA.
 int tc_xside(TcPlan* p, int T, const void* x, bool with_router, float* logits, void* h, void* zcat, long long ldz,
              int* status, cudaStream_t s, int* nl);
-// dst[route_pos[t * k + i]] = src[t] for t < T, i < k (rows of 2 x `cols`
-// bytes): token rows into expert order.
-int tc_scatter_rows(const void* src, int cols, const int* route_pos, int T, int k, void* dst, cudaStream_t s,
-                    int* nl);
 // Whether the MXFP4 expert GEMMs run on the block-scaled MMA: their token
 // inputs (h_perm, act) are then E4M3 bytes.
 bool tc_mx_scaled(const TcPlan* p);
