@@ -1456,8 +1456,8 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, v
         g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = m_tiles_of(c.latent, false, pair); g.m_begin = m;
         g.k_split = 1 << 30; g.out = h; g.ldo = c.latent;
         if (tc_mx_scaled(P)) {
-            // block-scaled experts read h as E4M3 pairs, converted once here
-            // rather than once per route in the dispatch gather
+            // block-scaled experts read h as E4M3 pairs: converted here once
+            // per token, then copied into expert order as plain bytes
             g.out_e4m3 = 1;
             g.ldo = 2LL * c.latent;
         }
