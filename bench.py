@@ -35,6 +35,7 @@ WORKLOADS = {"decode": QI.DECODE, "prefill": QI.PREFILL, "prefill_mxfp4": QI.PRE
              "decode_mxfp4": QI.DECODE_MXFP4, "route_qb": QI.ROUTE_QB, "route_qb_gs": QI.ROUTE_QB}
 ROUTE_WORKLOADS = ("route_qb", "route_qb_gs")
 METRIC = "MoE-layer fwd routed tokens/s on 1 GB300; % of HBM / tensor-core roofline"
+ROUTE_METRIC = "QB routing tokens/s on 1 GB300; % of HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -301,16 +302,47 @@ def run_reference(args, shape, world, rank):
                 times.append(t_route + t_dense * shape.T / n_tok)
     sec = statistics.mean(times)
     val = shape.T / sec
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "routed tokens/s", "n_gpus": 1,
+    route = args.workload in ROUTE_WORKLOADS
+    line = {"impl": "reference", "metric": ROUTE_METRIC if route else METRIC, "value": val,
+            "unit": "routed tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": config_of(shape, args),
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if route else "f64",
+            "data": "synthetic (seeded)",
+            "config": route_config(shape, args) if route else config_of(shape, args),
             "cpu_baseline": {"value": val, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": (f"each step: full routing of {shape.T} tokens" +
                                         ("" if args.workload in ROUTE_WORKLOADS else
                                          f" + dense layer of {n_tok} sampled tokens, scaled to {shape.T} tokens"))},
             "e2e": {"value": val, "unit": "routed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def route_config(shape, args):
+    gs = args.workload == "route_qb_gs"
+    return {"workload": shape.name + ("_gauss_seidel" if gs else "_jacobi"), "T": shape.T, "n_experts": shape.n,
+            "top_k": shape.k, "qb_sweeps": 1, "l2": "flushed between steps (512 MB write)",
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+def cpu_route_baseline(logits, k, gs):
+    """The oracle's routing of the same fp32 logits on the host cores: one
+    cyclic sweep (about 20 s at 4096 x 896), or Jacobi sweeps repeated for at
+    least 3 s."""
+    from oracle import qb_oracle as O
+    mode = "gauss_seidel" if gs else "jacobi"
+    times = []
+    t_end = time.perf_counter() + 3.0
+    while True:
+        t0 = time.perf_counter()
+        O.moe_route_qb(logits, None, k, 1, mode)
+        times.append(time.perf_counter() - t0)
+        if gs or time.perf_counter() >= t_end:
+            break
+    sec = statistics.mean(times)
+    T, n = logits.shape
+    return {"value": T / sec, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": (f"numpy oracle: {mode} routing of the same {T} x {n} fp32 logits, "
+                       f"{len(times)} run(s), mean {sec:.3f} s")}
 
 
 def config_of(shape, args):
@@ -485,21 +517,48 @@ def run_route(args, shape, world, rank, local):
     barrier(world)
     ms = sum(a.elapsed_time(b) for a, b in ev) / max(args.steps, 1)
     value_job, ms_max = replica_throughput(T, ms, world)
+
+    # end to end: pinned host logits -> device, routing, device -> host indices and weights
+    lg_host = logits.cpu().pin_memory()
+    idx_host = torch.empty((T, k), dtype=torch.int32).pin_memory()
+    w_host = torch.empty((T, k), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        logits.copy_(lg_host, non_blocking=True)
+        step()
+        idx_host.copy_(idx, non_blocking=True)
+        w_host.copy_(w, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev_e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev_e:
+        flush.fill_(1)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_e) / max(args.steps, 1), world)
     if rank != 0:
         return
+    cpu = cpu_route_baseline(lg_host.numpy(), k, gs) if world == 1 and not args.no_cpu else None
     pk, src = peaks()
     b_alg = T * n * 4 * 2 + T * k * 8 + n * 8       # logits in, scores out, idx/w out, bias/loads
     achieved = b_alg / (ms_max * 1e-3) / 1e9
-    line = {"metric": "QB routing tokens/s on 1 GB300; % of HBM roofline", "value": value_job,
+    line = {"metric": ROUTE_METRIC, "value": value_job,
             "unit": "routed tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded)",
-            "config": {"workload": shape.name + ("_gauss_seidel" if gs else "_jacobi"), "T": T, "n_experts": n,
-                       "top_k": k, "qb_sweeps": 1, "l2": "flushed between steps (512 MB write)",
-                       "parallelism": f"replicas x{args.gpus}"},
+            "config": route_config(shape, args),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / pk["hbm_gbs"], "traffic": None, "kernel": "routing (all kernels)",
                          "algorithmic_bytes": b_alg, "peak_source": src},
+            "cpu_baseline": cpu,
+            "e2e": {"value": T * world / (ms_e2e * 1e-3), "unit": "routed tokens/s",
+                    "h2d_bytes_per_step": logits.numel() * logits.element_size(),
+                    "d2h_bytes_per_step": idx.numel() * idx.element_size() + w.numel() * w.element_size()},
             "gpu_launches": launches, "clocks": clocks.summary()}
     print(json.dumps(line), flush=True)
 
