@@ -268,6 +268,146 @@ def route_topk(s: np.ndarray, b: np.ndarray, k: int):
     return idx, w, loads
 
 
+def signsgd_bias_step(s: np.ndarray, b: np.ndarray, k: int, gamma: float) -> np.ndarray:
+    """One step of DeepSeek-V3's fixed-step sign rule on the bias.
+
+    [K3-width] 延伸解读 "QB vs DeepSeek-V3": DeepSeek-V3 moves each bias by a
+    fixed, hand-tuned step in the direction of a sign; that rule is SignSGD
+    on the same dual objective QB minimises exactly.  The dual's partial
+    derivative in b_j is load_j(b) - r_j (routes j receives under the biased
+    top-k, minus its target), so the step is
+        b_j <- fl(b_j - gamma)  if load_j > r_j   (overloaded: lower the bias)
+        b_j <- fl(b_j + gamma)  if load_j < r_j   (underloaded: raise it)
+        b_j unchanged           if load_j = r_j.
+    No common offset is subtracted (the rule as the pages describe it has
+    none; a common shift changes no selection)."""
+    s = np.asarray(s, F32)
+    T, n = s.shape
+    r = qb_targets(T, n, k)
+    _, _, loads = route_topk(s, b, k)
+    g = np.sign(loads.astype(np.int64) - r)
+    b = np.asarray(b, F32)
+    step = F32(gamma)
+    return np.where(g > 0, b - step, np.where(g < 0, b + step, b)).astype(F32)
+
+
+def route_signsgd(logits: np.ndarray, bias_in: Optional[np.ndarray], k: int, steps: int, gamma: float):
+    """The sign-rule router: scores, `steps` sign steps from bias_in (each on
+    the loads of the previous bias), then the biased top-k of the final bias
+    with raw-score weights, as route_topk."""
+    s = sigmoid_score(logits)
+    T, n = s.shape
+    b = np.zeros(n, F32) if bias_in is None else np.array(bias_in, dtype=F32, copy=True)
+    for _ in range(steps):
+        b = signsgd_bias_step(s, b, k, gamma)
+    idx, w, loads = route_topk(s, b, k)
+    return s, b, idx, w, loads
+
+
+# ---------------------------------------------------------------------------
+# Token-sharded QB: exact quantiles from exchanged digit histograms
+# ---------------------------------------------------------------------------
+
+def descending_keys(m: np.ndarray) -> np.ndarray:
+    """uint32 keys whose ascending order is the descending order of the fp32
+    margins m (-0 already canonical): the IEEE bits made order-preserving
+    (sign bit flipped for non-negatives, all bits flipped for negatives),
+    then complemented."""
+    u = np.asarray(m, F32).view(np.uint32)
+    asc = np.where(u & np.uint32(0x80000000), ~u, u | np.uint32(0x80000000)).astype(np.uint32)
+    return (~asc).astype(np.uint32)
+
+
+def margin_of_key(key: np.ndarray) -> np.ndarray:
+    """Inverse of descending_keys."""
+    asc = (~np.asarray(key, np.uint32)).astype(np.uint32)
+    u = np.where(asc & np.uint32(0x80000000), asc & np.uint32(0x7FFFFFFF), ~asc).astype(np.uint32)
+    return u.view(F32)
+
+
+HIST_DIGIT_BITS = 8
+HIST_PASSES = 32 // HIST_DIGIT_BITS
+
+
+def shard_digit_histogram(keys_shard: np.ndarray, prefix: np.ndarray, n_pass: int) -> np.ndarray:
+    """One shard's histogram for one refinement pass: for every expert j
+    (rows of keys_shard [n, T_s]) and each of the two tracked ranks, the
+    count of the shard's keys that match that rank's prefix (the digits
+    fixed by earlier passes) per value of the pass's 8-bit digit.
+    prefix [n, 2] uint32.  Returns [n, 2, 256] int64."""
+    keys_shard = np.asarray(keys_shard, np.uint32)
+    n = keys_shard.shape[0]
+    shift = 32 - HIST_DIGIT_BITS * (n_pass + 1)
+    hi_mask = np.uint32(0) if n_pass == 0 else np.uint32((0xFFFFFFFF << (shift + HIST_DIGIT_BITS)) & 0xFFFFFFFF)
+    out = np.zeros((n, 2, 1 << HIST_DIGIT_BITS), dtype=np.int64)
+    for j in range(n):
+        for a in range(2):
+            sel = keys_shard[j][(keys_shard[j] & hi_mask) == (np.uint32(prefix[j, a]) & hi_mask)]
+            digits = (sel >> np.uint32(shift)) & np.uint32((1 << HIST_DIGIT_BITS) - 1)
+            out[j, a] = np.bincount(digits.astype(np.int64), minlength=1 << HIST_DIGIT_BITS)
+    return out
+
+
+def advance_selection(hist: np.ndarray, prefix: np.ndarray, rank: np.ndarray, n_pass: int):
+    """After the exchange (hist = sum of every shard's histogram), fix this
+    pass's digit of each tracked rank: the digit whose cumulative count
+    first reaches the rank; the rank becomes the rank within that digit's
+    bucket.  Returns the new (prefix, rank)."""
+    shift = 32 - HIST_DIGIT_BITS * (n_pass + 1)
+    prefix = np.array(prefix, dtype=np.uint32, copy=True)
+    rank = np.array(rank, dtype=np.int64, copy=True)
+    n = hist.shape[0]
+    for j in range(n):
+        for a in range(2):
+            c = np.cumsum(hist[j, a])
+            d = int(np.searchsorted(c, rank[j, a], side="left"))
+            before = int(c[d - 1]) if d > 0 else 0
+            rank[j, a] -= before
+            prefix[j, a] = np.uint32(prefix[j, a] | np.uint32(d << shift))
+    return prefix, rank
+
+
+def selection_ranks(T: int, r: np.ndarray) -> np.ndarray:
+    """The two ranks (1-based, descending margin) the coordinate step needs:
+    r_j and r_j + 1, or the largest margin twice for r_j = 0 and the
+    smallest twice for r_j >= T (qb_coordinate_bias's end cases)."""
+    r = np.asarray(r, np.int64)
+    a = np.clip(r, 1, T)
+    b = np.where((r >= 1) & (r <= T - 1), r + 1, a)
+    return np.stack([a, b], axis=1)
+
+
+def qb_sweep_jacobi_sharded(s_shards, b: np.ndarray, k: int, exchange=None) -> np.ndarray:
+    """One Jacobi QB sweep over a batch split into token shards, where no
+    shard sees another's margins: only per-expert digit histograms are
+    exchanged.
+
+    [K3-width] Q&A on Quantile Balancing: the quantiles are formed from
+    histogram estimates so that the communication stays cheap.  Here the
+    estimate is refined until it is exact: each of four passes exchanges,
+    per expert, the 256-bin histogram of one 8-bit digit of the margins'
+    order keys among the keys that match the digits already fixed, for the
+    two ranks the coordinate step needs (r_j-th and (r_j+1)-th largest
+    margin).  After the last pass both order statistics are known exactly,
+    so the bias is that of qb_sweep_jacobi on the whole batch.  `exchange`
+    sums a per-shard histogram list (default: plain sum; a distributed
+    caller all-reduces across ranks)."""
+    shards = [np.asarray(x, F32) for x in s_shards]
+    n = shards[0].shape[1]
+    T = sum(x.shape[0] for x in shards)
+    r = qb_targets(T, n, k)
+    keys = [descending_keys(qb_margins(x, b, k)).T.copy() for x in shards]   # [n, T_s] each
+    rank = selection_ranks(T, r)
+    prefix = np.zeros((n, 2), dtype=np.uint32)
+    for p in range(HIST_PASSES):
+        parts = [shard_digit_histogram(kx, prefix, p) for kx in keys]
+        hist = exchange(parts) if exchange else np.sum(parts, axis=0)
+        prefix, rank = advance_selection(hist, prefix, rank, p)
+    Ma, Mb = margin_of_key(prefix[:, 0]), margin_of_key(prefix[:, 1])
+    q = np.where(r <= 0, Ma + F32(1.0), np.where(r >= T, Ma - F32(1.0), (Ma + Mb) * F32(0.5))).astype(F32)
+    return common_offset((-q).astype(F32))
+
+
 def moe_route_qb(logits: np.ndarray, bias_in: Optional[np.ndarray], k: int,
                  qb_sweeps: int = 1, mode: str = "jacobi"):
     """The router: scores, QB biases, biased top-k, weights and loads.

@@ -59,6 +59,32 @@ def test_sigmoid_monotone_on_dense_grid():
     assert np.all(np.diff(O.sigmoid_score(x)) >= 0)
 
 
+def test_router_logits_hand_worked():
+    """x . W_r^T + o on a hand-worked dyadic example (tests/golden): the
+    offset belongs to the expert (a column), the weights are [experts, width]."""
+    g = load("router_logits_hand.json")
+    x, w, o = (np.array(g[k], np.float64) for k in ("x", "w_router", "offset"))
+    got = O.router_logits(x, w, o)
+    assert got.shape == (x.shape[0], w.shape[0])
+    assert got.dtype == F32
+    assert np.array_equal(got, np.array(g["logits"], F32))
+    assert np.array_equal(O.router_logits(x, w, None), np.array(g["dots"], F32))
+
+
+def test_router_logits_equal_a_loop_dot_product_with_the_offset():
+    """Per token and expert, a plain Python sum over the width plus the
+    expert's offset (one fp32 rounding of the fp64 value)."""
+    rng = np.random.default_rng(15)
+    T, d, n = 5, 19, 7
+    x, w, o = rng.normal(0, 1, (T, d)), rng.normal(0, 0.3, (n, d)), rng.normal(0, 1, n)
+    got = O.router_logits(x, w, o)
+    assert got.shape == (T, n)
+    for t in range(T):
+        for j in range(n):
+            want = math.fsum(float(x[t, c]) * float(w[j, c]) for c in range(d)) + float(o[j])
+            assert abs(float(got[t, j]) - want) <= 6e-8 * max(1.0, abs(want))
+
+
 # --------------------------------------------------------------------------
 # QB on hand-worked examples
 # --------------------------------------------------------------------------
@@ -287,6 +313,114 @@ def test_degenerate_targets():
 
 
 # --------------------------------------------------------------------------
+# DeepSeek-V3's sign rule (the comparator) and token-sharded QB
+# --------------------------------------------------------------------------
+
+def test_signsgd_hand_worked():
+    g = load("signsgd_hand_k1.json")
+    s = np.array(g["scores"], F32)
+    k = g["k"]
+    assert list(O.route_topk(s, np.zeros(3, F32), k)[2]) == g["loads_at_zero_bias"]
+    assert list(O.qb_targets(*s.shape, k)) == g["targets"]
+    for run in g["runs"]:
+        b = np.zeros(3, F32)
+        for st in run["steps"]:
+            b = O.signsgd_bias_step(s, b, k, run["gamma"])
+            assert np.array_equal(b, np.array(st["bias"], F32)), run["gamma"]
+            idx, _, loads = O.route_topk(s, b, k)
+            assert idx.tolist() == st["idx"] and list(loads) == st["loads"]
+
+
+def test_signsgd_moves_like_the_exact_coordinate_step():
+    """SignSGD on the dual and QB's exact coordinate minimiser move every
+    unbalanced expert's bias the same way (the page: both work on one dual;
+    QB jumps to the minimiser, the sign rule takes a fixed step)."""
+    rng = np.random.default_rng(17)
+    T, n, k = 400, 32, 4
+    s = _scores(rng, T, n, 1.0)
+    b_old = rng.normal(0, 0.05, n).astype(F32)
+    _, _, loads = O.route_topk(s, b_old, k)
+    r = O.qb_targets(T, n, k)
+    m = O.qb_margins(s, b_old, k)
+    braw = np.array([O.qb_coordinate_bias(m[:, j], int(r[j])) for j in range(n)], F32)
+    b_sign = O.signsgd_bias_step(s, b_old, k, 1.0 / 64)
+    unbalanced = loads != r
+    assert unbalanced.sum() > 10
+    assert np.array_equal(np.sign(b_sign - b_old)[unbalanced], np.sign(braw - b_old)[unbalanced])
+    assert np.array_equal(b_sign[~unbalanced], b_old[~unbalanced])
+
+
+def test_one_qb_sweep_balances_better_than_sign_steps():
+    """On skewed scores one QB sweep leaves a lower max/mean load than the
+    same number of sign steps of any of a range of step sizes."""
+    rng = np.random.default_rng(18)
+    T, n, k = 2048, 64, 4
+    s = _scores(rng, T, n, 2.0 ** 0.5)
+    mean = T * k / n
+    b = O.qb_sweep_jacobi(s, np.zeros(n, F32), k)
+    qb = O.route_topk(s, b, k)[2].max() / mean
+    for gamma in (1e-3, 1e-2, 1e-1):
+        bs = O.signsgd_bias_step(s, np.zeros(n, F32), k, gamma)
+        assert O.route_topk(s, bs, k)[2].max() / mean > qb
+
+
+def test_descending_keys_order_and_round_trip():
+    m = np.array([0.0, -0.0, 1.5, -1.5, 1e-40, -1e-40, 3.4e38, -3.4e38, 0.25, -0.25], F32)
+    m[m == 0] = F32(0.0)
+    key = O.descending_keys(m)
+    assert np.array_equal(O.margin_of_key(key).view(np.uint32), m.view(np.uint32))
+    order = np.argsort(key, kind="stable")
+    assert np.all(np.diff(m[order].astype(np.float64)) <= 0)     # ascending key = descending margin
+
+
+@pytest.mark.parametrize("split", [[300], [100, 200], [1, 150, 149], [37, 0, 263]])
+def test_histogram_selection_is_an_exact_order_statistic(split):
+    """Four exchanged 8-bit digit histograms pin down the exact r-th and
+    (r+1)-th largest margin of every expert, whatever the token split:
+    checked against a textbook sort of the whole column (ties included)."""
+    rng = np.random.default_rng(sum(split) + len(split))
+    n, T = 6, sum(split)
+    m = (rng.integers(-40, 40, (T, n)) / 64.0).astype(F32)   # many exact ties
+    m[m == 0] = F32(0.0)
+    keys = O.descending_keys(m).T.copy()
+    r = np.array([0, 1, 17, 150, T - 1, T])
+    ranks = O.selection_ranks(T, r)
+    prefix = np.zeros((n, 2), np.uint32)
+    bounds = np.cumsum([0] + split)
+    for p in range(O.HIST_PASSES):
+        parts = [O.shard_digit_histogram(keys[:, a:b], prefix, p) for a, b in zip(bounds[:-1], bounds[1:])]
+        prefix, ranks = O.advance_selection(np.sum(parts, axis=0), prefix, ranks, p)
+    for j in range(n):
+        desc = np.sort(m[:, j].astype(np.float64))[::-1]
+        want = O.selection_ranks(T, r)[j]
+        assert O.margin_of_key(prefix[j, 0]) == desc[want[0] - 1]
+        assert O.margin_of_key(prefix[j, 1]) == desc[want[1] - 1]
+
+
+@pytest.mark.parametrize("name,split", [("qb_hand_k1.json", [1, 3]), ("qb_hand_k2.json", [2, 2]),
+                                         ("qb_hand_k2.json", [3, 1])])
+def test_sharded_sweep_reproduces_the_hand_worked_biases(name, split):
+    g = load(name)
+    s = np.array(g["scores"], F32)
+    b0 = np.array(g["bias_in"], F32)
+    shards = np.split(s, np.cumsum(split)[:-1])
+    b = O.qb_sweep_jacobi_sharded(shards, b0, g["k"])
+    assert np.array_equal(b, np.array(g["bias_out"], F32))
+
+
+def test_sharded_sweep_equals_whole_batch_sweep():
+    rng = np.random.default_rng(19)
+    T, n, k = 500, 40, 5
+    s = _scores(rng, T, n, 1.5)
+    s[::7] = (np.round(s[::7] * 32) / 32).astype(F32)      # some tied scores
+    b0 = rng.normal(0, 0.02, n).astype(F32)
+    want = O.qb_sweep_jacobi(s, b0, k)
+    for split in ([250, 250], [1, 499], [123, 77, 300]):
+        shards = np.split(s, np.cumsum(split)[:-1])
+        assert np.array_equal(O.qb_sweep_jacobi_sharded(shards, b0, k), want)
+
+
+# --------------------------------------------------------------------------
 # SiTU-GLU, RMSNorm, shared expert, MXFP4
 # --------------------------------------------------------------------------
 
@@ -332,6 +466,28 @@ def test_merged_shared_expert_is_sum_of_two_halves():
     parts = (O.shared_mlp(x, wg[:half], wu[:half], wo[:, :half], "f32")
              + O.shared_mlp(x, wg[half:], wu[half:], wo[:, half:], "f32"))
     assert np.allclose(merged, parts, rtol=1e-12, atol=1e-12)
+
+
+def test_shared_expert_is_odd_in_its_up_branch_only():
+    """SiTU-GLU's up factor b = 25 tanh(u / 25) is odd and its gate factor
+    a sigma(a) is not, so negating the up weights negates the shared
+    expert's output exactly, while negating the gate weights does not (the
+    gate and up matrices are not interchangeable)."""
+    rng = np.random.default_rng(16)
+    d, m_s = 24, 16
+    x = rng.normal(0, 1, (6, d))
+    wg, wu, wo = rng.normal(0, 0.5, (m_s, d)), rng.normal(0, 0.5, (m_s, d)), rng.normal(0, 0.3, (d, m_s))
+    base = O.shared_mlp(x, wg, wu, wo, "f32")
+    assert np.array_equal(O.shared_mlp(x, wg, -wu, wo, "f32"), -base)
+    flipped_gate = O.shared_mlp(x, -wg, wu, wo, "f32")
+    assert np.max(np.abs(flipped_gate + base)) > 0.1 * np.max(np.abs(base))
+    # a saturated gate (a -> beta1 = 4) leaves 4 sigma(4) times the capped up branch
+    big = O.shared_mlp(x, wg * 1e6, wu, np.eye(m_s, m_s)[:, :m_s], "f32")
+    up = x @ wu.T
+    sgn = np.sign(x @ wg.T)
+    a = 4.0 * sgn
+    want = O.round_to(a / (1.0 + np.exp(-a)) * 25.0 * np.tanh(up / 25.0), "f32")
+    assert np.allclose(big, want, rtol=1e-6, atol=1e-6)
 
 
 def test_mxfp4_decode_against_ocp_table():
@@ -405,13 +561,26 @@ def test_routed_branch_is_insensitive_to_expert_output_scale():
     assert np.allclose(scaled, base, rtol=2e-5, atol=2e-6)
 
 
-def test_layer_matches_per_token_loop_on_tiny_case():
-    """Independent per-token, per-route restatement with python loops."""
-    inp = _tiny(T=6, n=8, k=2, d=32, latent=16, m=8, m_s=0)
+@pytest.mark.parametrize("m_s", [0, 8], ids=["routed_only", "with_shared_expert"])
+def test_layer_matches_per_token_loop_on_tiny_case(m_s):
+    """Independent per-token, per-route restatement with python loops; the
+    shared expert's gate (w_shared_gate, capped at 4, through the sigmoid)
+    and up (w_shared_up, capped at 25) branches are named explicitly."""
+    inp = _tiny(T=6, n=8, k=2, d=32, latent=16, m=8, m_s=m_s)
     W = O.LayerWeights(inp)
     res = O.layer_forward(inp, weights=W)
     X = W.dense("x")
     for t in range(6):
+        shared = [0.0] * 32
+        if m_s:
+            sg, su, so = W.dense("w_shared_gate"), W.dense("w_shared_up"), W.dense("w_shared_out")
+            act_s = []
+            for q in range(m_s):
+                gate = sum(X[t, c] * sg[q, c] for c in range(32))
+                up = sum(X[t, c] * su[q, c] for c in range(32))
+                a = 4 * math.tanh(gate / 4)
+                act_s.append(float(np.float32(a / (1 + math.exp(-a)) * 25 * math.tanh(up / 25))))
+            shared = [sum(act_s[q] * so[c, q] for q in range(m_s)) for c in range(32)]
         h = [float(np.float32(sum(X[t, c] * W.dense("w_down")[r, c] for c in range(32)))) for r in range(16)]
         y = [0.0] * 16
         for i in range(2):
@@ -428,7 +597,7 @@ def test_layer_matches_per_token_loop_on_tiny_case():
         rms = math.sqrt(sum(v * v for v in y) / 16 + 1e-6)
         z = [float(np.float32(y[r] / rms * W.dense("gamma")[r])) for r in range(16)]
         for c in range(32):
-            o = float(np.float32(sum(z[r] * W.dense("w_proj_up")[c, r] for r in range(16))))
+            o = float(np.float32(sum(z[r] * W.dense("w_proj_up")[c, r] for r in range(16)) + shared[c]))
             assert res["out"][t, c] == pytest.approx(o, rel=1e-5, abs=1e-6)
 
 
@@ -486,8 +655,43 @@ def _sigmoid_wrong_sign(x):
     return _ORIG["sigmoid_score"](-np.asarray(x, F32))
 
 
+def _logits_without_offset(x, w_router, offset):
+    return _ORIG["router_logits"](x, w_router, None)
+
+
+def _logits_offset_subtracted(x, w_router, offset):
+    return _ORIG["router_logits"](x, w_router, None if offset is None else -np.asarray(offset))
+
+
+def _shared_gate_up_swapped(x, w_gate, w_up, w_out, dtype):
+    return _ORIG["shared_mlp"](x, w_up, w_gate, w_out, dtype)
+
+
+def _sign_step_reversed(s, b, k, gamma):
+    return _ORIG["signsgd_bias_step"](s, b, k, -gamma)
+
+
+def _digit_off_by_one(hist, prefix, rank, n_pass):
+    shift = 32 - O.HIST_DIGIT_BITS * (n_pass + 1)
+    prefix = np.array(prefix, dtype=np.uint32, copy=True)
+    rank = np.array(rank, dtype=np.int64, copy=True)
+    for j in range(hist.shape[0]):
+        for a in range(2):
+            c = np.cumsum(hist[j, a])
+            d = min(int(np.searchsorted(c, rank[j, a], side="right")), 255)
+            rank[j, a] -= int(c[d - 1]) if d > 0 else 0
+            prefix[j, a] = np.uint32(prefix[j, a] | np.uint32(d << shift))
+    return prefix, rank
+
+
+def _histogram_ignores_prefix(keys_shard, prefix, n_pass):
+    return _ORIG["shard_digit_histogram"](keys_shard, np.zeros_like(prefix), n_pass)
+
+
 _ORIG = {nm: getattr(O, nm) for nm in ("qb_margins", "qb_coordinate_bias", "route_topk", "common_offset",
-                                       "situ_glu", "rank_experts", "rmsnorm", "sigmoid_score")}
+                                       "situ_glu", "rank_experts", "rmsnorm", "sigmoid_score", "router_logits",
+                                       "shared_mlp", "signsgd_bias_step", "advance_selection",
+                                       "shard_digit_histogram")}
 
 _PLANTS = [
     ("qb_margins", _margins_vs_biased_score, [test_margin_tau_equals_kth_best_among_other_experts]),
@@ -499,6 +703,19 @@ _PLANTS = [
     ("rank_experts", _rank_high_index_first, [test_rank_is_textbook_sort_with_index_ties]),
     ("rmsnorm", _rms_without_sqrt, [test_rmsnorm_scale_invariance_and_unit_rms]),
     ("sigmoid_score", _sigmoid_wrong_sign, [test_sigmoid_special_values_and_symmetry]),
+    ("router_logits", _logits_without_offset,
+     [test_router_logits_hand_worked, test_router_logits_equal_a_loop_dot_product_with_the_offset]),
+    ("router_logits", _logits_offset_subtracted, [test_router_logits_hand_worked]),
+    ("shared_mlp", _shared_gate_up_swapped,
+     [test_shared_expert_is_odd_in_its_up_branch_only,
+      lambda: test_layer_matches_per_token_loop_on_tiny_case(8)]),
+    ("signsgd_bias_step", _sign_step_reversed,
+     [test_signsgd_hand_worked, test_signsgd_moves_like_the_exact_coordinate_step]),
+    ("advance_selection", _digit_off_by_one, [lambda: test_histogram_selection_is_an_exact_order_statistic([300]),
+                                              lambda: test_sharded_sweep_reproduces_the_hand_worked_biases(
+                                                  "qb_hand_k1.json", [1, 3])]),
+    ("shard_digit_histogram", _histogram_ignores_prefix,
+     [lambda: test_histogram_selection_is_an_exact_order_statistic([100, 200])]),
 ]
 
 
