@@ -7,7 +7,10 @@ experts, combine + RMSNorm, up-projection + merged shared expert).  Prints one
 JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode|prefill|prefill_mxfp4]
+                  [--workload prefill|decode|prefill_mxfp4|decode_mxfp4|route_qb|route_qb_gs]
+
+The default workload is the largest single-GPU configuration: the K3-shape
+layer at prefill size (16384 tokens, bf16).
 
 Multi-GPU (torchrun): every rank runs an independent replica on its own batch
 (the path has no data exchange on one replica); value = all ranks' tokens /
@@ -210,10 +213,13 @@ def replica_throughput(tokens_per_rank, ms_local, world):
 # ---------------------------------------------------------------------------
 
 class OracleSample:
-    """The CPU oracle on a bounded sample of a workload: full routing of the
-    batch (QB quantiles are over all T tokens) plus the dense layer for n_tok
-    seeded sampled tokens.  Weight draws (and fp32 caches of the sampled
-    tokens' experts) are made once, before any clock starts."""
+    """The CPU oracle on a bounded sample of a workload: the routing of the
+    whole batch (router GEMM, QB sweep and biased top-k over all T tokens:
+    QB's quantiles are over the batch) and then the dense layer of n_tok
+    seeded sampled tokens.  The n_tok tokens are the units counted: each has
+    gone through the complete layer when the clock stops.  Weight draws (and
+    fp32 copies of the sampled tokens' experts) are made once, before any
+    clock starts, as the GPU's weights are resident before its clock."""
 
     def __init__(self, shape, n_tok, seed=0):
         from oracle import qb_oracle as O
@@ -244,17 +250,19 @@ class OracleSample:
         self.W = W
 
     def run(self):
-        """Seconds for (routing of all T tokens, dense layer of the sample)."""
-        O, W, shape = self.O, self.W, self.shape
+        """Seconds of one pass: the routing of all T tokens (inside
+        layer_forward, from the router GEMM on) and the dense layer of the
+        sampled tokens."""
+        O, W = self.O, self.W
         t0 = time.perf_counter()
-        logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
-        O.moe_route_qb(logits, None, shape.k, shape.qb_sweeps)
-        t_route = time.perf_counter() - t0
-        t1 = time.perf_counter()
-        O.layer_forward(self.inp, tokens=self.tokens, logits=logits, weights=W)
-        t_layer = time.perf_counter() - t1
-        # layer_forward re-runs the routing over all T tokens; count it once
-        return t_route, max(t_layer - t_route, 1e-9)
+        O.layer_forward(self.inp, tokens=self.tokens, weights=W)
+        return time.perf_counter() - t0
+
+    def describe(self, sec, runs):
+        s = self.shape
+        return (f"numpy oracle, {runs} pass(es), mean {sec:.2f} s: router GEMM (fp64), QB sweep and top-k of "
+                f"all {s.T} tokens, then the dense layer of {len(self.tokens)} seeded sampled tokens; "
+                f"value counts those {len(self.tokens)} tokens (no extrapolation); BLAS threads = cores")
 
 
 def cpu_cores():
@@ -264,14 +272,16 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(shape, n_tok):
-    t_route, t_dense = OracleSample(shape, n_tok).run()
-    S = n_tok
-    est = t_route + t_dense * shape.T / S
-    return {"value": shape.T / est, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": (f"numpy oracle: router GEMM (fp64) + QB routing of all {shape.T} tokens "
-                       f"({t_route:.2f} s) and the dense layer for {S} sampled tokens ({t_dense:.2f} s), "
-                       f"scaled to {shape.T} tokens; BLAS threads = cores, elementwise numpy single-threaded")}
+def cpu_baseline(shape, n_tok, min_seconds=10.0):
+    """The oracle as it stands on a bounded sample (about 10-30 s of work)."""
+    sample = OracleSample(shape, n_tok)
+    times = []
+    t_end = time.perf_counter() + min_seconds
+    while not times or time.perf_counter() < t_end:
+        times.append(sample.run())
+    sec = statistics.mean(times)
+    return {"value": n_tok / sec, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": sample.describe(sec, len(times))}
 
 
 # ---------------------------------------------------------------------------
@@ -279,7 +289,7 @@ def cpu_baseline(shape, n_tok):
 def run_reference(args, shape, world, rank):
     if rank != 0:
         return
-    n_tok = max(1, int(os.environ.get("QB_ORACLE_TOKENS", "2")))
+    n_tok = max(1, int(os.environ.get("QB_ORACLE_TOKENS", "4")))
     times = []
     if args.workload in ROUTE_WORKLOADS:
         # the oracle's routing of the whole batch from the same fp32 logits
@@ -297,11 +307,11 @@ def run_reference(args, shape, world, rank):
     else:
         sample = OracleSample(shape, n_tok)
         for i in range(args.warmup + args.steps):
-            t_route, t_dense = sample.run()
+            t = sample.run()
             if i >= args.warmup:
-                times.append(t_route + t_dense * shape.T / n_tok)
+                times.append(t)
     sec = statistics.mean(times)
-    val = shape.T / sec
+    val = n_tok / sec
     route = args.workload in ROUTE_WORKLOADS
     line = {"impl": "reference", "metric": ROUTE_METRIC if route else METRIC, "value": val,
             "unit": "routed tokens/s", "n_gpus": 1,
@@ -310,9 +320,10 @@ def run_reference(args, shape, world, rank):
             "data": "synthetic (seeded)",
             "config": route_config(shape, args) if route else config_of(shape, args),
             "cpu_baseline": {"value": val, "unit": "routed tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": (f"each step: full routing of {shape.T} tokens" +
+                             "sample": (f"each step: the oracle's routing of all {shape.T} tokens" +
                                         ("" if args.workload in ROUTE_WORKLOADS else
-                                         f" + dense layer of {n_tok} sampled tokens, scaled to {shape.T} tokens"))},
+                                         f" (router GEMM, QB sweep, top-k) and its dense layer of {n_tok} seeded "
+                                         f"sampled tokens; value = those {n_tok} tokens / step time"))},
             "e2e": {"value": val, "unit": "routed tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -353,6 +364,61 @@ def config_of(shape, args):
             "parallelism": f"replicas x{args.gpus}"}
 
 
+def expert_gemm_roofline(shape, stages, pk, src, mx_peak=None):
+    """Roofline of the dominant kernel: the grouped expert GEMM (the tcgen05
+    kernel in grouped mode), launched twice per step, for the expert gate/up
+    (with the SiTU-GLU epilogue) and the expert down-projection.  Achieved =
+    the two launches' algorithmic work / their summed CUDA-event durations
+    (the average launch's work over its average duration).  Tensor-bound
+    workloads (prefill) are taken against the burst bf16 peak (the kernel is
+    timed alone, between events), or the measured block-scaled peak for
+    MXFP4 experts; weight-streaming ones (decode) against the HBM copy."""
+    st = dict(stages)
+    work = stage_work(shape, shape.T)
+    names = ("expert_gate_up", "expert_down")
+    if not all(nm in st for nm in names):
+        return None
+    b = sum(work[nm][0] for nm in names)
+    f = sum(work[nm][1] for nm in names)
+    ms = sum(st[nm] for nm in names)
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if f / b >= ridge:
+        if shape.wfmt == "mxfp4":
+            # E2M1 weights x E4M3 token pairs on kind::mxf8f6f4: the MMA issues
+            # twice the layer's flops (hi and lo token planes).  Peak: the
+            # measured bf16 burst times the block-scaled : bf16 MMA rate ratio
+            # the library's probe measures on this GPU.
+            achieved = 2.0 * f / (ms * 1e-3) / 1e12
+            if mx_peak:
+                ratio, probe = mx_peak
+                peak = pk["bf16_tflops"] * ratio
+                note = (f"measured bf16 burst x measured mxf8f6f4:bf16 MMA rate ratio {ratio:.3f} (probe: "
+                        f"{probe['mxf8f6f4']:.0f} / {probe['bf16']:.0f} TFLOP/s raw back-to-back MMAs)")
+            else:
+                peak = 2.0 * pk["bf16_tflops"]
+                note = "2 x measured bf16 burst (nominal fp8:bf16 ratio; the probe was unavailable)"
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_note": note + "; issued MMA flops = 2 x layer flops (hi and lo token planes)"}
+        else:
+            achieved = f / (ms * 1e-3) / 1e12
+            peak = pk["bf16_tflops"]
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "peak_note": "measured cuBLAS bf16 burst"}
+    else:
+        achieved = b / (ms * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "peak_note": "measured copy bandwidth"}
+    roof["frac"] = achieved / peak
+    tr = [recorded_traffic(nm, shape.name) for nm in names]
+    roof.update({"traffic": sum(tr) / 2 if all(t is not None for t in tr) else None,
+                 "kernel": "k_tc_gemm grouped (expert gate/up + expert down launches)",
+                 "launches_per_step": 2, "ms_per_launch": ms / 2, "algorithmic_bytes_per_launch": b / 2,
+                 "algorithmic_flops_per_launch": f / 2, "peak_source": src,
+                 "per_launch_ms": {nm: round(st[nm], 4) for nm in names}})
+    return roof
+
+
 def run_ours(args, shape, world, rank, local):
     import torch
     from qb_inputs.device import layer_for, upload
@@ -365,14 +431,13 @@ def run_ours(args, shape, world, rank, local):
     x = d["x"]
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
-    lay.set_timing(max(args.steps, 1))
     for _ in range(args.warmup):
         lay.forward(x, out=out)
     rc = lay.status()
     if rc:
         raise RuntimeError(f"device status {rc} after warm-up")
-    lay.set_timing(max(args.steps, 1))
     launches_per_step = lay.last_launch_count()
+    # the headline loop: no per-stage events inside it
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -387,8 +452,14 @@ def run_ours(args, shape, world, rank, local):
     rc = lay.status()
     if rc:
         raise RuntimeError(f"device status {rc} in the timed region")
-    stages = lay.stage_times()
     value_job, ms_max = replica_throughput(shape.T, ms, world)
+
+    # per-stage times from a separate pass with CUDA events between the stages
+    lay.set_timing(max(args.steps, 1))
+    for _ in range(args.steps):
+        lay.forward(x, out=out)
+    stages = lay.stage_times()
+    lay.set_timing(0)
 
     # end to end: pinned host input -> device, forward, device -> host output
     x_host = x.cpu().pin_memory()
@@ -410,36 +481,15 @@ def run_ours(args, shape, world, rank, local):
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / max(args.steps, 1), world)
     lay.close()
+    mx_peak = None
+    if shape.wfmt == "mxfp4" and rank == 0:
+        mx_peak = mma_peak_ratio()
 
     if rank != 0:
         return
     pk, src = peaks()
-    work = stage_work(shape, shape.T)
-    dom_name, dom_ms = max(stages, key=lambda s: s[1]) if stages else ("expert_gate_up", float("nan"))
-    b, f = work.get(dom_name, (0, 0))
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if f / max(b, 1) >= ridge:
-        peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-        if shape.wfmt == "mxfp4" and dom_name.startswith("expert_"):
-            # block-scaled E2M1 x E4M3 MMA: it runs at the fp8 rate (the nominal
-            # fp8:bf16 ratio of 2 applied to the measured bf16 peak) and issues
-            # twice the layer's flops (hi and lo activation planes)
-            achieved = 2.0 * f / (dom_ms * 1e-3) / 1e12
-            peak = 2.0 * peak
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak,
-                    "peak_note": "fp8 rate = 2 x measured bf16 (nominal ratio); issued MMA flops = 2 x layer flops"}
-        else:
-            achieved = f / (dom_ms * 1e-3) / 1e12
-            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak}
-    else:
-        achieved = b / (dom_ms * 1e-3) / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak}
-    roof.update({"traffic": recorded_traffic(dom_name, shape.name), "kernel": dom_name, "ms_per_launch": dom_ms,
-                 "algorithmic_bytes": b, "algorithmic_flops": f, "peak_source": src})
-    n_cpu_tok = int(os.environ.get("QB_ORACLE_TOKENS", "4"))
+    roof = expert_gemm_roofline(shape, stages, pk, src, mx_peak)
+    n_cpu_tok = int(os.environ.get("QB_ORACLE_TOKENS", "8"))
     cpu = cpu_baseline(shape, n_cpu_tok) if world == 1 and not args.no_cpu else None
     tok = shape.T * world
     line = {
@@ -457,6 +507,18 @@ def run_ours(args, shape, world, rank, local):
         "stages_ms": {nm: round(t, 4) for nm, t in stages},
     }
     print(json.dumps(line), flush=True)
+
+
+def mma_peak_ratio():
+    """(block-scaled mxf8f6f4 : bf16 MMA rate ratio, the probe's raw rates in
+    TFLOP/s), measured by the library's own probe kernel on this GPU; None if
+    the probe is unavailable."""
+    try:
+        import quantile_balanced_routing_gb300 as Q
+        probe = {k: Q.mma_peak_tflops(k) for k in ("bf16", "mxf8f6f4")}
+        return probe["mxf8f6f4"] / probe["bf16"], probe
+    except Exception:
+        return None
 
 
 def run_route(args, shape, world, rank, local):
@@ -569,7 +631,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="prefill", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--experts", type=int, default=0,
                     help="profiling only: scale the workload down to this many experts, keeping tokens per expert")

@@ -6,8 +6,16 @@
  * host memory.  Every call that takes a stream is asynchronous and
  * stream-ordered on it (NULL = the legacy default stream); nothing here
  * synchronises the host except qbmoe_status and the functions documented as
- * synchronous.  A negative return value means nothing was launched and no
- * output was touched.
+ * synchronous.
+ *
+ * Errors.  Every call checks its arguments, encodes every tensor map and
+ * sets up the device (kernel attributes, once per device) before its first
+ * launch; a negative code from any of those steps means nothing was
+ * launched and no output was touched.  Only QBMOE_ECUDA can also come from a
+ * launch itself (the CUDA runtime refusing a launch or a copy); then the
+ * launches that preceded it in the same call stay enqueued and the call's
+ * outputs may be partly written.  Failures inside kernels are reported
+ * later, by qbmoe_status.
  *
  * Sources, by page title and section:
  *   [K3-width]  "Kimi K3 模型结构（5）：宽度维度，Stable LatentMoE" (xhh.club),
@@ -31,7 +39,7 @@ typedef struct CUstream_st* qbmoe_stream_t;
 typedef enum {
     QBMOE_OK = 0,
     QBMOE_EINVAL = -1,     /* bad size, null or misaligned pointer, unsupported option */
-    QBMOE_ENOMEM = -2,     /* device allocation failed (qbmoe_create only) */
+    QBMOE_ENOMEM = -2,     /* device allocation failed (qbmoe_create, qbmoe_pack_weights) */
     QBMOE_ECUDA = -3,      /* a CUDA runtime/driver call or a launch failed */
     QBMOE_EARCH = -4,      /* current device is not compute capability 10.3 */
     QBMOE_EWORKSPACE = -5, /* caller workspace too small / ctx built for fewer tokens */
@@ -43,6 +51,10 @@ typedef enum {
 enum { QBMOE_F32 = 0, QBMOE_BF16 = 1 };
 /* Routed-expert weight formats. */
 enum { QBMOE_W_F32 = 0, QBMOE_W_BF16 = 1, QBMOE_W_MXFP4 = 2 };
+/* QB sweep forms: every expert from the same biases (the default, one
+ * exchange of per-expert quantiles per sweep), or cyclic coordinate descent
+ * (each expert's step sees the latest biases; moe_route_qb_gs). */
+enum { QBMOE_QB_JACOBI = 0, QBMOE_QB_GAUSS_SEIDEL = 1 };
 
 /* Limits of this build. */
 #define QBMOE_MAX_EXPERTS 1024
@@ -91,7 +103,7 @@ enum { QBMOE_W_F32 = 0, QBMOE_W_BF16 = 1, QBMOE_W_MXFP4 = 2 };
  * workspace: device, >= qbmoe_route_workspace_bytes(T, n, k) bytes, 256-byte
  *          aligned; owned by the caller; contents are scratch.
  * All device pointers 16-byte aligned.  Results are bit-reproducible.
- * Returns QBMOE_OK after enqueueing, or a negative code (nothing launched).
+ * Returns QBMOE_OK after enqueueing, or a negative code (see Errors above).
  */
 size_t qbmoe_route_workspace_bytes(int T, int n, int k);
 int moe_route_qb(int T, int n, int k, int qb_sweeps,
@@ -127,13 +139,81 @@ int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_when_balanced,
                     qbmoe_stream_t stream);
 
 /*
+ * moe_route_signsgd — DeepSeek-V3's fixed-step sign rule, the comparator of
+ * Quantile Balancing.
+ *
+ * [K3-width] 延伸解读 "QB vs DeepSeek-V3": DeepSeek-V3 moves each expert's
+ * bias by a fixed, hand-tuned step along a sign; that rule is SignSGD on the
+ * same dual that QB minimises exactly.  From b = bias_in (NULL = zeros),
+ * `steps` times: loads under the biased top-k of b, then
+ *   b_j = fl(b_j - gamma) if load_j > r_j;  fl(b_j + gamma) if load_j < r_j;
+ *   unchanged if load_j = r_j  (r_j as in moe_route_qb, no common offset).
+ * Then the final routing on b as in moe_route_qb; bias_out = b.
+ * steps >= 0, 0 < gamma < inf; other arguments as moe_route_qb, workspace
+ * >= qbmoe_route_signsgd_workspace_bytes(T, n, k).  Bit-reproducible.
+ */
+size_t qbmoe_route_signsgd_workspace_bytes(int T, int n, int k);
+int moe_route_signsgd(int T, int n, int k, int steps, float gamma,
+                      const float* logits, const float* bias_in, float* bias_out,
+                      float* scores, int32_t* topk_idx, float* topk_w, int32_t* loads,
+                      void* workspace, size_t workspace_bytes, qbmoe_stream_t stream);
+
+/*
+ * Token-sharded Quantile Balancing with a histogram exchange.
+ *
+ * [K3-width] Q&A on Quantile Balancing: the quantiles are formed from
+ * histogram estimates so that the communication stays cheap.  A batch of
+ * T_total tokens is split into shards (on one or several devices); no shard
+ * sees another's margins.  Each expert's coordinate step needs the r_j-th
+ * and (r_j+1)-th largest margin over the whole batch (moe_route_qb).  Four
+ * passes each exchange, per expert and per tracked rank, the 256-bin
+ * histogram of one 8-bit digit of the margins' order keys among the keys
+ * that match the digits fixed so far (n * 2 * 256 int32 per pass, against
+ * T_total * n margins), and refine the estimate until both order
+ * statistics are exact.  The bias is then bit-identical to moe_route_qb's
+ * one-sweep bias of the whole batch, and each shard routes its tokens with
+ * moe_route_qb(qb_sweeps = 0, bias_in = that bias).
+ *
+ * Per sweep:
+ *   moe_qb_hist_init(T_total, n, k, state, hist)          targets, zeroed hist
+ *   moe_qb_shard_margins(shard)                          each local shard
+ *   for pass = 0..3:
+ *     moe_qb_shard_hist(shard, pass, state, ws, hist)    each local shard ADDS
+ *                                                        its counts into hist
+ *     (the caller sums hist over devices: an all-reduce)
+ *     moe_qb_hist_advance(n, pass, hist, state)          fixes the digit and
+ *                                                        zeroes hist
+ *   moe_qb_hist_bias(n, state, bias)                      b' and common offset
+ *
+ * state: device, qbmoe_qb_hist_state_bytes(n), caller-owned, one per device
+ * (every device holds the same state after each advance).  hist: device
+ * int32 [n][2][256] (qbmoe_qb_hist_bytes(n)).  Shard workspace: device,
+ * qbmoe_qb_shard_workspace_bytes(T_shard, n, k), 256-byte aligned; holds the
+ * shard's margins [n, T_shard] from moe_qb_shard_margins until its last
+ * moe_qb_shard_hist.  moe_qb_shard_margins: logits [T_shard, n] fp32 in,
+ * scores [T_shard, n] fp32 out, bias_in [n] or NULL (zeros) - the bias the
+ * sweep starts from, the same on every shard.  T_total * k < 2^31.
+ */
+size_t qbmoe_qb_hist_state_bytes(int n);
+size_t qbmoe_qb_hist_bytes(int n);
+size_t qbmoe_qb_shard_workspace_bytes(int T_shard, int n, int k);
+int moe_qb_hist_init(int T_total, int n, int k, void* state, int32_t* hist, qbmoe_stream_t stream);
+int moe_qb_shard_margins(int T_shard, int n, int k, const float* logits, const float* bias_in, float* scores,
+                         void* workspace, size_t workspace_bytes, qbmoe_stream_t stream);
+int moe_qb_shard_hist(int T_shard, int n, int pass, const void* state, const void* workspace, int32_t* hist,
+                      qbmoe_stream_t stream);
+int moe_qb_hist_advance(int n, int pass, int32_t* hist, void* state, qbmoe_stream_t stream);
+int moe_qb_hist_bias(int n, const void* state, float* bias_out, qbmoe_stream_t stream);
+
+/*
  * moe_route_qb_noalloc — moe_route_qb for callers that cannot allocate.
  *
  * The pages have no counterpart: this is a deployment variant of the router
  * above with identical results, for callers that cannot hand it a workspace
- * because they may not allocate device memory where they route (inside a
- * CUDA graph capture, on a serving path whose memory is planned up front, in
- * a plug-in that only receives its inputs and outputs).  Arguments are those
+ * because they may not allocate device memory where they route (a serving
+ * path whose device memory is planned up front and may not grow, or a
+ * plug-in that only receives its inputs and outputs from a host program
+ * that owns all memory).  Arguments are those
  * of moe_route_qb without the workspace.  The scratch lives in one fixed
  * device array of qbmoe_route_noalloc_max_bytes() bytes (32 MiB) that every
  * GPU which loads the library keeps until the process exits; sizes whose
@@ -142,8 +222,8 @@ int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_when_balanced,
  * or cudaFree and calls no allocating library routine.
  *
  * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress); make that first call before any stream
- * capture.  All calls share the one array, so calls that may overlap on the
+ * device (cudaGetSymbolAddress) and sets the library's kernel attributes
+ * there; make that first call before any stream capture.  All calls share the one array, so calls that may overlap on the
  * GPU (different streams, or different host threads on one device) race and
  * must be serialised by the caller.  Nothing needs to start at zero: every
  * scratch region is written before it is read.
@@ -171,6 +251,7 @@ typedef struct {
     int act_dtype;      /* QBMOE_F32 | QBMOE_BF16: activations and dense weights */
     int expert_wfmt;    /* QBMOE_W_F32 | QBMOE_W_BF16 | QBMOE_W_MXFP4 */
     int qb_sweeps;      /* 0 = frozen bias (inference); 1 = one QB step */
+    int qb_mode;        /* QBMOE_QB_JACOBI (default) | QBMOE_QB_GAUSS_SEIDEL */
 } qbmoe_config;
 
 /*
@@ -214,6 +295,16 @@ int qbmoe_create(qbmoe_ctx** out, const qbmoe_config* cfg, int max_tokens);
 size_t qbmoe_layer_workspace_bytes(const qbmoe_config* cfg, int max_tokens);
 /* Record the weight pointers (host call, no device work, no copies). */
 int qbmoe_set_weights(qbmoe_ctx* ctx, const qbmoe_weights* w);
+/* Copy the weights into device memory the context owns, then use the
+ * copies (as qbmoe_set_weights on them).  w holds device pointers in the
+ * layouts above; the caller may free or change its tensors once the call
+ * returns.  Synchronous: enqueues the copies and a check of every MXFP4
+ * scale byte on `stream`, then waits for them.  A scale byte of 0xFF (E8M0
+ * NaN, not a weight scale) gives QBMOE_EINVAL and leaves the context's
+ * weights as they were.  Allocates one buffer (cudaMalloc; QBMOE_ENOMEM on
+ * failure); a later call replaces it, qbmoe_destroy frees it.  Nothing else
+ * in the forward path allocates. */
+int qbmoe_pack_weights(qbmoe_ctx* ctx, const qbmoe_weights* w, qbmoe_stream_t stream);
 /* Free the context's workspace (synchronous). NULL is a no-op. */
 int qbmoe_destroy(qbmoe_ctx* ctx);
 
@@ -244,6 +335,8 @@ int qbmoe_destroy(qbmoe_ctx* ctx);
  * scores_opt [T, n] fp32, idx_opt [T, k] int32, w_opt [T, k] fp32,
  *   loads_opt [n] int32: device outputs, each NULL if not wanted.
  * 1 <= T <= max_tokens.  No allocation, no host synchronisation.
+ * With qb_mode = QBMOE_QB_GAUSS_SEIDEL the qb_sweeps sweeps are cyclic, as
+ * moe_route_qb_gs (about 2n launches per sweep).
  */
 int moe_latent_forward(qbmoe_ctx* ctx, int T, const void* x, const float* logits_in,
                        const float* bias_in, float* bias_out, void* out,
@@ -290,6 +383,20 @@ int qbmoe_debug_stall(qbmoe_ctx* ctx, int enable);
  * tiling does not cover, or QBMOE_DISABLE_TC=1 in the environment at
  * qbmoe_create). */
 int qbmoe_uses_tensor_cores(qbmoe_ctx* ctx);
+
+/*
+ * Tensor-core rate probe (synchronous; a measurement hook, not part of the
+ * layer).  Runs one CTA per SM that issues 4 * iters back-to-back MMAs of
+ * the given kind on fixed shared-memory tiles (M = 128, N = 256; no TMA, no
+ * epilogue) between two CUDA events on the legacy default stream.  Kinds:
+ * QBMOE_PROBE_BF16 (kind::f16, bf16 x bf16, K = 16 per MMA) and
+ * QBMOE_PROBE_MXF4F8 (kind::mxf8f6f4 block-scaled, E2M1 x E4M3 with E8M0
+ * scales, K = 32 per MMA: the MXFP4 expert GEMMs' instruction).  Writes the
+ * elapsed milliseconds and the flops issued (2 * M * N * K per MMA).
+ * Allocates a 4-byte status word (cudaMalloc) for its bounded wait.
+ */
+enum { QBMOE_PROBE_BF16 = 0, QBMOE_PROBE_MXF4F8 = 1 };
+int qbmoe_mma_probe(int kind, int iters, float* ms_out, double* flops_out);
 
 const char* qbmoe_strerror(int code);
 

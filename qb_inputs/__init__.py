@@ -12,8 +12,8 @@ Workload recipe (every weight is drawn with standard deviation 1/sqrt(fan_in);
   W_out [n, latent, m], W_proj_up [d, latent], W_shared_gate/up [m_s, d],
   W_shared_out [d, m_s] ~ N(0, 1/fan_in); router offsets o [n] ~ N(0, v_off);
   RMSNorm gain gamma = 1 + N(0, 0.01).
-* Draws are Irwin-Hall(4) with the stated mean and variance (tails at 3.46
-  sigma); weights are rounded to the workload's storage type.
+* Draws are Gaussian (Box-Muller from two SplitMix64 uniforms, untruncated
+  tails; see qbgen.c); weights are rounded to the workload's storage type.
 """
 from __future__ import annotations
 
@@ -137,6 +137,44 @@ def _sig(fan_in: int) -> float:
     return float(np.float32(1.0 / np.sqrt(fan_in)))
 
 
+# Whole tensors drawn once per process and shared by every workload that
+# draws the same stream with the same shape, spread and storage (decode and
+# prefill shapes share all their weights), least recently used first out
+# beyond QB_INPUTS_CACHE_GB (default 48).
+_shared = {}
+_shared_order = []
+_shared_lock = threading.Lock()
+
+
+def _shared_draw(key, make):
+    with _shared_lock:
+        if key in _shared:
+            _shared_order.remove(key)
+            _shared_order.append(key)
+            return _shared[key]
+    a = make()
+    cap = float(os.environ.get("QB_INPUTS_CACHE_GB", "48")) * 2 ** 30
+    with _shared_lock:
+        _shared[key] = a
+        _shared_order.append(key)
+        total = sum(v.nbytes for v in _shared.values())
+        while total > cap and len(_shared_order) > 1:
+            old = _shared_order.pop(0)
+            total -= _shared.pop(old).nbytes
+    return a
+
+
+def _shared_get(key):
+    with _shared_lock:
+        return _shared.get(key)
+
+
+def clear_shared_draws():
+    with _shared_lock:
+        _shared.clear()
+        _shared_order.clear()
+
+
 class LayerInputs:
     """Host-side inputs of one workload, drawn lazily per tensor.
 
@@ -178,11 +216,15 @@ class LayerInputs:
             a = (np.float32(1.0) + a).astype(np.float32)
         return a
 
+    def _key(self, name):
+        shape, sigma, fmt = self.specs[name]
+        return (self.shape.seed, name, tuple(shape), float(sigma), "f32" if fmt == "f32" else "bf16")
+
     def raw(self, name):
         """Whole tensor in its storage form (bf16 bits / fp32 / bf16 master of MXFP4)."""
         if name not in self._cache:
             shape, sigma, fmt = self.specs[name]
-            self._cache[name] = self._draw(name, shape, sigma, fmt)
+            self._cache[name] = _shared_draw(self._key(name), lambda: self._draw(name, shape, sigma, fmt))
         return self._cache[name]
 
     def drop(self, name):
@@ -194,8 +236,14 @@ class LayerInputs:
         return bf16_bits_to_f32(a) if a.dtype == np.uint16 else a
 
     def expert_raw(self, name, e: int):
-        """Storage form of expert e's slice of an expert tensor."""
+        """Storage form of expert e's slice of an expert tensor (a view of the
+        whole tensor when it has been drawn, else drawn alone)."""
         shape, sigma, fmt = self.specs[name]
+        whole = self._cache.get(name)
+        if whole is None:
+            whole = _shared_get(self._key(name))
+        if whole is not None:
+            return whole[int(e)]
         per = int(shape[1]) * int(shape[2])
         return self._draw(name, shape[1:], sigma, fmt, offset=int(e) * per)
 

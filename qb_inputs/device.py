@@ -45,9 +45,9 @@ def upload(inp: LayerInputs, device="cuda", drop_host=True):
     return out
 
 
-def layer_for(shape, max_tokens=None, qb_sweeps=None):
+def layer_for(shape, max_tokens=None, qb_sweeps=None, qb_mode="jacobi"):
     """A LatentMoE context configured for a workload shape."""
     from quantile_balanced_routing_gb300 import LatentMoE
     return LatentMoE(shape.d, shape.latent, shape.n, shape.k, shape.m, shape.m_s, act_dtype=shape.dtype,
                      expert_wfmt=shape.wfmt, qb_sweeps=shape.qb_sweeps if qb_sweeps is None else qb_sweeps,
-                     max_tokens=max_tokens or shape.T)
+                     max_tokens=max_tokens or shape.T, qb_mode=qb_mode)

@@ -6,21 +6,31 @@
  * method consumes (fp32, bf16, MXFP4).  Both sides of every parity test take
  * their inputs from here.
  *
- * Generator.  Element i of tensor (seed, id) is derived from one SplitMix64
- * output (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * Generator.  Element i of tensor (seed, id) is derived from two SplitMix64
+ * outputs (Steele, Lea and Flood, "Fast splittable pseudorandom number
  * generators", OOPSLA 2014: the increment 0x9E3779B97F4A7C15 and the
  * variant-13 finaliser of Stafford's Mix13), written here from that
  * published definition:
  *     key  = splitmix64(seed ^ splitmix64(id))
- *     h    = splitmix64(key + i)
- * The 64-bit word h is split into four 16-bit fields a0..a3; each field
- * maps to the odd integer 2a+1-65536 (uniform and symmetric on
- * [-65535, 65535]) and the four are summed, an Irwin-Hall(4) draw with
- * mean 0 and variance 4*65536^2/3 (to within 1e-9 relative).  The value is
- *     v = fp32( fp32(S) * c ),   c = fp32(sigma * sqrt(3) / 131072),
- * so v has mean 0 and standard deviation sigma, with tails cut at
- * +-2*sqrt(3)*sigma (= 3.46 sigma).  S is an integer below 2^19, so fp32(S)
- * is exact and v is one IEEE multiply: identical on every machine.
+ *     h1   = splitmix64(key + 2p),   h2 = splitmix64(key + 2p + 1),
+ * where p = floor(i / 2) is the element's pair.  Their top 53 bits give two
+ * uniforms, u1 = ((h1 >> 11) + 1) * 2^-53 in (0, 1] and u2 = (h2 >> 11) *
+ * 2^-53 in [0, 1), and the Box-Muller transform (Box and Muller, "A note on
+ * the generation of random normal deviates", Ann. Math. Stat. 1958) gives
+ * two independent standard normal draws
+ *     z = sqrt(-2 ln u1) * cos(2 pi u2)  (element 2p),
+ *     z = sqrt(-2 ln u1) * sin(2 pi u2)  (element 2p + 1),
+ * so v = fp32(z * sigma) is N(0, sigma^2) with untruncated tails (|z| <=
+ * 8.6 at u1 = 2^-53).  ln and cos are computed here in double precision with
+ * a fixed sequence of IEEE operations (no libm transcendental, built with
+ * -ffp-contract=off; sqrt is IEEE-exact), so every machine draws the same
+ * bits:
+ *   ln u = e ln2 + 2 atanh(f),  u = m 2^e with m in [sqrt(1/2), sqrt(2)),
+ *          f = (m - 1)/(m + 1), atanh by its odd series to f^25
+ *          (|f| <= 0.1716: remainder below 1e-21);
+ *   cos and sin of 2 pi t by the half-, quarter- and eighth-turn symmetries
+ *          down to an angle x in [0, pi/4], then the Taylor series of cos x
+ *          (to x^18) and sin x (to x^19), remainder below 1e-19.
  *
  * bf16 storage rounds v to nearest-even on its fp32 bits.
  *
@@ -35,6 +45,7 @@
 #include <stdint.h>
 #include <string.h>
 #include <math.h>
+#include <stdlib.h>
 
 static inline uint64_t splitmix64(uint64_t z) {
     z += 0x9E3779B97F4A7C15ull;
@@ -47,18 +58,118 @@ static inline uint64_t tensor_key(uint64_t seed, uint64_t id) {
     return splitmix64(seed ^ splitmix64(id));
 }
 
-static inline float draw(uint64_t key, uint64_t i, float c) {
-    uint64_t h = splitmix64(key + i);
-    int32_t s = 0;
-    for (int f = 0; f < 4; ++f) {
-        int32_t a = (int32_t)((h >> (16 * f)) & 0xFFFFu);
-        s += 2 * a + 1 - 65536;
+/* ln u for u in (0, 1] (see the header: fixed operation order).  u is a
+ * normal double (u >= 2^-53), so its exponent and mantissa come from its bits:
+ * u = m 2^e, m in [1, 2), then m is halved when above sqrt(2). */
+static inline double ln_fixed(double u) {
+    uint64_t b;
+    memcpy(&b, &u, 8);
+    int e = (int)((b >> 52) & 0x7FF) - 1023;
+    b = (b & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull;
+    double m;
+    memcpy(&m, &b, 8);                           /* [1, 2) */
+    if (m > 1.41421356237309504880) {
+        m *= 0.5;                                /* exact */
+        e += 1;
     }
-    return (float)s * c;   /* (float)s is exact: |s| < 2^19 */
+    const double f = (m - 1.0) / (m + 1.0);
+    const double f2 = f * f;
+    /* atanh(f) / f = sum f^(2q) / (2q + 1), q = 0..12, in Horner form */
+    double p = 1.0 / 25.0;
+    p = p * f2 + 1.0 / 23.0;
+    p = p * f2 + 1.0 / 21.0;
+    p = p * f2 + 1.0 / 19.0;
+    p = p * f2 + 1.0 / 17.0;
+    p = p * f2 + 1.0 / 15.0;
+    p = p * f2 + 1.0 / 13.0;
+    p = p * f2 + 1.0 / 11.0;
+    p = p * f2 + 1.0 / 9.0;
+    p = p * f2 + 1.0 / 7.0;
+    p = p * f2 + 1.0 / 5.0;
+    p = p * f2 + 1.0 / 3.0;
+    p = p * f2 + 1.0;
+    const double ln_m = 2.0 * f * p;
+    /* ln 2 split so that e * LN2_HI is exact for |e| < 2^11 */
+    const double LN2_HI = 6.93147180369123816490e-01, LN2_LO = 1.90821492927058770002e-10;
+    return ((double)e * LN2_HI + (double)e * LN2_LO) + ln_m;
 }
 
-static inline float scale_of(float sigma) {
-    return (float)((double)sigma * sqrt(3.0) / 131072.0);
+/* cos x and sin x for x in [0, pi/4]: Taylor series to x^18 and x^19 in
+ * Horner form (coefficients 1/((2q-1) 2q) and 1/(2q (2q+1)) folded at
+ * compile time). */
+static inline void cos_sin_series(double x, double* c, double* s) {
+    const double x2 = x * x;
+    double pc = 1.0 - x2 * (1.0 / (17.0 * 18.0));
+    pc = 1.0 - x2 * (1.0 / (15.0 * 16.0)) * pc;
+    pc = 1.0 - x2 * (1.0 / (13.0 * 14.0)) * pc;
+    pc = 1.0 - x2 * (1.0 / (11.0 * 12.0)) * pc;
+    pc = 1.0 - x2 * (1.0 / (9.0 * 10.0)) * pc;
+    pc = 1.0 - x2 * (1.0 / (7.0 * 8.0)) * pc;
+    pc = 1.0 - x2 * (1.0 / (5.0 * 6.0)) * pc;
+    pc = 1.0 - x2 * (1.0 / (3.0 * 4.0)) * pc;
+    pc = 1.0 - x2 * (1.0 / (1.0 * 2.0)) * pc;
+    double ps = 1.0 - x2 * (1.0 / (18.0 * 19.0));
+    ps = 1.0 - x2 * (1.0 / (16.0 * 17.0)) * ps;
+    ps = 1.0 - x2 * (1.0 / (14.0 * 15.0)) * ps;
+    ps = 1.0 - x2 * (1.0 / (12.0 * 13.0)) * ps;
+    ps = 1.0 - x2 * (1.0 / (10.0 * 11.0)) * ps;
+    ps = 1.0 - x2 * (1.0 / (8.0 * 9.0)) * ps;
+    ps = 1.0 - x2 * (1.0 / (6.0 * 7.0)) * ps;
+    ps = 1.0 - x2 * (1.0 / (4.0 * 5.0)) * ps;
+    ps = 1.0 - x2 * (1.0 / (2.0 * 3.0)) * ps;
+    *c = pc;
+    *s = x * ps;
+}
+
+/* (cos 2 pi t, sin 2 pi t) for t in [0, 1): the octant symmetries reduce the
+ * angle to [0, pi/4]; every reduction step is exact (t has 53 bits). */
+static inline void cos_sin_turns(double t, double* c, double* s) {
+    const double TWO_PI = 6.28318530717958647692;
+    double sgn_s = 1.0;
+    if (t >= 0.5) {                              /* angle - pi: both change sign... */
+        t = 1.0 - t;                             /* ...or mirror: cos even, sin odd */
+        sgn_s = -1.0;
+    }
+    double sgn_c = 1.0;
+    if (t > 0.25) {                              /* pi - angle */
+        t = 0.5 - t;
+        sgn_c = -1.0;
+    }
+    double cc, ss;
+    if (t > 0.125) {                             /* pi/2 - angle: cos <-> sin */
+        cos_sin_series(TWO_PI * (0.25 - t), &ss, &cc);
+    } else {
+        cos_sin_series(TWO_PI * t, &cc, &ss);
+    }
+    *c = sgn_c * cc;
+    *s = sgn_s * ss;
+}
+
+/* Box-Muller pair p of stream `key`: two independent standard normals. */
+static inline void normal_pair(uint64_t key, uint64_t p, double* z0, double* z1) {
+    const uint64_t h1 = splitmix64(key + 2u * p);
+    const uint64_t h2 = splitmix64(key + 2u * p + 1u);
+    const double u1 = (double)((h1 >> 11) + 1u) * 0x1.0p-53;
+    const double u2 = (double)(h2 >> 11) * 0x1.0p-53;
+    const double rad = sqrt(-2.0 * ln_fixed(u1));
+    double c, s;
+    cos_sin_turns(u2, &c, &s);
+    *z0 = rad * c;
+    *z1 = rad * s;
+}
+
+/* Elements [offset, offset + count) of stream `key` as fp32 values z * sigma:
+ * element i is the cosine (i even) or sine (i odd) member of pair i / 2. */
+static void draw_range(uint64_t key, int64_t offset, int64_t count, double sigma, float* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t q = (offset >> 1); q <= ((offset + count - 1) >> 1); ++q) {
+        double z[2];
+        normal_pair(key, (uint64_t)q, &z[0], &z[1]);
+        for (int h = 0; h < 2; ++h) {
+            const int64_t i = 2 * q + h;
+            if (i >= offset && i < offset + count) out[i - offset] = (float)(z[h] * sigma);
+        }
+    }
 }
 
 static inline uint16_t f32_to_bf16_rne(float v) {
@@ -71,19 +182,23 @@ static inline uint16_t f32_to_bf16_rne(float v) {
 /* out[j] = value of element (offset + j) of tensor (seed, id), j < count. */
 void qbgen_normal_f32(uint64_t seed, uint64_t id, int64_t offset, int64_t count,
                       float sigma, float* out) {
-    const uint64_t key = tensor_key(seed, id);
-    const float c = scale_of(sigma);
-#pragma omp parallel for schedule(static)
-    for (int64_t j = 0; j < count; ++j) out[j] = draw(key, (uint64_t)(offset + j), c);
+    if (count <= 0) return;
+    draw_range(tensor_key(seed, id), offset, count, (double)sigma, out);
 }
 
 void qbgen_normal_bf16(uint64_t seed, uint64_t id, int64_t offset, int64_t count,
                        float sigma, uint16_t* out) {
-    const uint64_t key = tensor_key(seed, id);
-    const float c = scale_of(sigma);
+    if (count <= 0) return;
+    /* fp32 values in chunks, then bf16 rounding of their bits */
+    const int64_t CH = 1 << 20;
+    float* buf = (float*)malloc((size_t)(count < CH ? count : CH) * sizeof(float));
+    for (int64_t a = 0; a < count; a += CH) {
+        const int64_t c = count - a < CH ? count - a : CH;
+        draw_range(tensor_key(seed, id), offset + a, c, (double)sigma, buf);
 #pragma omp parallel for schedule(static)
-    for (int64_t j = 0; j < count; ++j)
-        out[j] = f32_to_bf16_rne(draw(key, (uint64_t)(offset + j), c));
+        for (int64_t j = 0; j < c; ++j) out[a + j] = f32_to_bf16_rne(buf[j]);
+    }
+    free(buf);
 }
 
 /* E2M1 magnitudes by code 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6. */

@@ -24,6 +24,7 @@ QBMOE_OK, QBMOE_EINVAL, QBMOE_ENOMEM, QBMOE_ECUDA = 0, -1, -2, -3
 QBMOE_EARCH, QBMOE_EWORKSPACE, QBMOE_ETIMEOUT, QBMOE_EDEVICE = -4, -5, -6, -7
 QBMOE_F32, QBMOE_BF16 = 0, 1
 QBMOE_W_F32, QBMOE_W_BF16, QBMOE_W_MXFP4 = 0, 1, 2
+QBMOE_QB_JACOBI, QBMOE_QB_GAUSS_SEIDEL = 0, 1
 MAX_EXPERTS, MAX_TOPK = 1024, 32
 
 
@@ -31,7 +32,8 @@ class QbmoeConfig(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("latent", ctypes.c_int), ("n_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("expert_inter", ctypes.c_int), ("shared_inter", ctypes.c_int),
                 ("situ_beta1", ctypes.c_float), ("situ_beta2", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("act_dtype", ctypes.c_int), ("expert_wfmt", ctypes.c_int), ("qb_sweeps", ctypes.c_int)]
+                ("act_dtype", ctypes.c_int), ("expert_wfmt", ctypes.c_int), ("qb_sweeps", ctypes.c_int),
+                ("qb_mode", ctypes.c_int)]
 
 
 _WEIGHT_FIELDS = ["w_router", "router_offset", "w_down", "w_gate", "w_up", "w_out", "s_gate", "s_up",
@@ -73,12 +75,31 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_route_qb_noalloc.restype = i
     lib.qbmoe_route_noalloc_max_bytes.argtypes = []
     lib.qbmoe_route_noalloc_max_bytes.restype = sz
+    lib.qbmoe_route_signsgd_workspace_bytes.argtypes = [i, i, i]
+    lib.qbmoe_route_signsgd_workspace_bytes.restype = sz
+    lib.moe_route_signsgd.argtypes = [i, i, i, i, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_route_signsgd.restype = i
+    for nm in ("qbmoe_qb_hist_state_bytes", "qbmoe_qb_hist_bytes"):
+        getattr(lib, nm).argtypes = [i]
+        getattr(lib, nm).restype = sz
+    lib.qbmoe_qb_shard_workspace_bytes.argtypes = [i, i, i]
+    lib.qbmoe_qb_shard_workspace_bytes.restype = sz
+    lib.moe_qb_hist_init.argtypes = [i, i, i, vp, vp, vp]
+    lib.moe_qb_shard_margins.argtypes = [i, i, i, vp, vp, vp, vp, sz, vp]
+    lib.moe_qb_shard_hist.argtypes = [i, i, i, vp, vp, vp, vp]
+    lib.moe_qb_hist_advance.argtypes = [i, i, vp, vp, vp]
+    lib.moe_qb_hist_bias.argtypes = [i, vp, vp, vp]
+    for nm in ("moe_qb_hist_init", "moe_qb_shard_margins", "moe_qb_shard_hist", "moe_qb_hist_advance",
+               "moe_qb_hist_bias"):
+        getattr(lib, nm).restype = i
     lib.qbmoe_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(QbmoeConfig), i]
     lib.qbmoe_create.restype = i
     lib.qbmoe_layer_workspace_bytes.argtypes = [ctypes.POINTER(QbmoeConfig), i]
     lib.qbmoe_layer_workspace_bytes.restype = sz
     lib.qbmoe_set_weights.argtypes = [vp, ctypes.POINTER(QbmoeWeights)]
     lib.qbmoe_set_weights.restype = i
+    lib.qbmoe_pack_weights.argtypes = [vp, ctypes.POINTER(QbmoeWeights), vp]
+    lib.qbmoe_pack_weights.restype = i
     lib.qbmoe_destroy.argtypes = [vp]
     lib.qbmoe_destroy.restype = i
     lib.moe_latent_forward.argtypes = [vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -99,6 +120,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qbmoe_debug_stall.restype = i
     lib.qbmoe_uses_tensor_cores.argtypes = [vp]
     lib.qbmoe_uses_tensor_cores.restype = i
+    lib.qbmoe_mma_probe.argtypes = [i, i, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double)]
+    lib.qbmoe_mma_probe.restype = i
     lib.qbmoe_strerror.argtypes = [i]
     lib.qbmoe_strerror.restype = ctypes.c_char_p
     _lib = lib
@@ -207,17 +230,64 @@ def route_qb_gs(logits, k: int, max_sweeps: int = 1, stop_when_balanced: bool = 
     return scores, bias_out, idx, w, loads, done[:1]
 
 
+QBMOE_PROBE_BF16, QBMOE_PROBE_MXF4F8 = 0, 1
+
+
+def mma_probe(kind: str, iters: int = 20000):
+    """(milliseconds, flops) of one run of the library's tensor-core rate
+    probe for kind "bf16" (kind::f16) or "mxf8f6f4" (block-scaled E2M1 x
+    E4M3)."""
+    code = {"bf16": QBMOE_PROBE_BF16, "mxf8f6f4": QBMOE_PROBE_MXF4F8}[kind]
+    ms, fl = ctypes.c_float(), ctypes.c_double()
+    rc = load_library().qbmoe_mma_probe(code, iters, ctypes.byref(ms), ctypes.byref(fl))
+    if rc:
+        raise QbmoeError(rc, "qbmoe_mma_probe")
+    return ms.value, fl.value
+
+
+def mma_peak_tflops(kind: str, runs: int = 3, iters: int = 20000) -> float:
+    """Best TFLOP/s of `runs` probe runs of one MMA kind on the current GPU."""
+    best = 0.0
+    for _ in range(runs):
+        ms, fl = mma_probe(kind, iters)
+        best = max(best, fl / (ms * 1e-3) / 1e12)
+    return best
+
+
+def route_signsgd(logits, k: int, steps: int, gamma: float, bias_in=None, stream=None):
+    """DeepSeek-V3's sign rule on fp32 logits [T, n] (moe_route_signsgd).
+    Returns (scores, bias, idx, w, loads)."""
+    import torch
+    T, n = logits.shape
+    dev = logits.device
+    assert logits.dtype == torch.float32 and logits.is_contiguous() and dev.type == "cuda"
+    scores = torch.empty((T, n), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    loads = torch.empty((n,), dtype=torch.int32, device=dev)
+    bias_out = torch.empty((n,), dtype=torch.float32, device=dev)
+    lib = load_library()
+    need = lib.qbmoe_route_signsgd_workspace_bytes(T, n, k)
+    ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+    rc = lib.moe_route_signsgd(T, n, k, steps, gamma, _p(logits), _p(bias_in), _p(bias_out), _p(scores), _p(idx),
+                               _p(w), _p(loads), _p(ws), ws.numel(), _stream_ptr(stream))
+    if rc:
+        raise QbmoeError(rc, "moe_route_signsgd")
+    return scores, bias_out, idx, w, loads
+
+
 class LatentMoE:
     """One Stable LatentMoE layer bound to a libqbmoe context on the current device."""
 
     def __init__(self, d, latent, n_experts, top_k, expert_inter, shared_inter, act_dtype="bf16",
                  expert_wfmt="bf16", qb_sweeps=1, max_tokens=256, situ_beta1=4.0, situ_beta2=25.0,
-                 rms_eps=1e-6):
+                 rms_eps=1e-6, qb_mode="jacobi"):
         self.lib = load_library()
         self.cfg = QbmoeConfig(d, latent, n_experts, top_k, expert_inter, shared_inter, situ_beta1,
                                situ_beta2, rms_eps, QBMOE_BF16 if act_dtype == "bf16" else QBMOE_F32,
                                {"f32": QBMOE_W_F32, "bf16": QBMOE_W_BF16, "mxfp4": QBMOE_W_MXFP4}[expert_wfmt],
-                               qb_sweeps)
+                               qb_sweeps,
+                               {"jacobi": QBMOE_QB_JACOBI, "gauss_seidel": QBMOE_QB_GAUSS_SEIDEL}[qb_mode])
         self.ctx = ctypes.c_void_p()
         rc = self.lib.qbmoe_create(ctypes.byref(self.ctx), ctypes.byref(self.cfg), max_tokens)
         if rc:
@@ -243,6 +313,15 @@ class LatentMoE:
         rc = self.lib.qbmoe_set_weights(self.ctx, ctypes.byref(w))
         if rc:
             raise QbmoeError(rc, "qbmoe_set_weights")
+
+    def pack_weights(self, stream=None, **tensors):
+        """Copy the tensors (by qbmoe_weights field name) into memory the
+        context owns (qbmoe_pack_weights); the caller's tensors may then go."""
+        w = QbmoeWeights(*[_p(tensors.get(f)) for f in _WEIGHT_FIELDS])
+        rc = self.lib.qbmoe_pack_weights(self.ctx, ctypes.byref(w), _stream_ptr(stream))
+        if rc:
+            raise QbmoeError(rc, "qbmoe_pack_weights")
+        self._weights = {}
 
     def forward(self, x, logits_in=None, bias_in=None, bias_out=None, out=None, want_routing=False, stream=None):
         import torch

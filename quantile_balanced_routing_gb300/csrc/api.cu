@@ -13,16 +13,39 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
-int qbmoe_check_device_arch() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return QBMOE_ECUDA;
+namespace {
+
+int check_device_arch(int dev) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return QBMOE_ECUDA;
     if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return QBMOE_ECUDA;
     return (major == 10 && minor == 3) ? QBMOE_OK : QBMOE_EARCH;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_init_mu;
+bool g_init_done[kMaxDevices] = {};
+
+}  // namespace
+
+int qbh::device_init() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QBMOE_ECUDA;
+    std::lock_guard<std::mutex> lock(g_init_mu);
+    if (g_init_done[dev]) return QBMOE_OK;
+    int rc = check_device_arch(dev);
+    if (!rc) rc = qbh::route_init_attributes();
+    if (!rc) rc = qbh::tc_init_attributes();
+    if (rc) {
+        cudaGetLastError();
+        return rc;
+    }
+    g_init_done[dev] = true;
+    return QBMOE_OK;
 }
 
 namespace {
@@ -41,12 +64,14 @@ struct qbmoe_ctx {
     int device = 0;
     qbmoe_weights w{};
     bool have_weights = false;
+    void* packed = nullptr;    // weights copied by qbmoe_pack_weights (owned)
     void* ws = nullptr;
     size_t ws_bytes = 0;
     // workspace views
     float* scores = nullptr;
     float* logits = nullptr;   // router GEMM output (logit + offset) [T, n] fp32
     qbh::RouteBuffers rb{};
+    qbh::GsBuffers gb{};       // cyclic QB (qb_mode = QBMOE_QB_GAUSS_SEIDEL)
     int32_t* idx = nullptr;
     float* wts = nullptr;
     int32_t* loads = nullptr;
@@ -88,7 +113,9 @@ size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
     const size_t a = elt(c.act_dtype);
     char* p_scores = take((size_t)T * n * 4);
     char* p_logits = take((size_t)T * n * 4);
-    const size_t rbytes = qbh::route_ws_layout(T, n, k, nullptr, nullptr);
+    const bool gs = c.qb_mode == QBMOE_QB_GAUSS_SEIDEL;
+    const size_t rbytes = gs ? qbh::route_gs_ws_layout(T, n, k, nullptr, nullptr, nullptr)
+                             : qbh::route_ws_layout(T, n, k, nullptr, nullptr);
     char* p_route = take(rbytes);
     char* p_idx = take(routes * 4);
     char* p_w = take(routes * 4);
@@ -107,7 +134,8 @@ size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
     if (x && base) {
         x->scores = (float*)p_scores;
         x->logits = (float*)p_logits;
-        qbh::route_ws_layout(T, n, k, &x->rb, p_route);
+        if (gs) qbh::route_gs_ws_layout(T, n, k, &x->rb, &x->gb, p_route);
+        else qbh::route_ws_layout(T, n, k, &x->rb, p_route);
         x->idx = (int32_t*)p_idx;
         x->wts = (float*)p_w;
         x->loads = (int32_t*)p_loads;
@@ -132,6 +160,7 @@ int validate(const qbmoe_config* c, int max_tokens) {
     if (c->n_experts < 2 || c->n_experts > QBMOE_MAX_EXPERTS) return QBMOE_EINVAL;
     if (c->top_k < 1 || c->top_k >= c->n_experts || c->top_k > QBMOE_MAX_TOPK) return QBMOE_EINVAL;
     if (c->qb_sweeps < 0 || max_tokens < 1) return QBMOE_EINVAL;
+    if (c->qb_mode != QBMOE_QB_JACOBI && c->qb_mode != QBMOE_QB_GAUSS_SEIDEL) return QBMOE_EINVAL;
     if (c->act_dtype != QBMOE_F32 && c->act_dtype != QBMOE_BF16) return QBMOE_EINVAL;
     if (c->act_dtype == QBMOE_F32 && c->expert_wfmt != QBMOE_W_F32) return QBMOE_EINVAL;
     if (c->act_dtype == QBMOE_BF16 && c->expert_wfmt != QBMOE_W_BF16 && c->expert_wfmt != QBMOE_W_MXFP4)
@@ -177,7 +206,7 @@ extern "C" int qbmoe_create(qbmoe_ctx** out, const qbmoe_config* cfg, int max_to
     *out = nullptr;
     int rc = validate(cfg, max_tokens);
     if (rc) return rc;
-    if ((rc = qbmoe_check_device_arch())) return rc;
+    if ((rc = qbh::device_init())) return rc;
     qbmoe_ctx* c = new (std::nothrow) qbmoe_ctx();
     if (!c) return QBMOE_ENOMEM;
     c->cfg = *cfg;
@@ -206,6 +235,7 @@ extern "C" int qbmoe_destroy(qbmoe_ctx* c) {
     for (cudaEvent_t e : c->ev) cudaEventDestroy(e);
     qbh::tc_plan_destroy(c->tc);
     cudaFree(c->ws);
+    if (c->packed) cudaFree(c->packed);
     delete c;
     return QBMOE_OK;
 }
@@ -230,6 +260,105 @@ extern "C" int qbmoe_set_weights(qbmoe_ctx* c, const qbmoe_weights* w) {
     c->have_weights = true;
     int rc = qbh::tc_plan_set_weights(c->tc, c->cfg, *w);
     return rc;
+}
+
+namespace {
+
+// Flags E8M0 scale bytes of 0xFF (NaN: not a weight scale) in [n] bytes.
+__global__ void k_check_e8m0(const uint8_t* __restrict__ sc, long long n, int* __restrict__ bad) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        if (sc[i] == 0xFFu) atomicExch(bad, 1);
+}
+
+struct PackItem {
+    const void* src;
+    size_t bytes;
+    const void** dst;
+    bool scales;
+};
+
+}  // namespace
+
+extern "C" int qbmoe_pack_weights(qbmoe_ctx* c, const qbmoe_weights* w, qbmoe_stream_t stream) {
+    if (!c || !w) return QBMOE_EINVAL;
+    const qbmoe_config& g = c->cfg;
+    const size_t a = elt(g.act_dtype);
+    const size_t n = g.n_experts, d = g.d, L = g.latent, m = g.expert_inter, ms = g.shared_inter;
+    const bool mx = g.expert_wfmt == QBMOE_W_MXFP4;
+    const size_t we = mx ? 0 : elt(g.expert_wfmt);
+    // expert tensor bytes: MXFP4 packs two codes a byte with one scale byte per 32
+    auto ex = [&](size_t rows, size_t K) { return mx ? rows * K / 2 : rows * K * we; };
+    qbmoe_weights nw{};
+    std::vector<PackItem> items = {
+        {w->w_router, n * d * a, &nw.w_router, false},
+        {w->router_offset, w->router_offset ? n * 4 : 0, (const void**)&nw.router_offset, false},
+        {w->w_down, L * d * a, &nw.w_down, false},
+        {w->w_gate, ex(n * m, L), &nw.w_gate, false},
+        {w->w_up, ex(n * m, L), &nw.w_up, false},
+        {w->w_out, ex(n * L, m), &nw.w_out, false},
+        {w->rms_gamma, L * 4, (const void**)&nw.rms_gamma, false},
+        {w->w_proj_up, d * L * a, &nw.w_proj_up, false},
+    };
+    if (ms > 0) {
+        items.push_back({w->w_shared_gate, ms * d * a, &nw.w_shared_gate, false});
+        items.push_back({w->w_shared_up, ms * d * a, &nw.w_shared_up, false});
+        items.push_back({w->w_shared_out, d * ms * a, &nw.w_shared_out, false});
+    }
+    if (mx) {
+        items.push_back({w->s_gate, n * m * L / 32, (const void**)&nw.s_gate, true});
+        items.push_back({w->s_up, n * m * L / 32, (const void**)&nw.s_up, true});
+        items.push_back({w->s_out, n * L * m / 32, (const void**)&nw.s_out, true});
+    }
+    size_t total = 256;   // the first 256 bytes hold the scale check's flag
+    for (const PackItem& it : items) {
+        if (it.bytes && !it.src) return QBMOE_EINVAL;
+        total = qbh::align_up(total + it.bytes, 256);
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device) return QBMOE_EINVAL;
+    void* buf = nullptr;
+    if (cudaMalloc(&buf, total) != cudaSuccess) {
+        cudaGetLastError();
+        return QBMOE_ENOMEM;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(buf);
+    int* bad = reinterpret_cast<int*>(base);
+    bool ok = cudaMemsetAsync(bad, 0, sizeof(int), s) == cudaSuccess;
+    size_t off = 256;
+    for (const PackItem& it : items) {
+        if (!it.bytes) continue;
+        char* dst = base + off;
+        ok = ok && cudaMemcpyAsync(dst, it.src, it.bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess;
+        if (ok && it.scales) {
+            k_check_e8m0<<<1216, 256, 0, s>>>(reinterpret_cast<const uint8_t*>(dst), (long long)it.bytes, bad);
+            ok = cudaGetLastError() == cudaSuccess;
+        }
+        *it.dst = dst;
+        off = qbh::align_up(off + it.bytes, 256);
+    }
+    int flag = 0;
+    ok = ok && cudaMemcpyAsync(&flag, bad, sizeof(int), cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+         cudaStreamSynchronize(s) == cudaSuccess;
+    int rc = !ok ? QBMOE_ECUDA : (flag ? QBMOE_EINVAL : QBMOE_OK);
+    if (!rc) {
+        const qbmoe_weights prev = c->w;
+        const bool had = c->have_weights;
+        rc = qbmoe_set_weights(c, &nw);
+        if (rc) {
+            c->w = prev;
+            c->have_weights = had;
+            if (had) qbh::tc_plan_set_weights(c->tc, c->cfg, prev);
+        }
+    }
+    if (rc) {
+        cudaGetLastError();
+        cudaFree(buf);
+        return rc;
+    }
+    if (c->packed) cudaFree(c->packed);
+    c->packed = buf;
+    return QBMOE_OK;
 }
 
 extern "C" int qbmoe_set_timing(qbmoe_ctx* c, int slots) {
@@ -310,6 +439,7 @@ extern "C" const char* qbmoe_strerror(int code) {
 extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const float* logits_in, const float* bias_in,
                                   float* bias_out, void* out, float* scores_opt, int32_t* idx_opt, float* w_opt,
                                   int32_t* loads_opt, qbmoe_stream_t stream) {
+    // ---- every check, and every launch's parameters, before the first launch
     if (!c || !c->have_weights || !x || !out) return QBMOE_EINVAL;
     if (T < 1) return QBMOE_EINVAL;
     if (T > c->max_tokens) return QBMOE_EWORKSPACE;
@@ -318,6 +448,8 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
         if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device) return QBMOE_EINVAL;
+    int rc = qbh::device_init();
+    if (rc) return rc;
 
     const qbmoe_config& g = c->cfg;
     const int n = g.n_experts, k = g.top_k, L = g.latent, m = g.expert_inter, ms = g.shared_inter, d = g.d;
@@ -326,16 +458,29 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     const long long ldz = (long long)L + ms;
     const size_t a = elt(ad);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int nl = 0, rc = 0;
+    int nl = 0;
     StageClock clk{c, s};
     const bool use_tc = qbh::tc_enabled(c->tc);
+    const float* logits = logits_in ? logits_in : c->logits;
+    const int tpw = qbh::route_tokens_per_warp(T);
+    const int tile_rows = use_tc ? qbh::tc_token_tile(c->tc, T) : qbh::kSimtBM;
+    const size_t routes = (size_t)T * k;
+    const int max_tiles = (int)((routes + tile_rows - 1) / tile_rows) + n;
+    if (use_tc) {
+        if ((rc = qbh::tc_prepare_xside(c->tc, T, x, logits_in == nullptr, c->logits, c->h, c->zcat, ldz,
+                                        c->status)) ||
+            (rc = qbh::tc_prepare_gate_up(c->tc, T, c->h_perm, c->offsets, c->tile_off_simt, c->act, c->status)) ||
+            (rc = qbh::tc_prepare_down(c->tc, T, c->act, c->offsets, c->tile_off_simt, c->e, c->status)) ||
+            (rc = qbh::tc_prepare_up_shared(c->tc, T, c->zcat, ldz, out, c->status)))
+            return rc;
+    }
 
+    // ---- launches (a failure from here on may leave outputs partly written)
     // 1. router logits x W_r^T + o (tensor-core path: fused with the other
     //    x-side GEMMs), unless the caller gives them
-    const float* logits = logits_in ? logits_in : c->logits;
     if (use_tc) {
         clk.mark("xside_gemm");
-        rc = qbh::tc_xside(c->tc, T, x, logits_in == nullptr, c->logits, c->h, c->zcat, ldz, c->status, s, &nl);
+        rc = qbh::tc_launch(c->tc, qbh::TC_XSIDE, s, &nl);
     } else if (!logits_in) {
         clk.mark("router");
         qbh::GemmArgs ga;
@@ -347,30 +492,28 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
 
     // 2-3. scores (in the first QB token pass), QB sweeps and biased top-k
     clk.mark("qb_topk");
-    rc = qbh::launch_qb_and_topk(T, n, k, g.qb_sweeps, logits, c->scores, bias_in, bias_out, c->idx, c->wts,
-                                 c->rb.blk_cnt, c->rb, s, &nl);
+    if (g.qb_mode == QBMOE_QB_GAUSS_SEIDEL)
+        rc = qbh::launch_qb_gs(T, n, k, g.qb_sweeps, 0, logits, c->scores, bias_in, bias_out, c->idx, c->wts,
+                               c->loads, nullptr, c->rb, c->gb, s, &nl);
+    else
+        rc = qbh::launch_qb_and_topk(T, n, k, g.qb_sweeps, logits, c->scores, bias_in, bias_out, c->idx, c->wts,
+                                     c->rb.blk_cnt, c->rb, s, &nl);
     if (rc) return rc;
 
     // 4. dispatch: loads, offsets, stable permutation
     clk.mark("dispatch");
-    const int tpw = qbh::route_tokens_per_warp(T);
     if ((rc = qbh::launch_loads_from_counts(T, n, tpw, c->rb.blk_cnt, c->loads, s, &nl))) return rc;
-    const int tile_rows = use_tc ? qbh::tc_token_tile(c->tc, T) : qbh::kSimtBM;
     if ((rc = qbh::launch_expert_offsets(n, c->loads, c->offsets, tile_rows, c->tile_off_simt, s, &nl))) return rc;
     if ((rc = qbh::launch_scatter(T, n, k, tpw, c->idx, c->rb.blk_cnt, c->offsets, c->perm, c->route_pos, s, &nl)))
         return rc;
 
-    const size_t routes = (size_t)T * k;
-    const int max_tiles = (int)((routes + tile_rows - 1) / tile_rows) + n;
     if (use_tc) {
         // h rows are bf16, or E4M3 pairs of the same width for block-scaled experts
         if ((rc = qbh::launch_scatter_rows(c->h, 2 * L, c->route_pos, T, k, c->h_perm, s, &nl))) return rc;
         clk.mark("expert_gate_up");
-        rc = qbh::tc_expert_gate_up(c->tc, T, c->h_perm, c->offsets, c->tile_off_simt, c->act, c->status, s, &nl);
-        if (rc) return rc;
+        if ((rc = qbh::tc_launch(c->tc, qbh::TC_GATE_UP, s, &nl))) return rc;
         clk.mark("expert_down");
-        rc = qbh::tc_expert_down(c->tc, T, c->act, c->offsets, c->tile_off_simt, c->e, c->status, s, &nl);
-        if (rc) return rc;
+        if ((rc = qbh::tc_launch(c->tc, qbh::TC_DOWN, s, &nl))) return rc;
     } else {
         // 5. latent down-projection h = x W_down^T
         clk.mark("down_proj");
@@ -417,7 +560,7 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     // 9. out = [z | act_s] [W_proj_up | W_shared_out]^T
     clk.mark("up_proj_shared");
     if (use_tc) {
-        rc = qbh::tc_up_shared(c->tc, T, c->zcat, ldz, out, c->status, s, &nl);
+        rc = qbh::tc_launch(c->tc, qbh::TC_UP_SHARED, s, &nl);
     } else {
         qbh::GemmArgs ga;
         ga.A = c->zcat; ga.lda = ldz; ga.rows = T; ga.K1 = L; ga.W1 = c->w.w_proj_up; ga.K2 = ms;

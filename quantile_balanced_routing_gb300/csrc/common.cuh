@@ -37,7 +37,8 @@ QB_DEV float score_of_logit(float x) {
     p = __fadd_rn(__fmul_rn(p, r), 1.0f);
     const float two_j = __int_as_float(((int)j + 127) << 23);
     const float e = __fmul_rn(p, two_j);
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+    // the correctly rounded reciprocal is the IEEE quotient 1 / (1 + e)
+    return __frcp_rn(__fadd_rn(1.0f, e));
 }
 
 // SiTU-GLU: a = b1 tanh(g/b1), b = b2 tanh(u/b2), out = a sigmoid(a) b.
@@ -74,13 +75,47 @@ QB_DEV void set_status(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// scheduled while the kernel before it on the stream is still running;
+// pdl_wait blocks until that kernel has completed and its writes are
+// visible, so it comes before the first read of anything the earlier kernel
+// writes.  pdl_trigger lets the next kernel's CTAs be scheduled once every
+// CTA of this kernel has called it (or exited).  Both are no-ops for a
+// kernel launched without the attribute.
+QB_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QB_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace qb
 
 // Host-side launch helpers shared by the .cu files.
 namespace qbh {
 inline int cuda_err(cudaError_t e) { return e == cudaSuccess ? QBMOE_OK : QBMOE_ECUDA; }
+
+// Launch with programmatic stream serialisation (see qb::pdl_wait): the
+// kernel may start while the previous kernel on the stream drains.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cuda_err(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
+}
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Once per device (api.cu): checks that the current device is sm_103 and sets
+// every kernel's dynamic shared-memory limit to the largest size any call
+// uses, so that no launch sequence sets an attribute between its launches.
+int device_init();
+int route_init_attributes();   // route.cu
+int tc_init_attributes();      // gemm_tc.cu
 
 // Route kernels (route.cu)
 struct RouteBuffers {
@@ -97,4 +132,17 @@ int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* logits, flo
                        cudaStream_t s, int* nl);
 int launch_loads_from_counts(int T, int n, int tpw, const int* blk_cnt, int32_t* loads, cudaStream_t s,
                              int* nl);
+
+// Cyclic (Gauss-Seidel) QB (route.cu): the route buffers plus the sweep's own.
+struct GsBuffers {
+    float* lv;     // [T, k+1] top-(k+1) values per token
+    int* li;       // [T, k+1] their experts
+    float* mj;     // [T] margins of the expert being updated
+    float* b;      // [n] current biases
+    int* done;     // balanced flag
+};
+size_t route_gs_ws_layout(int T, int n, int k, RouteBuffers* rb, GsBuffers* gb, void* base);
+int launch_qb_gs(int T, int n, int k, int max_sweeps, int stop_when_balanced, const float* logits, float* scores,
+                 const float* bias_in, float* bias_out, int32_t* topk_idx, float* topk_w, int32_t* loads,
+                 int32_t* sweeps_done, const RouteBuffers& rb, const GsBuffers& gb, cudaStream_t s, int* nl);
 }  // namespace qbh

@@ -71,7 +71,9 @@ constexpr int kPackBytes = 128 * kBK / 2;              // packed E2M1 bytes of o
 constexpr int kScaleGroup = 8;                         // K blocks per E8M0 scale load (16 scale bytes per row)
 constexpr int kScaleBytes = 128 * 2 * kScaleGroup;     // 2 KB
 constexpr int kMaxSub = 3;
-constexpr int kStLd = 17;                      // epilogue staging row stride (floats)
+constexpr int kTokMaps = 16;                   // token-tile heights per launch (see TcParams::bx)
+constexpr int kStRow = 132;                    // epilogue staging: 16 token rows of 128 features (+4 pad)
+constexpr int kStBytes = 16 * kStRow * 4;
 constexpr long long kDefaultWait = 1LL << 17;  // polls (<= 20 us each) before a wait expires
 constexpr long long kDrainWait = 1LL << 12;    // polls per stage when draining after an expiry
 
@@ -111,7 +113,10 @@ struct SubGemm {
 struct TcParams {
     CUtensorMap a0[kMaxSub];
     CUtensorMap a1[kMaxSub];
-    CUtensorMap bx[6];  // activations, boxes {64, 8 << i} rows, i = 0..5 (8..256)
+    // token rows, one map per tile height: box {64 K, kTokUnit * (i + 1)} rows
+    // (one-CTA kernel: 16-row steps up to 256; 2-SM kernel: each CTA's half,
+    // 8-row steps up to 128), so that a token tile is one TMA copy
+    CUtensorMap bx[kTokMaps];
     CUtensorMap sc0, sc1;   // MXFP4 weights: E8M0 scales of a0 / a1 (box {16, rows})
     SubGemm sub[kMaxSub];
     int n_sub;
@@ -133,10 +138,12 @@ struct TileInfo {
 };
 
 // Tile -> (sub-GEMM, m-tile, expert, token rows).  Grouped launches read the
-// expert offsets from the CTA's shared-memory copy (s_toff, s_seg).
+// expert offsets (tile_off, seg_off: a few KB, L1-resident) from global
+// memory, which leaves the shared memory to the pipeline stages.
 template <int BN>
-__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_tiles_dense, const int* s_toff,
-                                            const int* s_seg, TileInfo& ti) {
+__device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_tiles_dense, TileInfo& ti) {
+    const int* __restrict__ s_toff = p.tile_off;
+    const int* __restrict__ s_seg = p.seg_off;
     int m;
     if (p.n_groups > 0) {
         const int ntg = tile / p.m_total;
@@ -182,36 +189,37 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, int n_t
 template <int BN>
 struct TileWalker {
     int ntg = 0, m = 0, g = 0;
-    __device__ __forceinline__ void seek(const TcParams& p, const int* s_toff) {
-        while (g + 8 < p.n_groups && s_toff[g + 8] <= ntg) g += 8;
-        while (g + 1 < p.n_groups && s_toff[g + 1] <= ntg) ++g;
+    __device__ __forceinline__ void seek(const TcParams& p) {
+        const int* __restrict__ s_toff = p.tile_off;
+        while (g + 8 < p.n_groups && __ldg(s_toff + g + 8) <= ntg) g += 8;
+        while (g + 1 < p.n_groups && __ldg(s_toff + g + 1) <= ntg) ++g;
     }
-    __device__ __forceinline__ void start(const TcParams& p, const int* s_toff) {
+    __device__ __forceinline__ void start(const TcParams& p) {
         if (p.n_groups > 0) {
             ntg = blockIdx.x / p.m_total;
             m = blockIdx.x - ntg * p.m_total;
             g = 0;
-            seek(p, s_toff);
+            seek(p);
         }
     }
-    __device__ __forceinline__ void next(const TcParams& p, const int* s_toff) {
+    __device__ __forceinline__ void next(const TcParams& p) {
         if (p.n_groups > 0) {
             m += gridDim.x;
             while (m >= p.m_total) { m -= p.m_total; ++ntg; }
-            seek(p, s_toff);
+            seek(p);
         }
     }
-    __device__ __forceinline__ void get(const TcParams& p, int tile, int n_tiles_dense, const int* s_toff,
-                                        const int* s_seg, TileInfo& ti) const {
+    __device__ __forceinline__ void get(const TcParams& p, int tile, int n_tiles_dense, TileInfo& ti) const {
         if (p.n_groups == 0) {
-            decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+            decode_tile<BN>(p, tile, n_tiles_dense, ti);
             return;
         }
         // the expert's rows split into equal tiles (multiples of 16 rows), as in decode_tile
         ti.g = g;
-        const int nt = ntg - s_toff[g];
-        const int ntiles = s_toff[g + 1] - s_toff[g];
-        const int seg0 = s_seg[g], seg1 = s_seg[g + 1];
+        const int t0 = __ldg(p.tile_off + g), t1 = __ldg(p.tile_off + g + 1);
+        const int nt = ntg - t0;
+        const int ntiles = t1 - t0;
+        const int seg0 = __ldg(p.seg_off + g), seg1 = __ldg(p.seg_off + g + 1);
         const int len = seg1 - seg0;
         const int per = ((ntiles == 1 ? len : (len + ntiles - 1) / ntiles) + 15) & ~15;
         ti.row0 = seg0 + nt * per;
@@ -249,6 +257,10 @@ __device__ __forceinline__ float situ_glu_hw(float g, float u, float b1, float i
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo& ti, const SubGemm& sg, int f_base,
                                               uint32_t tacc, int lo_col, int q, int lane, int et, float* st) {
     const int n_eff = (ti.nrows + 15) & ~15;
+    // Staging: st[j * kStRow + f] holds token j (of a 16-token chunk) of the
+    // tile's feature row f.  Each thread writes its feature row's 16 tokens
+    // (consecutive lanes, consecutive words: no bank conflict); the stores
+    // then read a token's consecutive features as float4 vectors.
     for (int c0 = 0; c0 < n_eff; c0 += 16) {
         float v[16];
         tc::tmem_ld16(tacc + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
@@ -260,7 +272,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
         }
         tc::named_bar_sync(1, 128);   // previous chunk's readers are done
 #pragma unroll
-        for (int j = 0; j < 16; ++j) st[(32 * q + lane) * kStLd + j] = v[j];
+        for (int j = 0; j < 16; ++j) st[j * kStRow + 32 * q + lane] = v[j];
         tc::named_bar_sync(1, 128);
         const int tok_left = ti.nrows - c0;
         if (sg.epi == SUB_STORE) {
@@ -272,21 +284,23 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
                 const int j = item >> 4, fg = item & 15;
                 const int f = f_base + fg * 8;
                 if (j < tok_left && f < sg.F) {
+                    const float4 a = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8);
+                    const float4 b = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8 + 4);
+                    const float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                     if (sg.out_e4m3) {
                         // the bf16 value as an E4M3 pair: hi plane, then lo plane F bytes on
                         __align__(8) uint8_t oh[8];
                         __align__(8) uint8_t ol[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            e4m3_pair(__bfloat162float(__float2bfloat16_rn(st[(fg * 8 + u) * kStLd + j])), oh[u],
-                                      ol[u]);
+                            e4m3_pair(__bfloat162float(__float2bfloat16_rn(x8[u])), oh[u], ol[u]);
                         uint8_t* o8 = static_cast<uint8_t*>(sg.out) + (long long)(ti.row0 + c0 + j) * sg.ldo + f;
                         *reinterpret_cast<uint2*>(o8) = *reinterpret_cast<const uint2*>(oh);
                         *reinterpret_cast<uint2*>(o8 + sg.F) = *reinterpret_cast<const uint2*>(ol);
                     } else {
                         __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(st[(fg * 8 + u) * kStLd + j]);
+                        for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(x8[u]);
                         *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
                             *reinterpret_cast<const uint4*>(o);
                     }
@@ -301,13 +315,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
                 const int j = item >> 5, fg = item & 31;
                 const int f = f_base + fg * 4;
                 if (j < tok_left && f < sg.F) {
-                    float4 o;
-                    float* op = &o.x;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float lg = st[(fg * 4 + u) * kStLd + j];
-                        if (sg.col_bias) lg = __fadd_rn(lg, sg.col_bias[f + u]);
-                        op[u] = lg;   // the score is taken from this logit by the QB token pass
+                    float4 o = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 4);
+                    if (sg.col_bias) {
+                        // the score is taken from this logit by the QB token pass
+                        o.x = __fadd_rn(o.x, sg.col_bias[f + 0]);
+                        o.y = __fadd_rn(o.y, sg.col_bias[f + 1]);
+                        o.z = __fadd_rn(o.z, sg.col_bias[f + 2]);
+                        o.w = __fadd_rn(o.w, sg.col_bias[f + 3]);
                     }
                     *reinterpret_cast<float4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) = o;
                 }
@@ -318,13 +332,16 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
             const int f = f_base + fg * 8;
             if (j < tok_left && f < sg.F) {
                 const float inv_b1 = 1.0f / p.beta1, inv_b2 = 1.0f / p.beta2;
+                const float* row = st + j * kStRow;
+                const float4 g0 = *reinterpret_cast<const float4*>(row + fg * 8);
+                const float4 g1 = *reinterpret_cast<const float4*>(row + fg * 8 + 4);
+                const float4 u0 = *reinterpret_cast<const float4*>(row + 64 + fg * 8);
+                const float4 u1 = *reinterpret_cast<const float4*>(row + 64 + fg * 8 + 4);
+                const float g8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                const float u8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 float a[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float g = st[(fg * 8 + u) * kStLd + j];
-                    const float up = st[(64 + fg * 8 + u) * kStLd + j];
-                    a[u] = situ_glu_hw(g, up, p.beta1, inv_b1, p.beta2, inv_b2);
-                }
+                for (int u = 0; u < 8; ++u) a[u] = situ_glu_hw(g8[u], u8[u], p.beta1, inv_b1, p.beta2, inv_b2);
                 const long long off = (long long)(ti.row0 + c0 + j) * sg.ldo + f;
                 if (sg.out_e4m3) {
                     // the bf16 activation as an E4M3 pair: hi plane, then lo plane F bytes on
@@ -431,18 +448,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* st = reinterpret_cast<float*>(tmem_slot + 4);   // [128][kStLd]
-    int* s_toff = reinterpret_cast<int*>(st + 128 * kStLd);   // [n_groups + 1] (grouped only)
-    int* s_seg = s_toff + (QBMOE_MAX_EXPERTS + 1);            // [n_groups + 1]
+    // [16][kStRow] epilogue staging, read and written as float4: 16-byte aligned
+    float* st = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long lim = p.wait_limit > 0 ? p.wait_limit : kDefaultWait;
-    if (p.n_groups > 0) {
-        for (int i = threadIdx.x; i <= p.n_groups; i += blockDim.x) {
-            s_toff[i] = __ldg(p.tile_off + i);
-            s_seg[i] = __ldg(p.seg_off + i);
-        }
-    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -466,7 +476,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::fence_proxy_async_smem();
-        for (int i = 0; i < 6; ++i) tc::prefetch_tmap(&p.bx[i]);
+        for (int i = 0; i < BN / 16; ++i) tc::prefetch_tmap(&p.bx[i]);
     }
     if (warp == kMmaWarp) {
         tc::tmem_alloc(tmem_slot, kCols);
@@ -478,7 +488,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     const uint32_t tbase = *tmem_slot;
 
     const int n_tiles_dense = p.n_groups > 0 ? 0 : (p.rows + BN - 1) / BN;
-    const int n_tiles = p.n_groups > 0 ? s_toff[p.n_groups] * p.m_total : n_tiles_dense * p.m_total;
+    const int n_tiles = p.n_groups > 0 ? __ldg(p.tile_off + p.n_groups) * p.m_total : n_tiles_dense * p.m_total;
 
     constexpr int kNProd = MX ? 1 : 2;   // producer pairs
     const bool is_prod = warp == kProdAWarp || warp == kProdBWarp ||
@@ -499,10 +509,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             int s = 0;
             uint32_t ph = 0;
             TileWalker<BN> tw;
-            tw.start(p, s_toff);
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p, s_toff)) {
+            tw.start(p);
+            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p)) {
                 TileInfo ti;
-                tw.get(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                tw.get(p, tile, n_tiles_dense, ti);
                 const SubGemm& sg = p.sub[ti.sub];
                 const int n_eff = (ti.nrows + 15) & ~15;
                 for (int kb = 0; kb < p.nkb; ++kb) {
@@ -580,21 +590,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                     } else {
                         uint8_t* B = b_ring + s * kBBytes;
                         tc::mbar_expect_tx(&fullx[s], (MXS ? 2 : 1) * n_eff * 128);
-                        // n_eff rows as a sum of power-of-two boxes (largest first): <= 5 TMA issues
-                        // per plane (block-scaled: hi columns kb * 128, lo columns K + kb * 128,
-                        // the lo rows stacked under the hi rows)
-                        int r = 0;
-#pragma unroll
-                        for (int i = 5; i >= 1; --i) {
-                            const int h = 8 << i;
-                            if (h <= BN && (n_eff - r) >= h) {
-                                tc::tma_load_2d(B + r * 128, &p.bx[i], &fullx[s], kb * kKS, ti.row0 + r);
-                                if (MXS)
-                                    tc::tma_load_2d(B + (n_eff + r) * 128, &p.bx[i], &fullx[s], (p.nkb + kb) * kKS,
-                                                    ti.row0 + r);
-                                r += h;
-                            }
-                        }
+                        // the n_eff token rows as one box (block-scaled: hi columns kb * 128, lo
+                        // columns K + kb * 128, the lo rows stacked under the hi rows)
+                        const CUtensorMap* bmap = &p.bx[(n_eff >> 4) - 1];
+                        tc::tma_load_2d(B, bmap, &fullx[s], kb * kKS, ti.row0);
+                        if (MXS) tc::tma_load_2d(B + n_eff * 128, bmap, &fullx[s], (p.nkb + kb) * kKS, ti.row0);
                     }
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -738,10 +738,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             int ab = 0;
             uint32_t aph = 0;
             TileWalker<BN> tw;
-            tw.start(p, s_toff);
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p, s_toff)) {
+            tw.start(p);
+            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p)) {
                 TileInfo ti;
-                tw.get(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                tw.get(p, tile, n_tiles_dense, ti);
                 const uint32_t n_eff = (ti.nrows + 15) & ~15;
                 const uint32_t idesc = tc::idesc_bf16_m128(n_eff);
                 if (!tc::mbar_wait<kTestFirst>(&acce[ab], aph ^ 1u, lim)) {
@@ -807,10 +807,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         uint32_t aph = 0;
         volatile int* ok_slot = abort_flag + 1;
         TileWalker<BN> tw;
-        tw.start(p, s_toff);
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, tw.next(p, s_toff)) {
+        tw.start(p);
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, tw.next(p)) {
             TileInfo ti;
-            tw.get(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+            tw.get(p, tile, n_tiles_dense, ti);
             const SubGemm& sg = p.sub[ti.sub];
             // one thread waits; the verdict is shared so the 128 threads stay uniform
             if (et == 0) {
@@ -869,20 +869,13 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* st = reinterpret_cast<float*>(tmem_slot + 4);
-    int* s_toff = reinterpret_cast<int*>(st + 128 * kStLd);
-    int* s_seg = s_toff + (QBMOE_MAX_EXPERTS + 1);
+    // [16][kStRow] epilogue staging, read and written as float4: 16-byte aligned
+    float* st = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = tc::cluster_ctarank();
     const bool leader = rank == 0;
     const long long lim = p.wait_limit > 0 ? p.wait_limit : kDefaultWait;
-    if (p.n_groups > 0) {
-        for (int i = threadIdx.x; i <= p.n_groups; i += blockDim.x) {
-            s_toff[i] = __ldg(p.tile_off + i);
-            s_seg[i] = __ldg(p.seg_off + i);
-        }
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(&full[s], 2);    // the leader's two producers arrive; both CTAs' copies complete on it
@@ -896,7 +889,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
         *abort_flag = 0;
         tc::fence_mbar_init();
         tc::fence_proxy_async_smem();
-        for (int i = 0; i < 6; ++i) tc::prefetch_tmap(&p.bx[i]);
+        for (int i = 0; i < kHalf / 8; ++i) tc::prefetch_tmap(&p.bx[i]);
     }
     if (warp == kMmaWarp) {
         tc::tmem_alloc_pair(tmem_slot, kCols);
@@ -910,7 +903,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
 
     const int cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
     const int n_tiles_dense = p.n_groups > 0 ? 0 : (p.rows + BN - 1) / BN;
-    const int n_tiles = p.n_groups > 0 ? s_toff[p.n_groups] * p.m_total : n_tiles_dense * p.m_total;
+    const int n_tiles = p.n_groups > 0 ? __ldg(p.tile_off + p.n_groups) * p.m_total : n_tiles_dense * p.m_total;
 
     const bool is_prod = warp == kProdAWarp || warp == kProdBWarp || warp == kProdA1Warp || warp == kProdB1Warp;
     if (is_prod) {
@@ -925,7 +918,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
             uint32_t ph = 0;
             for (int tile = cl; tile < n_tiles && !*abort_flag; tile += ncl) {
                 TileInfo ti;
-                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                decode_tile<BN>(p, tile, n_tiles_dense, ti);
                 const SubGemm& sg = p.sub[ti.sub];
                 const int n_eff = (ti.nrows + 15) & ~15;
                 const int half = n_eff >> 1;
@@ -958,15 +951,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
                         uint8_t* B = b_ring + s * kBBytes;
                         if (leader) tc::mbar_expect_tx(&fullx[s], n_eff * kBK * 2);
                         const int row0 = ti.row0 + (int)rank * half;
-                        int r = 0;
-#pragma unroll
-                        for (int i = 4; i >= 0; --i) {
-                            const int h = 8 << i;
-                            if (h <= kHalf && (half - r) >= h) {
-                                tc::tma_load_2d_pair(B + r * kBK * 2, &p.bx[i], bar, kb * kBK, row0 + r);
-                                r += h;
-                            }
-                        }
+                        tc::tma_load_2d_pair(B, &p.bx[(half >> 3) - 1], bar, kb * kBK, row0);
                     }
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -992,7 +977,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
             uint32_t aph = 0;
             for (int tile = cl; tile < n_tiles && !*abort_flag; tile += ncl) {
                 TileInfo ti;
-                decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+                decode_tile<BN>(p, tile, n_tiles_dense, ti);
                 const uint32_t n_eff = (ti.nrows + 15) & ~15;
                 const uint32_t idesc = tc::idesc_bf16_m256(n_eff);
                 if (!tc::mbar_wait<true>(&acce[ab], aph ^ 1u, lim)) {
@@ -1039,7 +1024,7 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
         volatile int* ok_slot = abort_flag + 1;
         for (int tile = cl; tile < n_tiles; tile += ncl) {
             TileInfo ti;
-            decode_tile<BN>(p, tile, n_tiles_dense, s_toff, s_seg, ti);
+            decode_tile<BN>(p, tile, n_tiles_dense, ti);
             const SubGemm& sg = p.sub[ti.sub];
             if (et == 0) {
                 const bool ok = tc::mbar_wait<true>(&accf[ab], aph, lim);
@@ -1079,20 +1064,19 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
 // Pipeline depths (stages of one weight tile + one token tile), chosen by
 // measurement on GB300 within the 227 KB of shared memory per CTA.
 template <int BN> struct Stages;
-template <> struct Stages<16> { static constexpr int S = 11; };
-template <> struct Stages<64> { static constexpr int S = 8; };
+template <> struct Stages<16> { static constexpr int S = 12; };
+template <> struct Stages<64> { static constexpr int S = 9; };
 template <> struct Stages<128> { static constexpr int S = 6; };
-template <> struct Stages<160> { static constexpr int S = 5; };
+template <> struct Stages<160> { static constexpr int S = 6; };
 template <> struct Stages<256> { static constexpr int S = 4; };
 
 // 2-SM kernel: per-CTA token stages hold BN/2 rows.
 template <int BN> struct Stages2;
-template <> struct Stages2<160> { static constexpr int S = 7; };
+template <> struct Stages2<160> { static constexpr int S = 8; };
 template <> struct Stages2<256> { static constexpr int S = 6; };
 template <int BN>
 constexpr size_t smem2_for() {
-    return 1024 + (size_t)Stages2<BN>::S * (kATileBytes + (BN / 2) * kBK * 2) + 512 + 128 * kStLd * 4 +
-           2 * (QBMOE_MAX_EXPERTS + 1) * 4;
+    return 1024 + (size_t)Stages2<BN>::S * (kATileBytes + (BN / 2) * kBK * 2) + 512 + kStBytes;
 }
 
 // MXFP4 weights: each stage also holds a 4 KB packed block.
@@ -1120,12 +1104,25 @@ constexpr size_t smem_for() {
     constexpr int S = stages_of<BN, MODE>();
     constexpr bool MX = MODE == MODE_MX_DECODE, MXS = MODE == MODE_MX_SCALED;
     return 1024 + (size_t)S * (kATileBytes + (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
-           (MX || MXS ? 2 * kScaleBytes : 0) + 768 + 128 * kStLd * 4 + 2 * (QBMOE_MAX_EXPERTS + 1) * 4;
+           (MX || MXS ? 2 * kScaleBytes : 0) + 768 + kStBytes;
 }
 
 }  // namespace
 
 namespace qbh {
+
+// One prepared launch: parameters with every tensor map encoded, the token
+// tile and the kernel variant.  Filled by the tc_prepare_* calls, consumed
+// by tc_launch.
+struct TcLaunch {
+    TcParams prm;
+    int BN = 0;
+    bool pair = false;
+    int mode = MODE_BF16;
+    bool grouped = false;
+    long long tiles = 0;
+    bool ready = false;
+};
 
 struct TcPlan {
     bool enabled = false;
@@ -1138,8 +1135,9 @@ struct TcPlan {
     bool pair_dense = false;     // dense 256-row launches on the 2-SM kernel (default; QBMOE_DISABLE_2SM=1 turns off)
     bool pair_grouped = false;   // grouped launches on the 2-SM kernel (QBMOE_ENABLE_2SM=1)
     bool mx_scaled = false;  // MXFP4 experts on the block-scaled MMA (else decoded to bf16 in SMEM)
-    int pair_clusters[2] = {0, 0};   // co-resident clusters of the 160 / 256 variants (0 = not queried)
+    int pair_clusters[2] = {0, 0};   // co-resident clusters of the 160 / 256 variants
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    TcLaunch stage[TC_STAGES];       // the forward's launches, prepared before the first one
 };
 
 namespace {
@@ -1172,12 +1170,13 @@ bool make_map(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long 
     return r == CUDA_SUCCESS;
 }
 
-// Token-tile maps with box heights 8, 16, ..., 256 (those above BN unused).
-bool make_token_maps(TcPlan* P, TcParams& prm, const void* x, long long rows, long long K, long long ld, int BN) {
-    for (int i = 0; i < 6; ++i) {
-        const int h = std::min(8 << i, BN);
-        if (!make_map(P, &prm.bx[i], x, rows, K, ld, h)) return false;
-    }
+// Token-tile maps with box heights unit, 2 unit, ..., max_rows (one per
+// tile height the launch can meet; unit 16 for the one-CTA kernel's tiles,
+// 8 for the 2-SM kernel's per-CTA halves).
+bool make_token_maps(TcPlan* P, TcParams& prm, const void* x, long long rows, long long K, long long ld, int unit,
+                     int max_rows) {
+    for (int i = 0; i < kTokMaps && unit * (i + 1) <= max_rows; ++i)
+        if (!make_map(P, &prm.bx[i], x, rows, K, ld, unit * (i + 1))) return false;
     return true;
 }
 
@@ -1196,10 +1195,8 @@ bool make_map_e4m3(TcPlan* P, CUtensorMap* m, const void* base, long long rows, 
 }
 
 bool make_token_maps_e4m3(TcPlan* P, TcParams& prm, const void* x, long long rows, long long K, int BN) {
-    for (int i = 0; i < 6; ++i) {
-        const int h = std::min(8 << i, BN);
-        if (!make_map_e4m3(P, &prm.bx[i], x, rows, K, K, h)) return false;
-    }
+    for (int i = 0; i < kTokMaps && 16 * (i + 1) <= BN; ++i)
+        if (!make_map_e4m3(P, &prm.bx[i], x, rows, K, K, 16 * (i + 1))) return false;
     return true;
 }
 
@@ -1234,33 +1231,59 @@ bool make_map_u8(TcPlan* P, CUtensorMap* m, const void* base, long long rows, lo
     return r == CUDA_SUCCESS;
 }
 
+// Dynamic shared memory limits are set once per device by
+// tc_init_attributes (before any launch of the library on that device).
+template <int BN, int MODE>
+int attr_bn() {
+    constexpr size_t smem = smem_for<BN, MODE>();
+    static_assert(smem <= 232448, "shared memory per CTA");
+    return cuda_err(cudaFuncSetAttribute(k_tc_gemm<BN, stages_of<BN, MODE>(), MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+}
+
+template <int BN>
+int attr_bn2() {
+    constexpr size_t smem = smem2_for<BN>();
+    static_assert(smem <= 232448, "shared memory per CTA");
+    return cuda_err(cudaFuncSetAttribute(k_tc_gemm2<BN, Stages2<BN>::S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem));
+}
+
 template <int BN, int MODE>
 int launch_bn(TcParams& prm, int grid, cudaStream_t s) {
     constexpr size_t smem = smem_for<BN, MODE>();
-    static_assert(smem <= 232448, "shared memory per CTA");
     constexpr int S = stages_of<BN, MODE>();
-    auto kern = k_tc_gemm<BN, S, MODE>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
-    if (attr_err != cudaSuccess) return QBMOE_ECUDA;
-    kern<<<grid, threads_of<MODE>(), smem, s>>>(prm);
+    k_tc_gemm<BN, S, MODE><<<grid, threads_of<MODE>(), smem, s>>>(prm);
     return cuda_err(cudaGetLastError());
+}
+
+// Co-resident clusters of the 2-SM kernel (queried once per plan).
+template <int BN>
+int pair_occupancy(int num_sms, int* out) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreadsBf16, 1, 1);
+    cfg.dynamicSmemBytes = smem2_for<BN>();
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(num_sms & ~1, 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_tc_gemm2<BN, Stages2<BN>::S>, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return QBMOE_ECUDA;
+    }
+    *out = n;
+    return QBMOE_OK;
 }
 
 template <int BN>
 int launch_bn2(TcPlan* P, TcParams& prm, int tiles, cudaStream_t s) {
     constexpr size_t smem = smem2_for<BN>();
-    static_assert(smem <= 232448, "shared memory per CTA");
     auto kern = k_tc_gemm2<BN, Stages2<BN>::S>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
-    if (attr_err != cudaSuccess) return QBMOE_ECUDA;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -1272,16 +1295,8 @@ int launch_bn2(TcPlan* P, TcParams& prm, int tiles, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int& maxc = P->pair_clusters[BN == 256 ? 1 : 0];
-    if (maxc == 0) {
-        cfg.gridDim = dim3(P->num_sms & ~1, 1, 1);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-            cudaGetLastError();
-            return QBMOE_ECUDA;
-        }
-        maxc = n;
-    }
+    const int maxc = P->pair_clusters[BN == 256 ? 1 : 0];
+    if (maxc <= 0) return QBMOE_ECUDA;
     const int clusters = std::max(1, std::min(maxc, tiles));
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return QBMOE_ECUDA;
@@ -1346,18 +1361,36 @@ bool use_pair(const TcPlan* P, int BN, bool grouped) {
 }
 
 // Dense launch over T token rows; n_tiles x m_total tiles.
-int launch_dense(TcPlan* P, TcParams& prm, int BN, bool pair, int T, const void* x, long long ldx, long long K,
-                 cudaStream_t s, int* nl) {
-    if (!make_token_maps(P, prm, x, T, K, ldx, BN)) return QBMOE_ECUDA;
+int prep_dense(TcPlan* P, TcLaunch& L, int BN, bool pair, int T, const void* x, long long ldx, long long K) {
+    TcParams& prm = L.prm;
+    if (!make_token_maps(P, prm, x, T, K, ldx, pair ? 8 : 16, pair ? BN / 2 : BN)) return QBMOE_ECUDA;
     prm.rows = T;
     prm.nkb = (int)((K + kBK - 1) / kBK);
     prm.n_groups = 0;
     prm.raster_g = std::min(prm.m_total, pair ? 8 : 16);
-    const long long tiles = (long long)prm.m_total * ((T + BN - 1) / BN);
-    if (nl) ++*nl;
-    if (pair) return BN == 256 ? launch_bn2<256>(P, prm, (int)std::min<long long>(tiles, 1 << 30), s) : QBMOE_EINVAL;
-    const int grid = (int)std::min<long long>(tiles, P->num_sms);
-    return launch_any(BN, prm, std::max(grid, 1), s);
+    L.BN = BN;
+    L.pair = pair;
+    L.mode = MODE_BF16;
+    L.grouped = false;
+    L.tiles = (long long)prm.m_total * ((T + BN - 1) / BN);
+    if (pair && BN != 256) return QBMOE_EINVAL;
+    L.ready = true;
+    return QBMOE_OK;
+}
+
+int launch_prepared(TcPlan* P, TcLaunch& L, cudaStream_t s) {
+    if (!L.ready) return QBMOE_EINVAL;
+    L.ready = false;
+    if (!L.grouped) {
+        if (L.pair) return launch_bn2<256>(P, L.prm, (int)std::min<long long>(L.tiles, 1 << 30), s);
+        const int grid = (int)std::min<long long>(L.tiles, P->num_sms);
+        return launch_any(L.BN, L.prm, std::max(grid, 1), s);
+    }
+    if (L.mode == MODE_MX_SCALED) return launch_mx_scaled(L.BN, L.prm, P->num_sms, s);
+    if (L.mode == MODE_MX_DECODE) return launch_mx_decode(L.BN, L.prm, P->num_sms, s);
+    if (L.pair)
+        return L.BN == 160 ? launch_bn2<160>(P, L.prm, 1 << 30, s) : launch_bn2<256>(P, L.prm, 1 << 30, s);
+    return launch_any(L.BN, L.prm, P->num_sms, s);
 }
 
 }  // namespace
@@ -1389,7 +1422,24 @@ TcPlan* tc_plan_create(const qbmoe_config& cfg) {
     // the in-SMEM decode to bf16.
     const char* env3 = getenv("QBMOE_MX_DECODE");
     P->mx_scaled = cfg.expert_wfmt == QBMOE_W_MXFP4 && !(env3 && env3[0] == '1');
+    if (P->enabled && (pair_occupancy<160>(P->num_sms, &P->pair_clusters[0]) ||
+                       pair_occupancy<256>(P->num_sms, &P->pair_clusters[1]))) {
+        // the 2-SM kernel cannot be placed: run everything on the one-CTA kernel
+        P->pair_dense = P->pair_grouped = false;
+    }
     return P;
+}
+
+int tc_init_attributes() {
+    int rc;
+    if ((rc = attr_bn<16, MODE_BF16>()) || (rc = attr_bn<64, MODE_BF16>()) || (rc = attr_bn<128, MODE_BF16>()) ||
+        (rc = attr_bn<160, MODE_BF16>()) || (rc = attr_bn<256, MODE_BF16>()) ||
+        (rc = attr_bn<16, MODE_MX_DECODE>()) || (rc = attr_bn<64, MODE_MX_DECODE>()) ||
+        (rc = attr_bn<160, MODE_MX_DECODE>()) || (rc = attr_bn<16, MODE_MX_SCALED>()) ||
+        (rc = attr_bn<64, MODE_MX_SCALED>()) || (rc = attr_bn<112, MODE_MX_SCALED>()) ||
+        (rc = attr_bn2<160>()) || (rc = attr_bn2<256>()))
+        return rc;
+    return QBMOE_OK;
 }
 
 void tc_plan_destroy(TcPlan* p) { delete p; }
@@ -1432,14 +1482,16 @@ static int m_tiles_of(int F, bool situ, bool pair) {
     return (F + rows - 1) / rows;
 }
 
-int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, void* h, void* zcat, long long ldz,
-             int* status, cudaStream_t s, int* nl) {
+int tc_prepare_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, void* h, void* zcat,
+                     long long ldz, int* status) {
     const qbmoe_config& c = P->cfg;
     const long long m128 = (with_router ? (c.n_experts + 127) / 128 : 0) + (c.latent + 127) / 128 +
                            (c.shared_inter + 63) / 64;
     const int BN = dense_bn(m128, T, P->num_sms);
     const bool pair = use_pair(P, BN, false);
-    TcParams prm;
+    TcLaunch& L = P->stage[TC_XSIDE];
+    L.ready = false;
+    TcParams& prm = L.prm;
     base_params(P, prm, status);
     int m = 0, ns = 0;
     if (with_router) {
@@ -1479,18 +1531,18 @@ int tc_xside(TcPlan* P, int T, const void* x, bool with_router, float* logits, v
     }
     prm.n_sub = ns;
     prm.m_total = m;
-    return launch_dense(P, prm, BN, pair, T, x, c.d, c.d, s, nl);
+    return prep_dense(P, L, BN, pair, T, x, c.d, c.d);
 }
 
-static int launch_grouped(TcPlan* P, TcParams& prm, bool pair, const void* act, long long routes, long long K,
-                          const int* offsets, const int* tile_off, int BN, cudaStream_t s, int* nl,
-                          int mode = MODE_BF16) {
+static int prep_grouped(TcPlan* P, TcLaunch& L, bool pair, const void* act, long long routes, long long K,
+                        const int* offsets, const int* tile_off, int BN, int mode) {
+    TcParams& prm = L.prm;
     if (mode == MODE_MX_SCALED) {
         // E4M3 pairs: rows of 2K bytes (hi plane, then lo plane)
         if (!make_token_maps_e4m3(P, prm, act, routes, 2 * K, BN)) return QBMOE_ECUDA;
         prm.nkb = (int)(K / kBKS);
     } else {
-        if (!make_token_maps(P, prm, act, routes, K, K, BN)) return QBMOE_ECUDA;
+        if (!make_token_maps(P, prm, act, routes, K, K, pair ? 8 : 16, pair ? BN / 2 : BN)) return QBMOE_ECUDA;
         prm.nkb = (int)((K + kBK - 1) / kBK);
     }
     prm.n_groups = P->cfg.n_experts;
@@ -1498,21 +1550,26 @@ static int launch_grouped(TcPlan* P, TcParams& prm, bool pair, const void* act, 
     prm.tile_off = tile_off;
     prm.rows = 0;
     prm.raster_g = 1;
-    if (nl) ++*nl;
-    if (mode == MODE_MX_SCALED) return launch_mx_scaled(BN, prm, P->num_sms, s);
-    if (mode == MODE_MX_DECODE) return launch_mx_decode(BN, prm, P->num_sms, s);
-    if (pair) return BN == 160 ? launch_bn2<160>(P, prm, 1 << 30, s) : launch_bn2<256>(P, prm, 1 << 30, s);
-    return launch_any(BN, prm, P->num_sms, s);
+    L.BN = BN;
+    L.pair = pair;
+    L.mode = mode;
+    L.grouped = true;
+    L.tiles = 0;
+    if (pair && BN != 160 && BN != 256) return QBMOE_EINVAL;
+    L.ready = true;
+    return QBMOE_OK;
 }
 
-int tc_expert_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets, const int* tile_off, void* act,
-                      int* status, cudaStream_t s, int* nl) {
+int tc_prepare_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets, const int* tile_off, void* act,
+                       int* status) {
     const qbmoe_config& c = P->cfg;
     const long long routes = (long long)T * c.top_k;
     const int BN = tc_token_tile(P, T);
     const bool mx = c.expert_wfmt == QBMOE_W_MXFP4;
     const bool pair = !mx && use_pair(P, BN, true);
-    TcParams prm;
+    TcLaunch& L = P->stage[TC_GATE_UP];
+    L.ready = false;
+    TcParams& prm = L.prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
     SubGemm& g = prm.sub[0];
@@ -1544,17 +1601,19 @@ int tc_expert_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets, 
         return QBMOE_ECUDA;
     }
     prm.m_total = g.m_tiles;
-    return launch_grouped(P, prm, pair, h_perm, routes, c.latent, offsets, tile_off, BN, s, nl, mode);
+    return prep_grouped(P, L, pair, h_perm, routes, c.latent, offsets, tile_off, BN, mode);
 }
 
-int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const int* tile_off, void* e,
-                   int* status, cudaStream_t s, int* nl) {
+int tc_prepare_down(TcPlan* P, int T, const void* act, const int* offsets, const int* tile_off, void* e,
+                    int* status) {
     const qbmoe_config& c = P->cfg;
     const long long routes = (long long)T * c.top_k;
     const int BN = tc_token_tile(P, T);
     const bool mx = c.expert_wfmt == QBMOE_W_MXFP4;
     const bool pair = !mx && use_pair(P, BN, true);
-    TcParams prm;
+    TcLaunch& L = P->stage[TC_DOWN];
+    L.ready = false;
+    TcParams& prm = L.prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
     SubGemm& g = prm.sub[0];
@@ -1577,15 +1636,16 @@ int tc_expert_down(TcPlan* P, int T, const void* act, const int* offsets, const 
     }
     prm.a1[0] = prm.a0[0];
     prm.m_total = g.m_tiles;
-    return launch_grouped(P, prm, pair, act, routes, c.expert_inter, offsets, tile_off, BN, s, nl, mode);
+    return prep_grouped(P, L, pair, act, routes, c.expert_inter, offsets, tile_off, BN, mode);
 }
 
-int tc_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, int* status, cudaStream_t s,
-                 int* nl) {
+int tc_prepare_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, int* status) {
     const qbmoe_config& c = P->cfg;
     const int BN = dense_bn((c.d + 127) / 128, T, P->num_sms);
     const bool pair = use_pair(P, BN, false);
-    TcParams prm;
+    TcLaunch& L = P->stage[TC_UP_SHARED];
+    L.ready = false;
+    TcParams& prm = L.prm;
     base_params(P, prm, status);
     prm.n_sub = 1;
     SubGemm& g = prm.sub[0];
@@ -1599,7 +1659,13 @@ int tc_up_shared(TcPlan* P, int T, const void* zcat, long long ldz, void* out, i
         prm.a1[0] = prm.a0[0];
     }
     prm.m_total = g.m_tiles;
-    return launch_dense(P, prm, BN, pair, T, zcat, ldz, (long long)c.latent + c.shared_inter, s, nl);
+    return prep_dense(P, L, BN, pair, T, zcat, ldz, (long long)c.latent + c.shared_inter);
+}
+
+int tc_launch(TcPlan* P, int stage, cudaStream_t s, int* nl) {
+    if (!P || stage < 0 || stage >= TC_STAGES) return QBMOE_EINVAL;
+    if (nl) ++*nl;
+    return launch_prepared(P, P->stage[stage], s);
 }
 
 }  // namespace qbh

@@ -17,20 +17,27 @@ int tc_token_tile(const TcPlan* p, int T);
 void tc_set_wait_limit(TcPlan* p, long long iterations);
 void tc_set_stall(TcPlan* p, int on);
 
+// The layer's tensor-core launches.  Each tc_prepare_* call builds one
+// launch's parameters (every tensor map encoded, tile and kernel variant
+// chosen) without touching the device; tc_launch enqueues a prepared launch.
+// moe_latent_forward prepares all of them before its first launch, so that
+// a failure to prepare leaves nothing launched.
+enum { TC_XSIDE = 0, TC_GATE_UP = 1, TC_DOWN = 2, TC_UP_SHARED = 3, TC_STAGES = 4 };
+
 // Router logits (optional; fp32 x W_r^T + o) + latent down-projection +
 // shared gate/up in one launch.  h is bf16 [T, latent], or E4M3 pairs (hi
 // plane, then lo plane: 2 x latent bytes a row) when the expert GEMMs run on
 // the block-scaled MMA.
-int tc_xside(TcPlan* p, int T, const void* x, bool with_router, float* logits, void* h, void* zcat, long long ldz,
-             int* status, cudaStream_t s, int* nl);
+int tc_prepare_xside(TcPlan* p, int T, const void* x, bool with_router, float* logits, void* h, void* zcat,
+                     long long ldz, int* status);
 // Whether the MXFP4 expert GEMMs run on the block-scaled MMA: their token
 // inputs (h_perm, act) are then E4M3 bytes.
 bool tc_mx_scaled(const TcPlan* p);
-int tc_expert_gate_up(TcPlan* p, int T, const void* h_perm, const int* offsets, const int* tile_off, void* act,
-                      int* status, cudaStream_t s, int* nl);
-int tc_expert_down(TcPlan* p, int T, const void* act, const int* offsets, const int* tile_off, void* e,
-                   int* status, cudaStream_t s, int* nl);
-int tc_up_shared(TcPlan* p, int T, const void* zcat, long long ldz, void* out, int* status, cudaStream_t s,
-                 int* nl);
+int tc_prepare_gate_up(TcPlan* p, int T, const void* h_perm, const int* offsets, const int* tile_off, void* act,
+                       int* status);
+int tc_prepare_down(TcPlan* p, int T, const void* act, const int* offsets, const int* tile_off, void* e,
+                    int* status);
+int tc_prepare_up_shared(TcPlan* p, int T, const void* zcat, long long ldz, void* out, int* status);
+int tc_launch(TcPlan* p, int stage, cudaStream_t s, int* nl);
 
 }  // namespace qbh

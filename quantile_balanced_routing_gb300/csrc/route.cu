@@ -36,9 +36,9 @@ using namespace qb;
 constexpr int kTokPassTokens = 8;    // tokens per CTA in the token pass (one per warp)
 constexpr int kTokPassWarps = 8;
 constexpr int kTopkWarps = 8;
-constexpr int kSelectThreads = 512;
+constexpr int kSelectThreads = 256;
 constexpr int kSelectSmemMaxT = 48 * 1024;   // margins staged in SMEM up to this T
-constexpr int kSelectCand = 4096;            // candidate words after the first digit pass
+constexpr int kSelectCand = 1024;            // candidate words after the first digit pass (6 CTAs per SM at T = 4096)
 
 __global__ void k_scores(const float* __restrict__ logits, float* __restrict__ scores, long long count) {
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -252,6 +252,8 @@ k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __res
     constexpr int LD = kTokPassTokens + 1;
     const int tl = warp;
     const int t = t0 + tl;
+    pdl_wait();
+    pdl_trigger();
     // the token's row is requested before the biases are staged
     const float* src = kFromLogits ? logits + (size_t)t * n : scores + (size_t)t * n;
     float x[NPL];
@@ -300,30 +302,38 @@ k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __res
 }
 
 // Radix select of the rank-th largest margin of one expert's column: the
-// rank-th smallest descending key (~order_key(margin), rank 1-based), four
-// 8-bit digit passes.  With the column staged in shared memory, the keys of
-// the first pass's chosen bucket are compacted (when they fit kSelectCand
-// words) and the later passes run over them alone.
+// rank-th smallest descending key (~order_key(margin), rank 1-based), in
+// three digit passes of 12, 10 and 10 bits.  A 12-bit first digit (sign,
+// exponent and three mantissa bits) splits QB margins finely: at 4096 tokens
+// and 896 experts the bucket holding the target rank keeps a few dozen keys,
+// where an 8-bit digit (sign and exponent only) often keeps the whole
+// column.  With the column staged in shared memory, the keys of the first
+// pass's chosen bucket are compacted (when they fit kSelectCand words) and
+// the later passes run over them alone.
+constexpr int kSelectMaxBits = 12;
 struct SelectShared {
-    unsigned hist[256];
-    unsigned wsum[8];
+    unsigned hist[1 << kSelectMaxBits];
+    unsigned wsum[kSelectThreads / 32];
     int digit, rank, cnt, ncand;
     uint32_t next;
     float red[kSelectThreads / 32];
 };
 
-// One digit pass over src[0..count) (keys matching prefix under mask):
-// picks the digit holding rank; leaves the digit, the rank within it and the
-// bucket's size in sh.
-// kFromCol: keys come from the margin column (and are stored to stage[] when
-// stage is set), else from src[] in shared memory.
-template <bool kFromCol>
+// One digit pass over src[0..count) (keys matching prefix under mask): the
+// BITS-wide digit at `shift` that holds rank; leaves the digit, the rank
+// within it and the bucket's size in sh.  kFromCol: keys come from the
+// margin column (and are stored to stage[] when stage is set), else from
+// src[] in shared memory.
+template <bool kFromCol, int BITS>
 QB_DEV void radix_pass(const uint32_t* src, const float* col, uint32_t* stage, int count, uint32_t prefix,
                        uint32_t mask, int shift, int rank, SelectShared& sh) {
+    constexpr int kBins = 1 << BITS;
+    constexpr int kPer = kBins / kSelectThreads;   // bins per thread in the scan
+    static_assert(kPer >= 1 && kBins % kSelectThreads == 0, "bins per thread");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < 256; i += blockDim.x) sh.hist[i] = 0;
+    for (int i = tid; i < kBins; i += kSelectThreads) sh.hist[i] = 0;
     __syncthreads();
-    for (int base = 0; base < count; base += blockDim.x) {
+    for (int base = 0; base < count; base += kSelectThreads) {
         const int i = base + tid;
         uint32_t key = 0;
         bool pred = false;
@@ -338,33 +348,40 @@ QB_DEV void radix_pass(const uint32_t* src, const float* col, uint32_t* stage, i
         }
         const unsigned active = __ballot_sync(0xffffffffu, pred);
         if (pred) {
-            const unsigned digit = (key >> shift) & 0xFFu;
+            const unsigned digit = (key >> shift) & (unsigned)(kBins - 1);
             const unsigned peers = __match_any_sync(active, digit);
             if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (unsigned)__popc(peers));
         }
     }
     __syncthreads();
-    // inclusive scan of the 256 bins by warps 0..7 (one bin per thread)
-    if (warp < 8) {
-        const int bin = tid;
-        const unsigned c = sh.hist[bin];
-        unsigned incl = c;
+    // each thread scans kPer consecutive bins; warp and block prefixes on top
+    unsigned c[kPer];
+    unsigned tot = 0;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (lane == 31) sh.wsum[warp] = incl;
-        __syncwarp();
-        asm volatile("bar.sync 1, 256;");
-        unsigned before = 0;
-        for (int w = 0; w < warp; ++w) before += sh.wsum[w];
-        incl += before;
-        const unsigned excl = incl - c;
-        if ((int)excl < rank && rank <= (int)incl) {
-            sh.digit = bin;
-            sh.rank = rank - (int)excl;
-            sh.cnt = (int)c;
+    for (int q = 0; q < kPer; ++q) {
+        c[q] = sh.hist[tid * kPer + q];
+        tot += c[q];
+    }
+    unsigned incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) sh.wsum[warp] = incl;
+    __syncthreads();
+    unsigned before = 0;
+    for (int w = 0; w < warp; ++w) before += sh.wsum[w];
+    unsigned excl = before + incl - tot;
+    if ((int)excl < rank && rank <= (int)(excl + tot)) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            if ((int)excl < rank && rank <= (int)(excl + c[q])) {
+                sh.digit = tid * kPer + q;
+                sh.rank = rank - (int)excl;
+                sh.cnt = (int)c[q];
+            }
+            excl += c[q];
         }
     }
     __syncthreads();
@@ -377,8 +394,8 @@ template <bool kSmem>
 QB_DEV uint32_t radix_select(uint32_t* keys, uint32_t* cand, const float* col, int T, int rank,
                              SelectShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31;
-    radix_pass<true>(nullptr, col, kSmem ? keys : nullptr, T, 0u, 0u, 24, rank, sh);
-    uint32_t prefix = (uint32_t)sh.digit << 24, mask = 0xFF000000u;
+    radix_pass<true, 12>(nullptr, col, kSmem ? keys : nullptr, T, 0u, 0u, 20, rank, sh);
+    uint32_t prefix = (uint32_t)sh.digit << 20, mask = 0xFFF00000u;
     rank = sh.rank;
     const uint32_t* src = keys;
     int count = T;
@@ -399,11 +416,11 @@ QB_DEV uint32_t radix_select(uint32_t* keys, uint32_t* cand, const float* col, i
         src = cand;
         count = sh.ncand;
     }
-    for (int shift = 16; shift >= 0; shift -= 8) {
-        if (kSmem) radix_pass<false>(src, col, nullptr, count, prefix, mask, shift, rank, sh);
-        else radix_pass<true>(nullptr, col, nullptr, count, prefix, mask, shift, rank, sh);
+    for (int shift = 10; shift >= 0; shift -= 10) {
+        if (kSmem) radix_pass<false, 10>(src, col, nullptr, count, prefix, mask, shift, rank, sh);
+        else radix_pass<true, 10>(nullptr, col, nullptr, count, prefix, mask, shift, rank, sh);
         prefix |= (uint32_t)sh.digit << shift;
-        mask |= 0xFFu << shift;
+        mask |= 0x3FFu << shift;
         rank = sh.rank;
         __syncthreads();
     }
@@ -484,6 +501,8 @@ k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* _
     extern __shared__ uint32_t keys[];   // [T] keys, then [min(T, kSelectCand)] candidates
     __shared__ SelectShared sh;
     const int j = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const float b = coordinate_bias<kSmem>(T, target_load(T, n, k, j), margins + (size_t)j * T, keys, sh);
     if (threadIdx.x == 0) bias_raw[j] = b;
 }
@@ -498,6 +517,8 @@ k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, BiasArg ba, in
     __shared__ float sb[QBMOE_MAX_EXPERTS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int j = threadIdx.x; j < n; j += blockDim.x) cnt[j] = 0;
+    pdl_wait();
+    pdl_trigger();
     const int blk_tokens = kTopkWarps * tpw;
     const int t0 = blockIdx.x * blk_tokens + warp * tpw;
     // the first token's row is requested before the biases are staged
@@ -563,6 +584,8 @@ k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, BiasArg ba, in
 __global__ void k_block_scan(int nblk, int n, int* __restrict__ blk_cnt, int32_t* __restrict__ loads) {
     const int lane = threadIdx.x & 31;
     const int j = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_trigger();
     if (j >= n) return;
     int* row = blk_cnt + (size_t)j * nblk;
     int running = 0;
@@ -780,20 +803,33 @@ int dispatch_npl(int npl, Args... args) {
     }
 }
 
+// Kernel attributes are set once per device (route_init_attributes) to the
+// largest size any call uses, never per call: a per-call set could lower the
+// limit between another host thread's set and its launch.
+template <int NPL>
+struct TokenPassAttr {
+    static int run() {
+        const int smem = QBMOE_MAX_EXPERTS * (kTokPassTokens + 1) * (int)sizeof(float);
+        for (auto kern : {k_token_pass<NPL, true>, k_token_pass<NPL, false>}) {
+            // the largest shared-memory carveout lets several tiles share an SM
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+                return QBMOE_ECUDA;
+        }
+        return QBMOE_OK;
+    }
+};
+
 template <int NPL>
 struct TokenPassLaunch {
     static int run(int T, int n, int k, const float* logits, float* scores, BiasArg ba, float* margins,
                    cudaStream_t st) {
         const size_t smem = (size_t)n * (kTokPassTokens + 1) * sizeof(float);
         auto kern = logits ? k_token_pass<NPL, true> : k_token_pass<NPL, false>;
-        // the largest shared-memory carveout lets several tiles share an SM
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-            return QBMOE_ECUDA;
         const int grid = (T + kTokPassTokens - 1) / kTokPassTokens;
-        kern<<<grid, kTokPassWarps * 32, smem, st>>>(T, n, k, logits, scores, ba, margins);
-        return qbh::cuda_err(cudaGetLastError());
+        return qbh::launch_pdl(kern, dim3(grid), dim3(kTokPassWarps * 32), smem, st, T, n, k, logits, scores, ba,
+                               margins);
     }
 };
 
@@ -803,8 +839,8 @@ struct TopkLaunch {
                    int* blk_cnt, cudaStream_t st) {
         const size_t smem = (size_t)n * sizeof(int);
         const int grid = (T + kTopkWarps * tpw - 1) / (kTopkWarps * tpw);
-        k_topk<NPL><<<grid, kTopkWarps * 32, smem, st>>>(T, n, k, tpw, s, ba, idx, w, blk_cnt);
-        return qbh::cuda_err(cudaGetLastError());
+        return qbh::launch_pdl(k_topk<NPL>, dim3(grid), dim3(kTopkWarps * 32), smem, st, T, n, k, tpw, s, ba, idx, w,
+                               blk_cnt);
     }
 };
 
@@ -813,14 +849,191 @@ size_t select_smem_bytes(int T) { return (size_t)(T + std::min(T, kSelectCand)) 
 int launch_select(int T, int n, int k, const float* margins, float* bias_raw, cudaStream_t st) {
     if (T <= kSelectSmemMaxT) {
         const size_t smem = select_smem_bytes(T);
-        if (cudaFuncSetAttribute(k_expert_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)std::max<size_t>(smem, 1)) != cudaSuccess)
-            return QBMOE_ECUDA;
-        k_expert_select<true><<<n, kSelectThreads, smem, st>>>(T, n, k, margins, bias_raw);
-    } else {
-        k_expert_select<false><<<n, kSelectThreads, 0, st>>>(T, n, k, margins, bias_raw);
+        return qbh::launch_pdl(k_expert_select<true>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
+                               bias_raw);
     }
-    return qbh::cuda_err(cudaGetLastError());
+    return qbh::launch_pdl(k_expert_select<false>, dim3(n), dim3(kSelectThreads), 0, st, T, n, k, margins, bias_raw);
+}
+
+}  // namespace
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// DeepSeek-V3's fixed-step sign rule (the comparator of QB): every expert's
+// bias moves by -gamma when its load exceeds its target and +gamma when it
+// falls short ([K3-width] 延伸解读 "QB vs DeepSeek-V3": SignSGD on the dual
+// that QB minimises exactly).
+__global__ void k_sign_step(int T, int n, int k, const int32_t* __restrict__ loads, float gamma,
+                            float* __restrict__ b) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= n) return;
+    const int r = target_load(T, n, k, j);
+    const int l = loads[j];
+    if (l > r) b[j] = __fsub_rn(b[j], gamma);
+    else if (l < r) b[j] = __fadd_rn(b[j], gamma);
+}
+
+// ---------------------------------------------------------------------------
+// Token-sharded QB: the r_j-th and (r_j+1)-th largest margins of every
+// expert over a batch split into shards that exchange only per-expert digit
+// histograms ([K3-width] Q&A on Quantile Balancing: histogram estimates keep
+// the communication cheap).  Margins are compared through descending order
+// keys (~f32_order_key); each of four passes fixes one 8-bit digit of both
+// order statistics from the histogram of that digit among the keys that
+// match the digits already fixed, summed over the shards.
+struct HistSel {
+    uint32_t prefix[2];   // digits fixed so far of the two tracked keys
+    int rank[2];          // 1-based rank within the keys matching prefix
+    int r;                // target load r_j
+    int T;                // tokens of the whole batch
+    int pad[2];
+};
+static_assert(sizeof(HistSel) == 32, "state layout");
+constexpr int kHistBins = 256;
+constexpr int kHistThreads = 256;
+constexpr int kHistKeysPerThread = 8;
+
+__global__ void k_hist_init(int T, int n, int k, HistSel* __restrict__ st, int* __restrict__ hist) {
+    const long long total = (long long)n * 2 * kHistBins;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x)
+        hist[i] = 0;
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j < n) {
+        const int r = target_load(T, n, k, j);
+        HistSel s;
+        s.prefix[0] = s.prefix[1] = 0u;
+        // r = 0: the largest margin (twice); r >= T: the smallest (twice)
+        s.rank[0] = min(max(r, 1), T);
+        s.rank[1] = (r >= 1 && r <= T - 1) ? r + 1 : s.rank[0];
+        s.r = r;
+        s.T = T;
+        s.pad[0] = s.pad[1] = 0;
+        st[j] = s;
+    }
+}
+
+// One shard's histogram of pass `pass` added into hist [n][2][256]: CTA
+// (chunk, expert), keys counted through warp-aggregated shared-memory atomics.
+__global__ void __launch_bounds__(kHistThreads)
+k_hist_count(int Ts, int pass, const float* __restrict__ margins, const HistSel* __restrict__ st,
+             int* __restrict__ hist) {
+    __shared__ unsigned h[2][kHistBins];
+    const int j = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < 2 * kHistBins; i += blockDim.x) (&h[0][0])[i] = 0u;
+    __syncthreads();
+    const HistSel s = st[j];
+    const int shift = 24 - 8 * pass;
+    const uint32_t hi = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+    const bool same = s.prefix[0] == s.prefix[1];
+    const float* col = margins + (size_t)j * Ts;
+    const int per_cta = kHistThreads * kHistKeysPerThread;
+    const int end = min(Ts, (blockIdx.x + 1) * per_cta);
+    for (int base = blockIdx.x * per_cta; base < end; base += kHistThreads) {
+        const int i = base + tid;
+        uint32_t key = 0u;
+        if (i < end) key = ~f32_order_key(col[i]);
+        const unsigned dg = (key >> shift) & 0xFFu;
+        const bool pa = i < end && (key & hi) == s.prefix[0];
+        const bool pb = i < end && !same && (key & hi) == s.prefix[1];
+        const unsigned ma = __ballot_sync(0xffffffffu, pa);
+        if (pa) {
+            const unsigned peers = __match_any_sync(ma, dg);
+            if (lane == __ffs(peers) - 1) atomicAdd(&h[0][dg], (unsigned)__popc(peers));
+        }
+        const unsigned mb = __ballot_sync(0xffffffffu, pb);
+        if (pb) {
+            const unsigned peers = __match_any_sync(mb, dg);
+            if (lane == __ffs(peers) - 1) atomicAdd(&h[1][dg], (unsigned)__popc(peers));
+        }
+    }
+    __syncthreads();
+    int* out = hist + (size_t)j * 2 * kHistBins;
+    for (int i = tid; i < kHistBins; i += blockDim.x) {
+        const unsigned a = h[0][i];
+        const unsigned b = same ? a : h[1][i];
+        if (a) atomicAdd(out + i, (int)a);
+        if (b) atomicAdd(out + kHistBins + i, (int)b);
+    }
+}
+
+// After the exchange: fix pass `pass`'s digit of both tracked keys of every
+// expert (one warp each) from the summed histogram, then clear it for the
+// next pass.
+__global__ void k_hist_advance(int n, int pass, int* __restrict__ hist, HistSel* __restrict__ st) {
+    const int lane = threadIdx.x & 31;
+    const int j = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (j >= n) return;
+    HistSel s = st[j];
+    const int shift = 24 - 8 * pass;
+    int* row = hist + (size_t)j * 2 * kHistBins;
+    for (int a = 0; a < 2; ++a) {
+        int v[8];
+        int tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = row[a * kHistBins + lane * 8 + i];
+            tot += v[i];
+        }
+        int incl = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const int rank = s.rank[a];
+        int digit = -1, within = 0;
+        int c = incl - tot;
+        if (c < rank && rank <= incl) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (digit < 0 && c + v[i] >= rank) {
+                    digit = lane * 8 + i;
+                    within = rank - c;
+                }
+                c += v[i];
+            }
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, digit >= 0);
+        const int src = m ? __ffs(m) - 1 : 0;
+        digit = __shfl_sync(0xffffffffu, digit, src);
+        within = __shfl_sync(0xffffffffu, within, src);
+        if (m) {
+            s.prefix[a] |= (uint32_t)digit << shift;
+            s.rank[a] = within;
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 2 * kHistBins / 32; ++i) row[lane + 32 * i] = 0;
+    if (lane == 0) st[j] = s;
+}
+
+// After the last pass: b'_j = -(midpoint of the two order statistics), or the
+// end cases of the coordinate step, then the common offset (one CTA).
+__global__ void __launch_bounds__(1024) k_hist_bias(int n, const HistSel* __restrict__ st, float* __restrict__ bias) {
+    __shared__ float raw[QBMOE_MAX_EXPERTS];
+    __shared__ float s_off;
+    const int j = threadIdx.x;
+    if (j < n) {
+        const HistSel s = st[j];
+        const float Ma = f32_from_order_key(~s.prefix[0]);
+        const float Mb = f32_from_order_key(~s.prefix[1]);
+        float q;
+        if (s.r <= 0) q = __fadd_rn(Ma, 1.0f);
+        else if (s.r >= s.T) q = __fsub_rn(Ma, 1.0f);
+        else q = __fmul_rn(__fadd_rn(Ma, Mb), 0.5f);
+        raw[j] = -q;
+    }
+    __syncthreads();
+    if (j < 32) {
+        const float c = common_offset_warp(raw, n, j);
+        if (j == 0) s_off = c;
+    }
+    __syncthreads();
+    if (j < n) bias[j] = __fsub_rn(raw[j], s_off);
 }
 
 }  // namespace
@@ -896,9 +1109,21 @@ int launch_loads_from_counts(int T, int n, int tpw, const int* blk_cnt, int32_t*
                              int* nl) {
     const int nblk = (T + kTopkWarps * tpw - 1) / (kTopkWarps * tpw);
     const int warps = 8;
-    k_block_scan<<<(n + warps - 1) / warps, warps * 32, 0, s>>>(nblk, n, const_cast<int*>(blk_cnt), loads);
     if (nl) ++*nl;
-    return cuda_err(cudaGetLastError());
+    return launch_pdl(k_block_scan, dim3((n + warps - 1) / warps), dim3(warps * 32), 0, s, nblk, n,
+                      const_cast<int*>(blk_cnt), loads);
+}
+
+int route_init_attributes() {
+    int rc;
+    for (int npl : {1, 2, 4, 8, 16, 28, 32})
+        if ((rc = dispatch_npl<TokenPassAttr>(npl))) return rc;
+    const int sel = (int)select_smem_bytes(kSelectSmemMaxT);
+    if (cudaFuncSetAttribute(k_expert_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_gs_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel) != cudaSuccess)
+        return QBMOE_ECUDA;
+    return QBMOE_OK;
 }
 
 }  // namespace qbh
@@ -915,8 +1140,6 @@ extern "C" size_t qbmoe_route_workspace_bytes(int T, int n, int k) {
 
 extern "C" int qbmoe_route_last_launch_count(void) { return g_route_launches; }
 
-int qbmoe_check_device_arch();   // api.cu
-
 extern "C" int moe_route_qb(int T, int n, int k, int qb_sweeps, const float* logits, const float* bias_in,
                             float* bias_out, float* scores, int32_t* topk_idx, float* topk_w, int32_t* loads,
                             void* workspace, size_t workspace_bytes, qbmoe_stream_t stream) {
@@ -928,7 +1151,7 @@ extern "C" int moe_route_qb(int T, int n, int k, int qb_sweeps, const float* log
         if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QBMOE_EINVAL;
     if (workspace_bytes < qbmoe_route_workspace_bytes(T, n, k)) return QBMOE_EWORKSPACE;
-    int rc = qbmoe_check_device_arch();
+    int rc = qbh::device_init();
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     qbh::RouteBuffers rb;
@@ -944,22 +1167,14 @@ extern "C" int moe_route_qb(int T, int n, int k, int qb_sweeps, const float* log
 // ---------------------------------------------------------------------------
 // C ABI: moe_route_qb_gs (cyclic coordinate-descent QB)
 // ---------------------------------------------------------------------------
-namespace {
+namespace qbh {
 
-struct GsBuffers {
-    float* lv;     // [T, k+1] top-(k+1) values per token
-    int* li;       // [T, k+1] their experts
-    float* mj;     // [T] margins of the expert being updated
-    float* b;      // [n] current biases
-    int* done;     // balanced flag
-};
-
-size_t gs_ws_layout(int T, int n, int k, qbh::RouteBuffers* rb, GsBuffers* gb, void* base) {
+size_t route_gs_ws_layout(int T, int n, int k, RouteBuffers* rb, GsBuffers* gb, void* base) {
     char* p = static_cast<char*>(base);
-    size_t off = qbh::align_up(qbh::route_ws_layout(T, n, k, rb, base), 256);
+    size_t off = align_up(route_ws_layout(T, n, k, rb, base), 256);
     auto take = [&](size_t bytes) {
         const size_t o = off;
-        off = qbh::align_up(off + bytes, 256);
+        off = align_up(off + bytes, 256);
         return p ? p + o : nullptr;
     };
     char* p_lv = take((size_t)T * (k + 1) * sizeof(float));
@@ -977,11 +1192,61 @@ size_t gs_ws_layout(int T, int n, int k, qbh::RouteBuffers* rb, GsBuffers* gb, v
     return off;
 }
 
-}  // namespace
+// Scores, max_sweeps cyclic sweeps (each followed by the loads under the new
+// biases, for the sweep count and the balance test), then the final biased
+// top-k; blk_cnt is left holding the final top-k's per-block counts (the
+// caller turns them into loads).  `loads` is scratch for the balance test.
+int launch_qb_gs(int T, int n, int k, int max_sweeps, int stop_when_balanced, const float* logits, float* scores,
+                 const float* bias_in, float* bias_out, int32_t* topk_idx, float* topk_w, int32_t* loads,
+                 int32_t* sweeps_done, const RouteBuffers& rb, const GsBuffers& gb, cudaStream_t s, int* nl) {
+    const int npl = npl_for(n);
+    if (npl < 0) return QBMOE_EINVAL;
+    int rc;
+    if ((rc = launch_scores(logits, scores, (long long)T * n, s, nl))) return rc;
+    if (bias_in) {
+        if (cudaMemcpyAsync(gb.b, bias_in, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return QBMOE_ECUDA;
+    } else if (cudaMemsetAsync(gb.b, 0, (size_t)n * sizeof(float), s) != cudaSuccess) {
+        return QBMOE_ECUDA;
+    }
+    if (cudaMemsetAsync(gb.done, 0, sizeof(int), s) != cudaSuccess) return QBMOE_ECUDA;
+    if (sweeps_done && cudaMemsetAsync(sweeps_done, 0, sizeof(int32_t), s) != cudaSuccess) return QBMOE_ECUDA;
+    const bool smem_sel = T <= kSelectSmemMaxT;
+    const size_t sel_smem = smem_sel ? select_smem_bytes(T) : 0;
+    const int tpw = route_tokens_per_warp(T);
+    for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+        if ((rc = dispatch_npl<GsListsLaunch>(npl, T, n, k, (const float*)scores, (const float*)gb.b, gb.lv, gb.li,
+                                              (const int*)gb.done, s)))
+            return rc;
+        for (int j = 0; j < n; ++j) {
+            if ((rc = dispatch_npl<GsTokenLaunch>(npl, T, n, k, j, j - 1, (const float*)scores, (const float*)gb.b,
+                                                  gb.lv, gb.li, gb.mj, (const int*)gb.done, s)))
+                return rc;
+            if (smem_sel) k_gs_select<true><<<1, kSelectThreads, sel_smem, s>>>(T, n, k, j, gb.mj, gb.b, gb.done);
+            else k_gs_select<false><<<1, kSelectThreads, 0, s>>>(T, n, k, j, gb.mj, gb.b, gb.done);
+            if ((rc = cuda_err(cudaGetLastError()))) return rc;
+        }
+        k_gs_offset<<<1, 32, 0, s>>>(n, gb.b, gb.done);
+        if ((rc = cuda_err(cudaGetLastError()))) return rc;
+        if (nl) *nl += 2 * n + 2;
+        // loads under the new biases, for the sweep count and the balance test
+        if ((rc = launch_qb_and_topk(T, n, k, 0, nullptr, scores, gb.b, nullptr, topk_idx, topk_w, rb.blk_cnt, rb, s,
+                                     nl)))
+            return rc;
+        if ((rc = launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, nl))) return rc;
+        k_gs_check<<<1, 1024, 0, s>>>(T, n, k, loads, gb.done, sweeps_done, sweep, stop_when_balanced);
+        if ((rc = cuda_err(cudaGetLastError()))) return rc;
+        if (nl) ++*nl;
+    }
+    // final routing with the final biases
+    return launch_qb_and_topk(T, n, k, 0, nullptr, scores, gb.b, bias_out, topk_idx, topk_w, rb.blk_cnt, rb, s, nl);
+}
+
+}  // namespace qbh
 
 extern "C" size_t qbmoe_route_gs_workspace_bytes(int T, int n, int k) {
     if (T < 1 || n < 2 || k < 1) return 0;
-    return gs_ws_layout(T, n, k, nullptr, nullptr, nullptr);
+    return qbh::route_gs_ws_layout(T, n, k, nullptr, nullptr, nullptr);
 }
 
 extern "C" int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_when_balanced, const float* logits,
@@ -996,54 +1261,161 @@ extern "C" int moe_route_qb_gs(int T, int n, int k, int max_sweeps, int stop_whe
         if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QBMOE_EINVAL;
     if (workspace_bytes < qbmoe_route_gs_workspace_bytes(T, n, k)) return QBMOE_EWORKSPACE;
-    int rc = qbmoe_check_device_arch();
+    int rc = qbh::device_init();
     if (rc) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     qbh::RouteBuffers rb;
-    GsBuffers gb;
-    gs_ws_layout(T, n, k, &rb, &gb, workspace);
-    const int npl = npl_for(n);
-    if (npl < 0) return QBMOE_EINVAL;
+    qbh::GsBuffers gb;
+    qbh::route_gs_ws_layout(T, n, k, &rb, &gb, workspace);
     int nl = 0;
+    rc = qbh::launch_qb_gs(T, n, k, max_sweeps, stop_when_balanced, logits, scores, bias_in, bias_out, topk_idx,
+                           topk_w, loads, sweeps_done, rb, gb, s, &nl);
+    if (!rc) rc = qbh::launch_loads_from_counts(T, n, qbh::route_tokens_per_warp(T), rb.blk_cnt, loads, s, &nl);
+    g_route_launches = nl;
+    return rc;
+}
+
+// ---------------------------------------------------------------------------
+// C ABI: moe_route_signsgd (DeepSeek-V3's sign rule, the comparator of QB)
+// ---------------------------------------------------------------------------
+namespace {
+
+size_t signsgd_ws_layout(int T, int n, int k, qbh::RouteBuffers* rb, float** b, void* base) {
+    size_t off = qbh::align_up(qbh::route_ws_layout(T, n, k, rb, base), 256);
+    if (b && base) *b = reinterpret_cast<float*>(static_cast<char*>(base) + off);
+    return qbh::align_up(off + (size_t)n * sizeof(float), 256);
+}
+
+}  // namespace
+
+extern "C" size_t qbmoe_route_signsgd_workspace_bytes(int T, int n, int k) {
+    if (T < 1 || n < 2 || k < 1) return 0;
+    return signsgd_ws_layout(T, n, k, nullptr, nullptr, nullptr);
+}
+
+extern "C" int moe_route_signsgd(int T, int n, int k, int steps, float gamma, const float* logits,
+                                 const float* bias_in, float* bias_out, float* scores, int32_t* topk_idx,
+                                 float* topk_w, int32_t* loads, void* workspace, size_t workspace_bytes,
+                                 qbmoe_stream_t stream) {
+    if (T < 1 || n < 2 || n > QBMOE_MAX_EXPERTS || k < 1 || k >= n || k > QBMOE_MAX_TOPK || steps < 0)
+        return QBMOE_EINVAL;
+    if (!(gamma > 0.0f) || !(gamma < INFINITY)) return QBMOE_EINVAL;
+    if (!logits || !scores || !topk_idx || !topk_w || !loads || !workspace) return QBMOE_EINVAL;
+    const void* ptrs[] = {logits, bias_in, bias_out, scores, topk_idx, topk_w, loads};
+    for (const void* p : ptrs)
+        if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QBMOE_EINVAL;
+    if (workspace_bytes < qbmoe_route_signsgd_workspace_bytes(T, n, k)) return QBMOE_EWORKSPACE;
+    int rc = qbh::device_init();
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    qbh::RouteBuffers rb;
+    float* b = nullptr;
+    signsgd_ws_layout(T, n, k, &rb, &b, workspace);
+    int nl = 0;
+    const int tpw = qbh::route_tokens_per_warp(T);
     if ((rc = qbh::launch_scores(logits, scores, (long long)T * n, s, &nl))) return rc;
     if (bias_in) {
-        if (cudaMemcpyAsync(gb.b, bias_in, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        if (cudaMemcpyAsync(b, bias_in, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
             return QBMOE_ECUDA;
-    } else if (cudaMemsetAsync(gb.b, 0, (size_t)n * sizeof(float), s) != cudaSuccess) {
+    } else if (cudaMemsetAsync(b, 0, (size_t)n * sizeof(float), s) != cudaSuccess) {
         return QBMOE_ECUDA;
     }
-    if (cudaMemsetAsync(gb.done, 0, sizeof(int), s) != cudaSuccess) return QBMOE_ECUDA;
-    if (sweeps_done && cudaMemsetAsync(sweeps_done, 0, sizeof(int32_t), s) != cudaSuccess) return QBMOE_ECUDA;
-    const bool smem_sel = T <= kSelectSmemMaxT;
-    const size_t sel_smem = smem_sel ? select_smem_bytes(T) : 0;
-    if (smem_sel && cudaFuncSetAttribute(k_gs_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)std::max<size_t>(sel_smem, 1)) != cudaSuccess)
-        return QBMOE_ECUDA;
-    const int tpw = qbh::route_tokens_per_warp(T);
-    for (int sweep = 0; sweep < max_sweeps; ++sweep) {
-        if ((rc = dispatch_npl<GsListsLaunch>(npl, T, n, k, (const float*)scores, (const float*)gb.b, gb.lv, gb.li,
-                                              (const int*)gb.done, s)))
+    for (int it = 0; it < steps; ++it) {
+        // loads under the current biases, then one sign step
+        if ((rc = qbh::launch_qb_and_topk(T, n, k, 0, nullptr, scores, b, nullptr, topk_idx, topk_w, rb.blk_cnt, rb,
+                                          s, &nl)) ||
+            (rc = qbh::launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, &nl)))
             return rc;
-        for (int j = 0; j < n; ++j) {
-            if ((rc = dispatch_npl<GsTokenLaunch>(npl, T, n, k, j, j - 1, (const float*)scores, (const float*)gb.b,
-                                                  gb.lv, gb.li, gb.mj, (const int*)gb.done, s)))
-                return rc;
-            if (smem_sel) k_gs_select<true><<<1, kSelectThreads, sel_smem, s>>>(T, n, k, j, gb.mj, gb.b, gb.done);
-            else k_gs_select<false><<<1, kSelectThreads, 0, s>>>(T, n, k, j, gb.mj, gb.b, gb.done);
-            if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
-        }
-        k_gs_offset<<<1, 32, 0, s>>>(n, gb.b, gb.done);
+        k_sign_step<<<(n + 255) / 256, 256, 0, s>>>(T, n, k, loads, gamma, b);
         if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
-        // loads under the new biases, for the sweep count and the balance test
-        if ((rc = qbh::launch_qb_and_topk(T, n, k, 0, nullptr, scores, gb.b, nullptr, topk_idx, topk_w, rb.blk_cnt, rb, s,
-                                          &nl)))
-            return rc;
-        if ((rc = qbh::launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, &nl))) return rc;
-        k_gs_check<<<1, 1024, 0, s>>>(T, n, k, loads, gb.done, sweeps_done, sweep, stop_when_balanced);
-        if ((rc = qbh::cuda_err(cudaGetLastError()))) return rc;
+        ++nl;
     }
-    // final routing with the final biases
-    rc = qbh::launch_qb_and_topk(T, n, k, 0, nullptr, scores, gb.b, bias_out, topk_idx, topk_w, rb.blk_cnt, rb, s, &nl);
+    rc = qbh::launch_qb_and_topk(T, n, k, 0, nullptr, scores, b, bias_out, topk_idx, topk_w, rb.blk_cnt, rb, s, &nl);
     if (!rc) rc = qbh::launch_loads_from_counts(T, n, tpw, rb.blk_cnt, loads, s, &nl);
+    g_route_launches = nl;
     return rc;
+}
+
+// ---------------------------------------------------------------------------
+// C ABI: token-sharded QB with a histogram exchange
+// ---------------------------------------------------------------------------
+extern "C" size_t qbmoe_qb_hist_state_bytes(int n) {
+    return n < 2 ? 0 : qbh::align_up((size_t)n * sizeof(HistSel), 256);
+}
+
+extern "C" size_t qbmoe_qb_hist_bytes(int n) { return n < 2 ? 0 : (size_t)n * 2 * kHistBins * sizeof(int); }
+
+extern "C" size_t qbmoe_qb_shard_workspace_bytes(int T_shard, int n, int k) {
+    if (T_shard < 1 || n < 2 || k < 1) return 0;
+    return qbh::align_up((size_t)n * T_shard * sizeof(float), 256);
+}
+
+namespace {
+
+int hist_common_checks(int n, const void* state, const void* hist) {
+    if (n < 2 || n > QBMOE_MAX_EXPERTS || !state || !hist) return QBMOE_EINVAL;
+    if (!qbh::aligned16(state) || !qbh::aligned16(hist)) return QBMOE_EINVAL;
+    return qbh::device_init();
+}
+
+}  // namespace
+
+extern "C" int moe_qb_hist_init(int T_total, int n, int k, void* state, int32_t* hist, qbmoe_stream_t stream) {
+    if (T_total < 1 || k < 1 || k >= n || k > QBMOE_MAX_TOPK) return QBMOE_EINVAL;
+    if ((long long)T_total * k >= (1LL << 31)) return QBMOE_EINVAL;
+    int rc = hist_common_checks(n, state, hist);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    k_hist_init<<<(n * 2 * kHistBins + 255) / 256, 256, 0, s>>>(T_total, n, k, static_cast<HistSel*>(state), hist);
+    return qbh::cuda_err(cudaGetLastError());
+}
+
+extern "C" int moe_qb_shard_margins(int T_shard, int n, int k, const float* logits, const float* bias_in,
+                                    float* scores, void* workspace, size_t workspace_bytes, qbmoe_stream_t stream) {
+    if (T_shard < 1 || n < 2 || n > QBMOE_MAX_EXPERTS || k < 1 || k >= n || k > QBMOE_MAX_TOPK) return QBMOE_EINVAL;
+    if (!logits || !scores || !workspace) return QBMOE_EINVAL;
+    const void* ptrs[] = {logits, bias_in, scores};
+    for (const void* p : ptrs)
+        if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QBMOE_EINVAL;
+    if (workspace_bytes < qbmoe_qb_shard_workspace_bytes(T_shard, n, k)) return QBMOE_EWORKSPACE;
+    int rc = qbh::device_init();
+    if (rc) return rc;
+    const int npl = npl_for(n);
+    if (npl < 0) return QBMOE_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return dispatch_npl<TokenPassLaunch>(npl, T_shard, n, k, logits, scores, BiasArg{bias_in, nullptr, nullptr},
+                                         static_cast<float*>(workspace), s);
+}
+
+extern "C" int moe_qb_shard_hist(int T_shard, int n, int pass, const void* state, const void* workspace,
+                                 int32_t* hist, qbmoe_stream_t stream) {
+    if (T_shard < 1 || pass < 0 || pass >= 4 || !workspace) return QBMOE_EINVAL;
+    int rc = hist_common_checks(n, state, hist);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int per_cta = kHistThreads * kHistKeysPerThread;
+    const dim3 grid((T_shard + per_cta - 1) / per_cta, n);
+    k_hist_count<<<grid, kHistThreads, 0, s>>>(T_shard, pass, static_cast<const float*>(workspace),
+                                               static_cast<const HistSel*>(state), hist);
+    return qbh::cuda_err(cudaGetLastError());
+}
+
+extern "C" int moe_qb_hist_advance(int n, int pass, int32_t* hist, void* state, qbmoe_stream_t stream) {
+    if (pass < 0 || pass >= 4) return QBMOE_EINVAL;
+    int rc = hist_common_checks(n, state, hist);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    k_hist_advance<<<(n + 7) / 8, 256, 0, s>>>(n, pass, hist, static_cast<HistSel*>(state));
+    return qbh::cuda_err(cudaGetLastError());
+}
+
+extern "C" int moe_qb_hist_bias(int n, const void* state, float* bias_out, qbmoe_stream_t stream) {
+    if (!bias_out || !qbh::aligned16(bias_out)) return QBMOE_EINVAL;
+    int rc = hist_common_checks(n, state, state);
+    if (rc) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    k_hist_bias<<<1, 1024, 0, s>>>(n, static_cast<const HistSel*>(state), bias_out);
+    return qbh::cuda_err(cudaGetLastError());
 }

@@ -1,10 +1,9 @@
 // moe_route_qb_noalloc: the QB router with its scratch in a fixed device array.
 //
 // Some callers cannot allocate device memory at the point where they route:
-// code that runs while a stream is being captured into a CUDA graph (where a
-// cudaMalloc is not permitted), engines that plan every buffer up front and
-// forbid allocation on the serving path, and plug-ins that are handed only
-// their inputs and outputs by a host program that owns all memory.  This
+// engines that plan every buffer up front and forbid allocation on the
+// serving path, and plug-ins that are handed only their inputs and outputs
+// by a host program that owns all memory.  This
 // entry point serves them: it takes only inputs and outputs and keeps its
 // scratch (the margin matrix, raw biases, per-block counts) in a file-scope
 // __device__ array of kNoAllocScratchBytes, which every GPU that loads the
@@ -45,8 +44,6 @@ int scratch_for_current_device(void** out) {
 
 }  // namespace
 
-int qbmoe_check_device_arch();   // api.cu
-
 extern "C" size_t qbmoe_route_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
 
 extern "C" int moe_route_qb_noalloc(int T, int n, int k, int qb_sweeps, const float* logits, const float* bias_in,
@@ -60,7 +57,7 @@ extern "C" int moe_route_qb_noalloc(int T, int n, int k, int qb_sweeps, const fl
         if (p && !qbh::aligned16(p)) return QBMOE_EINVAL;
     // Sizes whose scratch does not fit the fixed array are refused.
     if (qbmoe_route_workspace_bytes(T, n, k) > kNoAllocScratchBytes) return QBMOE_EWORKSPACE;
-    int rc = qbmoe_check_device_arch();
+    int rc = qbh::device_init();
     if (rc) return rc;
     void* scratch = nullptr;
     if ((rc = scratch_for_current_device(&scratch))) return rc;

@@ -15,7 +15,7 @@ def lib():
 def test_every_declared_function_is_exported(lib):
     names = Q.declared_functions()
     for must in ("moe_route_qb", "moe_latent_forward", "qbmoe_create", "qbmoe_destroy", "qbmoe_set_weights",
-                 "qbmoe_status", "qbmoe_route_workspace_bytes"):
+                 "qbmoe_pack_weights", "qbmoe_status", "qbmoe_route_workspace_bytes"):
         assert must in names
     for nm in names:
         assert hasattr(lib, nm), nm
@@ -62,7 +62,8 @@ def test_route_rejects_null_misaligned_and_small_workspace(lib):
 
 def _cfg(**kw):
     base = dict(d=256, latent=128, n_experts=32, top_k=4, expert_inter=64, shared_inter=0, situ_beta1=4.0,
-                situ_beta2=25.0, rms_eps=1e-6, act_dtype=Q.QBMOE_F32, expert_wfmt=Q.QBMOE_W_F32, qb_sweeps=1)
+                situ_beta2=25.0, rms_eps=1e-6, act_dtype=Q.QBMOE_F32, expert_wfmt=Q.QBMOE_W_F32, qb_sweeps=1,
+                qb_mode=Q.QBMOE_QB_JACOBI)
     base.update(kw)
     return Q.QbmoeConfig(**base)
 
@@ -72,7 +73,8 @@ def _cfg(**kw):
                                 dict(act_dtype=Q.QBMOE_BF16, expert_wfmt=Q.QBMOE_W_F32),
                                 dict(act_dtype=Q.QBMOE_BF16, expert_wfmt=Q.QBMOE_W_MXFP4, latent=120),
                                 dict(situ_beta1=0.0), dict(qb_sweeps=-1), dict(top_k=40, n_experts=64),
-                                dict(act_dtype=Q.QBMOE_BF16, expert_wfmt=Q.QBMOE_W_BF16, d=260)])
+                                dict(act_dtype=Q.QBMOE_BF16, expert_wfmt=Q.QBMOE_W_BF16, d=260),
+                                dict(qb_mode=2), dict(qb_mode=-1)])
 def test_create_rejects_bad_configs(lib, kw):
     ctx = ctypes.c_void_p()
     cfg = _cfg(**kw)
@@ -94,4 +96,5 @@ def test_null_context_calls(lib):
     assert lib.moe_latent_forward(None, 4, FAKE, None, None, None, FAKE, None, None, None, None, None) == Q.QBMOE_EINVAL
     assert lib.qbmoe_set_weights(None, None) == Q.QBMOE_EINVAL
     assert lib.qbmoe_set_timing(None, 1) == Q.QBMOE_EINVAL
+    assert lib.qbmoe_pack_weights(None, None, None) == Q.QBMOE_EINVAL
 

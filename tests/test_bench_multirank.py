@@ -31,7 +31,7 @@ def _rank_main(rank, world, port, out):
 def test_two_gloo_ranks_agree_on_max_time_and_total_tokens():
     import torch.multiprocessing as mp
     world, port = 2, _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1]

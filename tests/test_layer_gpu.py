@@ -145,6 +145,65 @@ def test_layer_own_router(shape):
     compare_own_router(shape, min_agree=0.95)
 
 
+@pytest.mark.parametrize("shape", [SMALL_BF16.with_(name="gs_bf16", T=150), RAGGED_F32.with_(name="gs_f32", qb_sweeps=2)],
+                         ids=lambda s: s.name)
+def test_layer_gauss_seidel_mode(shape):
+    """qb_mode = QBMOE_QB_GAUSS_SEIDEL: the layer's QB sweeps are cyclic
+    (each expert's step sees the latest biases); routing bit-exact against
+    the oracle's cyclic sweep, outputs within tolerance."""
+    compare_fed(shape, qb_mode="gauss_seidel")
+
+
+@pytest.mark.parametrize("shape", [TC_DECODE_LIKE, TC_MXFP4_DECODE_LIKE], ids=lambda s: s.name)
+def test_packed_weights_give_identical_outputs(shape):
+    """qbmoe_pack_weights copies the weights into the context: the forward
+    gives the same bits as with the caller's tensors, and keeps doing so once
+    the caller's tensors are freed."""
+    from qb_inputs.device import layer_for, upload
+    d = upload(QI.LayerInputs(shape), "cuda:0")
+    x = d.pop("x")
+    a = layer_for(shape)
+    a.set_weights(**d)
+    want = a.forward(x).clone()
+    b = layer_for(shape)
+    b.pack_weights(**d)
+    got1 = b.forward(x).clone()
+    assert b.status() == 0 and a.status() == 0
+    a.close()
+    del d
+    torch.cuda.empty_cache()
+    junk = torch.full((64 << 20,), 7, dtype=torch.uint8, device="cuda")   # reuse the freed memory
+    got2 = b.forward(x)
+    assert b.status() == 0
+    del junk
+    assert torch.equal(got1.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(got2.view(torch.int16), want.view(torch.int16))
+    b.close()
+
+
+def test_pack_weights_rejects_a_nan_scale():
+    """An E8M0 scale byte of 0xFF (NaN) is not a weight scale: packing fails
+    with QBMOE_EINVAL and the context keeps its previous weights."""
+    import quantile_balanced_routing_gb300 as Q
+    from qb_inputs.device import layer_for, upload
+    shape = TC_MXFP4_DECODE_LIKE
+    d = upload(QI.LayerInputs(shape), "cuda:0")
+    x = d.pop("x")
+    lay = layer_for(shape)
+    lay.pack_weights(**d)
+    want = lay.forward(x).clone()
+    bad = dict(d)
+    bad["s_up"] = d["s_up"].clone()
+    bad["s_up"].view(-1)[12345] = 0xFF
+    with pytest.raises(Q.QbmoeError) as e:
+        lay.pack_weights(**bad)
+    assert e.value.code == Q.QBMOE_EINVAL
+    got = lay.forward(x)
+    assert lay.status() == 0
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    lay.close()
+
+
 def test_layer_reuses_context_and_bias_chains():
     """Two forwards in a row through one context; the second starts from the
     first's QB bias (the caller carries it between batches)."""
@@ -199,6 +258,16 @@ def test_forward_rejects_too_many_tokens():
     lay.close()
 
 
+def _full_size_tokens(shape, n_prefill=512):
+    """Tokens whose layer outputs a full-size test compares: every token of
+    a decode batch (256), a seeded subset of 512 tokens of a prefill batch
+    (routing is still checked on every token)."""
+    if shape.T <= 256:
+        return np.arange(shape.T)
+    rng = np.random.default_rng(0)
+    return np.sort(rng.choice(shape.T, n_prefill, replace=False))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("shape", [QI.DECODE, QI.PREFILL, QI.PREFILL_MXFP4, QI.DECODE_MXFP4],
                          ids=lambda s: s.name)
@@ -206,7 +275,22 @@ def test_full_size_workload_sampled_tokens(shape):
     """The full K3-shape workloads (20 GB of bf16 or 5.2 GB of MXFP4 expert
     weights, up to 16384 tokens) in the launch configuration the bench times:
     routing of every token bit-exact against the oracle (fed the oracle's
-    router logits), layer outputs within tolerance on seeded sampled tokens."""
-    rng = np.random.default_rng(0)
-    tokens = np.sort(rng.choice(shape.T, 4, replace=False))
-    compare_fed(shape, tokens=tokens)
+    router logits), layer outputs within tolerance on all 256 decode tokens
+    and on 512 seeded tokens of the 16384-token prefill batches."""
+    err = compare_fed(shape, tokens=_full_size_tokens(shape))
+    assert err.shape[0] == min(shape.T, 512)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("shape", [QI.DECODE, QI.PREFILL], ids=lambda s: s.name)
+def test_full_size_own_router(shape):
+    """The layer's own router at full size: the K = 7168 router sub-GEMM of
+    the fused x-side launch (2-SM tiles at prefill, as the bench runs it)
+    and its logit + offset epilogue.  Scores within 1e-5 of the oracle's
+    fp64 router, the GPU's routing self-consistent, at least 99% of tokens
+    routed identically, and outputs of identically routed tokens within
+    tolerance (32 seeded tokens)."""
+    rng = np.random.default_rng(1)
+    tokens = np.sort(rng.choice(shape.T, 32, replace=False))
+    err, agree = compare_own_router(shape, tokens=tokens, min_agree=0.99)
+    assert agree >= 0.99

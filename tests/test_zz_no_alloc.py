@@ -1,6 +1,6 @@
 """moe_route_qb_noalloc: the router for callers that cannot allocate device
-memory (graph capture, pre-planned serving memory, plug-ins given only their
-inputs and outputs).  Its results must equal moe_route_qb's, bit for bit, on
+memory (serving paths whose memory is planned up front, plug-ins given only
+their inputs and outputs).  Its results must equal moe_route_qb's, bit for bit, on
 consecutive calls that reuse its fixed scratch array.  This file is collected
 last so that a run stopping at the first failure has run every other test."""
 import numpy as np
