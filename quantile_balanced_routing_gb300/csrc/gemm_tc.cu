@@ -402,10 +402,17 @@ __device__ __forceinline__ void mx_decode_word(uint32_t w, const uint32_t (&h)[2
     for (int q = 0; q < 4; ++q) o[q] |= __byte_perm(w, w4, (q << 12) | ((4 + q) << 4)) & 0x80008000u;
 }
 
+// Every mode adds one warp after its others: the MMA waiter (see the MMA
+// issuer below).
 template <int MODE>
-constexpr int threads_of() {
+constexpr int base_threads_of() {
     return MODE == MODE_MX_DECODE ? kThreadsMx : (MODE == MODE_MX_SCALED ? kThreadsMxS : kThreadsBf16);
 }
+template <int MODE>
+constexpr int threads_of() {
+    return base_threads_of<MODE>() + 32;
+}
+constexpr int kHandoffBar = 2;   // named barrier of the MMA warp and its waiter (64 threads)
 constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
 template <int BN, int S, int MODE>
@@ -448,11 +455,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* go_flag = reinterpret_cast<volatile int*>(tmem_slot + 4);   // [2]: per-tile MMA go/stop
     // [16][kStRow] epilogue staging, read and written as float4: 16-byte aligned
-    float* st = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
+    float* st = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 6) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long lim = p.wait_limit > 0 ? p.wait_limit : kDefaultWait;
+    constexpr int kWaitWarp = base_threads_of<MODE>() / 32;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -610,7 +619,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             for (int g = 0; g < 2; ++g)
                 if ((sc_issued >> g) & 1u) tc::mbar_wait<kTestFirst>(&fullS[g], (sc_par >> g) & 1u, kDrainWait);
         }
-    } else if (MX && warp >= kConvFirstWarp) {
+    } else if (MX && warp >= kConvFirstWarp && warp < kConvFirstWarp + kConvWarps) {
         // ------------------------------------------------- MXFP4 converters
         // Two threads per weight row: thread (r, hh) decodes elements
         // 32*hh .. 32*hh+31 of row r of each 128 x 64 block (16 packed bytes,
@@ -679,7 +688,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             if (!ok || stop) break;
         }
         __syncthreads();
-    } else if (MXS && warp >= kSfFirstWarp) {
+    } else if (MXS && warp >= kSfFirstWarp && warp < kSfFirstWarp + kSfWarps) {
         // ------------------------------------------------- weight scales -> TMEM
         // Warp w writes TMEM lane quarter w % 4.  A stage's scale words (four
         // E8M0 bytes per weight row, one per 32-wide K slice) go to its
@@ -732,44 +741,43 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         __syncthreads();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int sa = 0;
-            uint32_t pha = 0;
-            int ab = 0;
-            uint32_t aph = 0;
-            TileWalker<BN> tw;
-            tw.start(p);
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p)) {
-                TileInfo ti;
-                tw.get(p, tile, n_tiles_dense, ti);
-                const uint32_t n_eff = (ti.nrows + 15) & ~15;
-                const uint32_t idesc = tc::idesc_bf16_m128(n_eff);
-                if (!tc::mbar_wait<kTestFirst>(&acce[ab], aph ^ 1u, lim)) {
-                    set_status(p.status, QBMOE_ETIMEOUT);
-                    *abort_flag = 1;
-                    break;
-                }
-                tc::tc_fence_after();
-                const uint32_t d = tbase + ab * kAccCols;
-                // Descriptors step by plain adds: the start-address field holds
-                // address / 16, so a 32-byte K step is +2 and a stage is
-                // +stage_bytes / 16 (addresses stay below 256 KB, inside the
-                // 14-bit field).  At small N the issuing thread, not the tensor
-                // pipe, sets the pace, so the loop keeps its arithmetic minimal.
-                const uint64_t a_desc0 = tc::desc_sw128(tc::smem_u32(a_ring));
-                const uint64_t b_desc0 = tc::desc_sw128(tc::smem_u32(b_ring));
-                uint32_t id_k[4];
+        // Lane 0 issues the MMAs and never touches an mbarrier itself in the
+        // main loop: measured on GB300, an mbarrier wait by the thread that
+        // issues tcgen05.mma stalls its MMA stream (45% of the tensor rate at
+        // N = 160, even when the barrier has long completed), while a named
+        // barrier with a waiter warp that does the mbarrier waits keeps it at
+        // 84% (N = 160) to 100% (N = 256).  So the waiter warp below waits
+        // for "accumulator free" and "stage landed" and releases this warp
+        // through named barrier kHandoffBar; once per tile it also passes the
+        // go/stop decision in go_flag.
+        int sa = 0;
+        int ab = 0;
+        int h = 0;
+        TileWalker<BN> tw;
+        tw.start(p);
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, tw.next(p)) {
+            TileInfo ti;
+            tw.get(p, tile, n_tiles_dense, ti);
+            const uint32_t n_eff = (ti.nrows + 15) & ~15;
+            const uint32_t idesc = tc::idesc_bf16_m128(n_eff);
+            tc::named_bar_sync(kHandoffBar, 64);   // accumulator ab is free (or stop)
+            const bool go = go_flag[h & 1] != 0;
+            ++h;
+            if (!go) break;
+            const uint32_t d = tbase + ab * kAccCols;
+            // Descriptors step by plain adds: the start-address field holds
+            // address / 16, so a 32-byte K step is +2 and a stage is
+            // +stage_bytes / 16 (addresses stay below 256 KB, inside the
+            // 14-bit field).
+            const uint64_t a_desc0 = tc::desc_sw128(tc::smem_u32(a_ring));
+            const uint64_t b_desc0 = tc::desc_sw128(tc::smem_u32(b_ring));
+            uint32_t id_k[4];
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    id_k[kk] = MXS ? tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, kk, 0) : idesc;
-                bool ok = true;
-                for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait<kTestFirst>(&full[sa], pha, lim)) {
-                        set_status(p.status, QBMOE_ETIMEOUT);
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
+            for (int kk = 0; kk < 4; ++kk)
+                id_k[kk] = MXS ? tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, kk, 0) : idesc;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                tc::named_bar_sync(kHandoffBar, 64);   // stage sa has landed
+                if (lane == 0) {
                     tc::tc_fence_after();
                     const uint64_t ad = a_desc0 + (uint64_t)(sa * (kATileBytes >> 4));
                     const uint64_t bd = b_desc0 + (uint64_t)(sa * (kBBytes >> 4));
@@ -786,16 +794,64 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         }
                     }
                     tc::tc_commit(&empty[sa]);
-                    if (++sa == S) { sa = 0; pha ^= 1u; }
                 }
-                if (!ok) break;
-                if (!(p.stall_first_tile && tile == (int)blockIdx.x)) tc::tc_commit(&accf[ab]);
-                ab ^= 1;
-                if (ab == 0) aph ^= 1u;
+                __syncwarp();
+                if (++sa == S) sa = 0;
             }
-            // all MMAs issued by this thread complete before TMEM is freed
+            if (lane == 0 && !(p.stall_first_tile && tile == (int)blockIdx.x)) tc::tc_commit(&accf[ab]);
+            __syncwarp();
+            ab ^= 1;
+        }
+        // all MMAs issued by this thread complete before TMEM is freed
+        if (lane == 0) {
             tc::tc_commit(drain);
             tc::mbar_wait<kTestFirst>(drain, 0, kDefaultWait);
+        }
+        __syncwarp();
+        __syncthreads();
+    } else if (warp == kWaitWarp) {
+        // ------------------------------------------------------------ MMA waiter
+        // Mirrors the issuer's loop: lane 0 waits (bounded) for the tile's
+        // accumulator and for each stage, then the warp meets the issuer at
+        // kHandoffBar.  After an expiry or an abort it stops waiting and only
+        // releases the issuer, whose MMAs then read stale tiles (outputs are
+        // undefined after an expiry), until the next tile boundary stops both.
+        int sa = 0;
+        uint32_t pha = 0;
+        int ab = 0;
+        uint32_t aph = 0;
+        int h = 0;
+        bool dead = false;   // lane 0: stop waiting
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            if (lane == 0) {
+                if (!dead && *abort_flag) dead = true;
+                if (!dead && !tc::mbar_wait<kTestFirst>(&acce[ab], aph ^ 1u, lim)) {
+                    set_status(p.status, QBMOE_ETIMEOUT);
+                    *abort_flag = 1;
+                    dead = true;
+                }
+                go_flag[h & 1] = dead ? 0 : 1;
+            }
+            __syncwarp();
+            tc::named_bar_sync(kHandoffBar, 64);
+            const bool go = go_flag[h & 1] != 0;
+            ++h;
+            if (!go) break;
+            for (int kb = 0; kb < p.nkb; ++kb) {
+                if (lane == 0) {
+                    if (!dead && *abort_flag) dead = true;
+                    if (!dead && !tc::mbar_wait<kTestFirst>(&full[sa], pha, lim)) {
+                        set_status(p.status, QBMOE_ETIMEOUT);
+                        *abort_flag = 1;
+                        dead = true;
+                    }
+                }
+                __syncwarp();
+                tc::named_bar_sync(kHandoffBar, 64);
+                if (++sa == S) { sa = 0; pha ^= 1u; }
+            }
+            ab ^= 1;
+            if (ab == 0) aph ^= 1u;
         }
         __syncwarp();
         __syncthreads();
@@ -854,7 +910,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
 // epilogue drains its own TMEM lanes (weight rows) and arrives on the
 // leader's accumulator-free barrier.
 template <int BN, int S>
-__global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreadsBf16 + 32, 1) k_tc_gemm2(const __grid_constant__ TcParams p) {
     constexpr int kHalf = BN / 2;                            // token rows per CTA per stage
     constexpr int kBBytes = kHalf * kBK * 2;
     constexpr uint32_t kCols = (2 * BN <= 128) ? 128 : 512;  // two accumulators of BN columns
@@ -869,10 +925,12 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
     uint64_t* drain = acce + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* go_flag = reinterpret_cast<volatile int*>(tmem_slot + 4);   // [2]: per-tile MMA go/stop
     // [16][kStRow] epilogue staging, read and written as float4: 16-byte aligned
-    float* st = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
+    float* st = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 6) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWaitWarp = kThreadsBf16 / 32;   // the leader's MMA waiter
     const uint32_t rank = tc::cluster_ctarank();
     const bool leader = rank == 0;
     const long long lim = p.wait_limit > 0 ? p.wait_limit : kDefaultWait;
@@ -970,49 +1028,89 @@ __global__ void __launch_bounds__(kThreadsBf16, 1) k_tc_gemm2(const __grid_const
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0 && leader) {
+        // The leader's lane 0 issues the pair's MMAs; as in the one-CTA
+        // kernel, a waiter warp does its mbarrier waits and releases it
+        // through named barrier kHandoffBar (go/stop once per tile).
+        if (leader) {
             int sa = 0;
-            uint32_t pha = 0;
             int ab = 0;
-            uint32_t aph = 0;
-            for (int tile = cl; tile < n_tiles && !*abort_flag; tile += ncl) {
+            int h = 0;
+            for (int tile = cl; tile < n_tiles; tile += ncl) {
                 TileInfo ti;
                 decode_tile<BN>(p, tile, n_tiles_dense, ti);
                 const uint32_t n_eff = (ti.nrows + 15) & ~15;
                 const uint32_t idesc = tc::idesc_bf16_m256(n_eff);
-                if (!tc::mbar_wait<true>(&acce[ab], aph ^ 1u, lim)) {
-                    set_status(p.status, QBMOE_ETIMEOUT);
-                    *abort_flag = 1;
-                    break;
-                }
-                tc::tc_fence_after();
+                tc::named_bar_sync(kHandoffBar, 64);   // accumulator ab is free (or stop)
+                const bool go = go_flag[h & 1] != 0;
+                ++h;
+                if (!go) break;
                 const uint32_t d = tbase + ab * BN;
-                bool ok = true;
                 for (int kb = 0; kb < p.nkb; ++kb) {
-                    if (!tc::mbar_wait<true>(&full[sa], pha, lim)) {
+                    tc::named_bar_sync(kHandoffBar, 64);   // both CTAs' halves of stage sa have landed
+                    if (lane == 0) {
+                        tc::tc_fence_after();
+                        const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
+                        const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            tc::tc_mma_bf16_pair(d, tc::desc_sw128(a_addr + kk * 32),
+                                                 tc::desc_sw128(b_addr + kk * 32), idesc, (kb | kk) != 0);
+                        }
+                        tc::tc_commit_pair(&empty[sa], 0x3);
+                    }
+                    __syncwarp();
+                    if (++sa == S) sa = 0;
+                }
+                if (lane == 0) tc::tc_commit_pair(&accf[ab], 0x3);
+                __syncwarp();
+                ab ^= 1;
+            }
+            if (lane == 0) {
+                tc::tc_commit_pair(drain, 0x1);
+                tc::mbar_wait<true>(drain, 0, kDefaultWait);
+            }
+        }
+        __syncwarp();
+        __syncthreads();
+    } else if (warp == kWaitWarp) {
+        if (leader) {
+            int sa = 0;
+            uint32_t pha = 0;
+            int ab = 0;
+            uint32_t aph = 0;
+            int h = 0;
+            bool dead = false;
+            for (int tile = cl; tile < n_tiles; tile += ncl) {
+                if (lane == 0) {
+                    if (!dead && *abort_flag) dead = true;
+                    if (!dead && !tc::mbar_wait<true>(&acce[ab], aph ^ 1u, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
-                        ok = false;
-                        break;
+                        dead = true;
                     }
-                    tc::tc_fence_after();
-                    const uint32_t a_addr = tc::smem_u32(a_ring + sa * kATileBytes);
-                    const uint32_t b_addr = tc::smem_u32(b_ring + sa * kBBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        tc::tc_mma_bf16_pair(d, tc::desc_sw128(a_addr + kk * 32), tc::desc_sw128(b_addr + kk * 32),
-                                             idesc, (kb | kk) != 0);
+                    go_flag[h & 1] = dead ? 0 : 1;
+                }
+                __syncwarp();
+                tc::named_bar_sync(kHandoffBar, 64);
+                const bool go = go_flag[h & 1] != 0;
+                ++h;
+                if (!go) break;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (lane == 0) {
+                        if (!dead && *abort_flag) dead = true;
+                        if (!dead && !tc::mbar_wait<true>(&full[sa], pha, lim)) {
+                            set_status(p.status, QBMOE_ETIMEOUT);
+                            *abort_flag = 1;
+                            dead = true;
+                        }
                     }
-                    tc::tc_commit_pair(&empty[sa], 0x3);
+                    __syncwarp();
+                    tc::named_bar_sync(kHandoffBar, 64);
                     if (++sa == S) { sa = 0; pha ^= 1u; }
                 }
-                if (!ok) break;
-                tc::tc_commit_pair(&accf[ab], 0x3);
                 ab ^= 1;
                 if (ab == 0) aph ^= 1u;
             }
-            tc::tc_commit_pair(drain, 0x1);
-            tc::mbar_wait<true>(drain, 0, kDefaultWait);
         }
         __syncwarp();
         __syncthreads();
@@ -1266,7 +1364,7 @@ int pair_occupancy(int num_sms, int* out) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreadsBf16, 1, 1);
+    cfg.blockDim = dim3(kThreadsBf16 + 32, 1, 1);
     cfg.dynamicSmemBytes = smem2_for<BN>();
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -1290,7 +1388,7 @@ int launch_bn2(TcPlan* P, TcParams& prm, int tiles, cudaStream_t s) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreadsBf16, 1, 1);
+    cfg.blockDim = dim3(kThreadsBf16 + 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;

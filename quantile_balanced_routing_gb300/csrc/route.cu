@@ -495,6 +495,132 @@ QB_DEV int target_load(int T, int n, int k, int j) {
     return (int)(total / n) + (j < (int)(total % n) ? 1 : 0);
 }
 
+// Fast path of the coordinate step for 2 <= r <= T - 1 and T <= kSelectThreads
+// * KPT: each thread holds KPT keys of the column in registers (all loads in
+// flight at once), one 12-bit histogram pass locates the bins of ranks r and
+// r + 1, and the keys of those bins (a few dozen on QB margins) are ranked
+// exactly by counting.  Returns false (CTA-uniform) when the bins hold more
+// than kRankCand keys; the caller then runs the general radix select.
+constexpr int kRankCand = 256;
+
+template <int KPT>
+QB_DEV bool select_by_bins(int T, int r, const float* __restrict__ col, uint32_t* keys, uint32_t* cand,
+                           SelectShared& sh, float& q_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kBins = 1 << 12;
+    constexpr int kPer = kBins / kSelectThreads;
+    for (int i = tid; i < kBins; i += kSelectThreads) sh.hist[i] = 0;
+    if (tid == 0) sh.ncand = 0;
+    {
+        float m[KPT];   // every load of the column in flight at once
+#pragma unroll
+        for (int c = 0; c < KPT; ++c) {
+            const int i = tid + kSelectThreads * c;
+            m[c] = i < T ? col[i] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < KPT; ++c) {
+            const int i = tid + kSelectThreads * c;
+            if (i < T) {
+                const uint32_t key = ~f32_order_key(m[c]);
+                keys[i] = key;
+                atomicAdd(&sh.hist[key >> 20], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    // bins of ranks r and r + 1 and the keys before the first of them
+    unsigned cb[kPer];
+    unsigned tot = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        cb[q] = sh.hist[tid * kPer + q];
+        tot += cb[q];
+    }
+    unsigned incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) sh.wsum[warp] = incl;
+    __syncthreads();
+    unsigned excl = incl - tot;
+    for (int w = 0; w < warp; ++w) excl += sh.wsum[w];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        if ((int)excl < r && r <= (int)(excl + cb[q])) {
+            sh.digit = tid * kPer + q;   // bin of rank r
+            sh.rank = (int)excl;         // keys before it
+        }
+        if ((int)excl < r + 1 && r + 1 <= (int)(excl + cb[q])) sh.cnt = tid * kPer + q;   // bin of rank r + 1
+        excl += cb[q];
+    }
+    __syncthreads();
+    const uint32_t bin_a = (uint32_t)sh.digit, bin_b = (uint32_t)sh.cnt;
+    const int before = sh.rank;
+    // gather the keys of bins [bin_a, bin_b]
+#pragma unroll 4
+    for (int c = 0; c < KPT; ++c) {
+        const int i = tid + kSelectThreads * c;
+        const uint32_t key = i < T ? keys[i] : 0xFFFFFFFFu;
+        const uint32_t b = key >> 20;
+        const bool pred = i < T && b >= bin_a && b <= bin_b;
+        const unsigned bal = __ballot_sync(0xffffffffu, pred);
+        int base = 0;
+        if (lane == 0 && bal) base = atomicAdd(&sh.ncand, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int pos = base + __popc(bal & ((1u << lane) - 1u));
+        if (pred && pos < kRankCand) cand[pos] = key;
+    }
+    __syncthreads();
+    const int nc = sh.ncand;
+    if (nc > kRankCand) return false;
+    // rank of each candidate among them: keys below and equal
+    if (tid < nc) {
+        const uint32_t me = cand[tid];
+        int less = 0, eq = 0;
+        for (int i = 0; i < nc; ++i) {
+            const uint32_t o = cand[i];
+            less += o < me ? 1 : 0;
+            eq += o == me ? 1 : 0;
+        }
+        const int lo = before + less + 1, hi = before + less + eq;
+        if (lo <= r && r <= hi) sh.next = me;            // key of rank r
+        if (lo <= r + 1 && r + 1 <= hi) sh.wsum[0] = me;  // key of rank r + 1
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const float Mr = f32_from_order_key(~sh.next);
+        const float Mr1 = f32_from_order_key(~sh.wsum[0]);
+        q_out = -__fmul_rn(__fadd_rn(Mr, Mr1), 0.5f);
+    }
+    return true;
+}
+
+// One CTA per expert: the fast path when it applies, else the general
+// radix select (coordinate_bias) over the column staged in shared memory.
+template <int KPT>
+__global__ void __launch_bounds__(kSelectThreads, KPT <= 16 ? 6 : 2)
+k_expert_select_reg(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw) {
+    extern __shared__ uint32_t keys[];   // [T] keys, then [min(T, kSelectCand)] candidates
+    __shared__ SelectShared sh;
+    const int j = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const int r = target_load(T, n, k, j);
+    const float* col = margins + (size_t)j * T;
+    float b = 0.0f;
+    if (r >= 1 && r <= T - 1 && select_by_bins<KPT>(T, r, col, keys, keys + T, sh, b)) {
+        if (threadIdx.x == 0) bias_raw[j] = b;
+        return;
+    }
+    __syncthreads();
+    b = coordinate_bias<true>(T, r, col, keys, sh);
+    if (threadIdx.x == 0) bias_raw[j] = b;
+}
+
 template <bool kSmem>
 __global__ void __launch_bounds__(kSelectThreads)
 k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw) {
@@ -847,6 +973,19 @@ struct TopkLaunch {
 size_t select_smem_bytes(int T) { return (size_t)(T + std::min(T, kSelectCand)) * sizeof(uint32_t); }
 
 int launch_select(int T, int n, int k, const float* margins, float* bias_raw, cudaStream_t st) {
+    if (T <= 16 * kSelectThreads) {
+        const size_t smem = select_smem_bytes(T);
+        if (T <= 4 * kSelectThreads)
+            return qbh::launch_pdl(k_expert_select_reg<4>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
+                                   bias_raw);
+        return qbh::launch_pdl(k_expert_select_reg<16>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
+                               bias_raw);
+    }
+    if (T <= 64 * kSelectThreads) {
+        const size_t smem = select_smem_bytes(T);
+        return qbh::launch_pdl(k_expert_select_reg<64>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
+                               bias_raw);
+    }
     if (T <= kSelectSmemMaxT) {
         const size_t smem = select_smem_bytes(T);
         return qbh::launch_pdl(k_expert_select<true>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
@@ -1119,6 +1258,10 @@ int route_init_attributes() {
     for (int npl : {1, 2, 4, 8, 16, 28, 32})
         if ((rc = dispatch_npl<TokenPassAttr>(npl))) return rc;
     const int sel = (int)select_smem_bytes(kSelectSmemMaxT);
+    for (auto kern : {k_expert_select_reg<4>, k_expert_select_reg<16>, k_expert_select_reg<64>})
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)select_smem_bytes(64 * kSelectThreads)) != cudaSuccess)
+            return QBMOE_ECUDA;
     if (cudaFuncSetAttribute(k_expert_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel) !=
             cudaSuccess ||
         cudaFuncSetAttribute(k_gs_select<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sel) != cudaSuccess)
