@@ -335,6 +335,20 @@ def route_config(shape, args):
             "parallelism": f"replicas x{args.gpus}"}
 
 
+def route_balance(logits, k, qb_loads, T, n):
+    """Max/mean expert load after one QB sweep (the timed routing's loads)
+    and after DeepSeek-V3's fixed-step sign rule (moe_route_signsgd) for a few
+    step sizes and step counts, on the same logits, from the GPU kernels."""
+    import quantile_balanced_routing_gb300 as Q
+    mean = T * k / n
+    out = {"qb_one_sweep": float(qb_loads.max().item()) / mean}
+    for gamma in (0.01, 0.03, 0.1):
+        for steps in (0, 1, 8, 32):
+            loads = Q.route_signsgd(logits, k, steps, gamma)[4]
+            out[f"sign_gamma{gamma}_steps{steps}"] = float(loads.max().item()) / mean
+    return {"max_over_mean_load": out}
+
+
 def cpu_route_baseline(logits, k, gs):
     """The oracle's routing of the same fp32 logits on the host cores: one
     cyclic sweep (about 20 s at 4096 x 896), or Jacobi sweeps repeated for at
@@ -605,6 +619,7 @@ def run_route(args, shape, world, rank, local):
     ms_e2e = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_e) / max(args.steps, 1), world)
     if rank != 0:
         return
+    balance = route_balance(logits, k, loads, T, n) if not gs else None
     cpu = cpu_route_baseline(lg_host.numpy(), k, gs) if world == 1 and not args.no_cpu else None
     pk, src = peaks()
     b_alg = T * n * 4 * 2 + T * k * 8 + n * 8       # logits in, scores out, idx/w out, bias/loads
@@ -622,6 +637,8 @@ def run_route(args, shape, world, rank, local):
                     "h2d_bytes_per_step": logits.numel() * logits.element_size(),
                     "d2h_bytes_per_step": idx.numel() * idx.element_size() + w.numel() * w.element_size()},
             "gpu_launches": launches, "clocks": clocks.summary()}
+    if balance:
+        line["balance"] = balance
     print(json.dumps(line), flush=True)
 
 
