@@ -323,9 +323,10 @@ int qbmoe_destroy(qbmoe_ctx* ctx);
  * ("round" = to act_dtype; accumulation is fp32.  With bf16 activations the
  * tensor-core SiTU epilogues use the hardware tanh approximation, relative
  * error about 2^-11, below the bf16 rounding.  MXFP4 experts run on the
- * block-scaled MMA: each bf16 activation a enters as e4m3(a) + e4m3(16 (a -
- * e4m3(a))) / 16, which is exact for 2^-6 <= |a| <= 448; magnitudes above
- * 448 saturate.)
+ * block-scaled MMA: each block of 32 bf16 activations along K gets an E8M0
+ * scale 2^e, e = floor(log2 max|a|) - 7, and each scaled value c = a 2^-e
+ * (|c| < 256) enters as e4m3(c) + e4m3(16 (c - e4m3(c))) / 16, which is
+ * exact for 2^-6 <= |c| < 256; nothing saturates.)
  *
  * x [T, d] act_dtype device; out [T, d] act_dtype device.
  * logits_in: NULL, or [T, n] fp32 device router logits used instead of the

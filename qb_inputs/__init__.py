@@ -111,6 +111,12 @@ class LayerShape:
     offset_var: float   # variance of the per-expert router offsets
     seed: int = 0
     qb_sweeps: int = 1
+    # Scale of the latent activations: x is drawn with standard deviation
+    # h_scale (so h = x W_down^T grows by it) and the expert gate/up weights
+    # with their usual deviation / h_scale, which leaves the expert's GLU
+    # inputs as they were.  1 for every workload; large values exercise the
+    # block scales of E4M3 token rows.
+    h_scale: float = 1.0
 
     def with_(self, **kw) -> "LayerShape":
         return replace(self, **kw)
@@ -188,12 +194,12 @@ class LayerInputs:
         self.shape = shape
         s = shape
         self.specs = {
-            "x": ((s.T, s.d), 1.0, s.dtype),
+            "x": ((s.T, s.d), float(s.h_scale), s.dtype),
             "w_router": ((s.n, s.d), _sig(s.d), s.dtype),
             "router_offset": ((s.n,), float(np.sqrt(s.offset_var)), "f32"),
             "w_down": ((s.latent, s.d), _sig(s.d), s.dtype),
-            "w_gate": ((s.n, s.m, s.latent), _sig(s.latent), s.wfmt),
-            "w_up": ((s.n, s.m, s.latent), _sig(s.latent), s.wfmt),
+            "w_gate": ((s.n, s.m, s.latent), _sig(s.latent) / float(s.h_scale), s.wfmt),
+            "w_up": ((s.n, s.m, s.latent), _sig(s.latent) / float(s.h_scale), s.wfmt),
             "w_out": ((s.n, s.latent, s.m), _sig(s.m), s.wfmt),
             "gamma": ((s.latent,), 0.1, "f32"),
             "w_proj_up": ((s.d, s.latent), _sig(s.latent), s.dtype),

@@ -125,9 +125,14 @@ size_t layout(const qbmoe_config& c, int T, qbmoe_ctx* x, char* base) {
     char* p_toff2 = take((size_t)(n + 1) * 4);
     char* p_perm = take(routes * 4);
     char* p_rpos = take(routes * 4);
-    char* p_h = take((size_t)T * c.latent * a);
-    char* p_hp = take(routes * c.latent * a);
-    char* p_act = take(routes * c.expert_inter * a);
+    // h, h_perm and act rows: bf16 or fp32, or, for MXFP4 experts on the
+    // block-scaled MMA, E4M3 rows with their block scales (the larger size)
+    const bool mx = c.expert_wfmt == QBMOE_W_MXFP4;
+    const size_t h_row = mx ? (size_t)qbh::mx_row_bytes(c.latent) : c.latent * a;
+    const size_t act_row = mx ? (size_t)qbh::mx_row_bytes(c.expert_inter) : c.expert_inter * a;
+    char* p_h = take((size_t)T * h_row);
+    char* p_hp = take(routes * h_row);
+    char* p_act = take(routes * act_row);
     char* p_e = take(routes * c.latent * a);
     char* p_z = take((size_t)T * (c.latent + c.shared_inter) * a);
     char* p_status = take(256);
@@ -508,8 +513,9 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
         return rc;
 
     if (use_tc) {
-        // h rows are bf16, or E4M3 pairs of the same width for block-scaled experts
-        if ((rc = qbh::launch_scatter_rows(c->h, 2 * L, c->route_pos, T, k, c->h_perm, s, &nl))) return rc;
+        // h rows are bf16, or E4M3 rows with block scales for block-scaled experts
+        const int h_row = qbh::tc_mx_scaled(c->tc) ? (int)qbh::mx_row_bytes(L) : 2 * L;
+        if ((rc = qbh::launch_scatter_rows(c->h, h_row, c->route_pos, T, k, c->h_perm, s, &nl))) return rc;
         clk.mark("expert_gate_up");
         if ((rc = qbh::tc_launch(c->tc, qbh::TC_GATE_UP, s, &nl))) return rc;
         clk.mark("expert_down");

@@ -120,7 +120,9 @@ int tc_init_attributes();      // gemm_tc.cu
 // Route kernels (route.cu)
 struct RouteBuffers {
     float* margins;      // [n, T]
-    float* bias_raw;     // [n]
+    float* bias_raw;     // [n] coordinate biases b' of the last sweep
+    float* bias_fin;     // [n] b' minus the common offset (written by the sweep's last select CTA)
+    unsigned* ticket;    // select CTAs finished (zeroed by the sweep's token pass)
     int* blk_cnt;        // [n, nblk] per-block expert counts (expert-major)
 };
 size_t route_ws_layout(int T, int n, int k, RouteBuffers* rb, void* base);

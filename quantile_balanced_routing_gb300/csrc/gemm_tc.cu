@@ -84,20 +84,43 @@ enum { SUB_STORE = 0, SUB_ROUTER = 1, SUB_SITU = 2 };
 // (kind::mxf8f6f4) with E4M3 tokens.
 enum { MODE_BF16 = 0, MODE_MX_DECODE = 1, MODE_MX_SCALED = 2 };
 
-// Block-scaled MMAs take fp8 tokens, so a bf16 activation a enters as two
-// E4M3 terms, a = hi + lo / 16 with hi = e4m3(a) and lo = e4m3(16 (a - hi));
-// the lo rows are stacked under the hi rows in one MMA and the epilogue
-// combines the two accumulators as hi + lo / 16.  For bf16 a with
-// 2^-6 <= |a| <= 448 both terms are exact (the residual has at most four
-// significant bits), so the product is that of the bf16 activation; smaller
-// magnitudes keep an absolute error below 2^-14 and larger ones saturate.
+// Block-scaled MMAs take fp8 tokens with an E8M0 scale per 32 K elements.
+// A token row's bf16 activations are cut into blocks of 32; block b gets the
+// scale 2^e_b with e_b = floor(log2 max|a|) - 7, so that every scaled value
+// c = a 2^-e_b has |c| < 256, inside E4M3's finite range (448).  c enters as
+// two E4M3 terms, c = hi + lo / 16 with hi = e4m3(c) and lo = e4m3(16 (c -
+// hi)); the lo rows are stacked under the hi rows in one MMA, both with the
+// block's scale, and the epilogue combines the two accumulators as
+// hi + lo / 16.  For 2^-6 <= |c| < 256 both terms are exact (a bf16 residual
+// has at most four significant bits), so the product is that of the bf16
+// activation; smaller values of the block keep an absolute error below
+// 2^(e_b - 14).  Nothing saturates.
 constexpr int kLoShift = 4;
+constexpr int kTokScaleHeadroom = 7;   // e_b = floor(log2 amax) - 7
 __device__ __forceinline__ void e4m3_pair(float a, uint8_t& hi, uint8_t& lo) {
     hi = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
     const float h = __half2float(__half(__nv_cvt_fp8_to_halfraw(hi, __NV_E4M3)));
     lo = __nv_cvt_float_to_fp8(__fmul_rn(__fsub_rn(a, h), float(1 << kLoShift)), __NV_SATFINITE, __NV_E4M3);
 }
-
+// The E8M0 scale of the 32-value block spread over four consecutive lanes
+// (8 values each, every lane of the warp calling): x8 is scaled by 2^-e in
+// place and e + 127 returned (127, i.e. 2^0, for an all-zero block).  The
+// exponent is read from amax's bits: a subnormal amax takes the smallest
+// scale, 2^-127.
+__device__ __forceinline__ uint8_t mx_block_scale(float (&x8)[8]) {
+    float m = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m = fmaxf(m, fabsf(x8[u]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    int e = 0;
+    if (m > 0.f) e = max(((__float_as_int(m) >> 23) & 0xff) - 127 - kTokScaleHeadroom, -127);
+    e = min(e, 126);
+    const float inv = __int_as_float((127 - e) << 23);   // 2^-e, a normal float for -127 <= e <= 126
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x8[u] = __fmul_rn(x8[u], inv);
+    return static_cast<uint8_t>(e + 127);
+}
 struct SubGemm {
     int epi;
     int F;              // output features (rows of W per group)
@@ -118,6 +141,7 @@ struct TcParams {
     // 8-row steps up to 128), so that a token tile is one TMA copy
     CUtensorMap bx[kTokMaps];
     CUtensorMap sc0, sc1;   // MXFP4 weights: E8M0 scales of a0 / a1 (box {16, rows})
+    CUtensorMap bsc;        // block-scaled: the token rows' E8M0 scales (box {16, BN rows})
     SubGemm sub[kMaxSub];
     int n_sub;
     int m_total;
@@ -251,6 +275,24 @@ __device__ __forceinline__ float situ_glu_hw(float g, float u, float b1, float i
     return a * fmaf(0.5f, tanh_hw(0.5f * a), 0.5f) * b;
 }
 
+// Word i of a 16-byte vector (i a compile-time constant after unrolling).
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One lane's 8 scaled activations (features f .. f + 7 of an E4M3 row of F
+// features) as hi and lo bytes; the first lane of a 32-feature block also
+// stores the block's scale byte.
+__device__ __forceinline__ void store_e4m3_block(uint8_t* row, int F, int f, const float (&c8)[8], uint8_t sc) {
+    __align__(8) uint8_t oh[8];
+    __align__(8) uint8_t ol[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) e4m3_pair(c8[u], oh[u], ol[u]);
+    *reinterpret_cast<uint2*>(row + f) = *reinterpret_cast<const uint2*>(oh);
+    *reinterpret_cast<uint2*>(row + F + f) = *reinterpret_cast<const uint2*>(ol);
+    if ((f & 31) == 0) row[2 * F + f / 32] = sc;
+}
+
 // lo_col > 0 (block-scaled, stacked token planes): the accumulator holds
 // W * hi in columns [0, n) and W * lo in [lo_col, lo_col + n); the result is
 // hi + lo * 2^-kLoShift.
@@ -283,27 +325,28 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
                 const int item = et + 128 * it;
                 const int j = item >> 4, fg = item & 15;
                 const int f = f_base + fg * 8;
-                if (j < tok_left && f < sg.F) {
+                const bool ok = j < tok_left && f < sg.F;
+                if (sg.out_e4m3) {
+                    // E4M3 row: hi plane, lo plane, block scales.  Four consecutive
+                    // lanes hold one token's 32-feature block (F % 32 == 0, so they
+                    // agree on ok); rows past the tile's end are read but not stored.
+                    const float4 a = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8);
+                    const float4 b = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8 + 4);
+                    float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x8[u] = __bfloat162float(__float2bfloat16_rn(x8[u]));
+                    const uint8_t sc = mx_block_scale(x8);
+                    if (ok) store_e4m3_block(static_cast<uint8_t*>(sg.out) + (long long)(ti.row0 + c0 + j) * sg.ldo,
+                                             sg.F, f, x8, sc);
+                } else if (ok) {
                     const float4 a = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8);
                     const float4 b = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8 + 4);
                     const float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                    if (sg.out_e4m3) {
-                        // the bf16 value as an E4M3 pair: hi plane, then lo plane F bytes on
-                        __align__(8) uint8_t oh[8];
-                        __align__(8) uint8_t ol[8];
+                    __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            e4m3_pair(__bfloat162float(__float2bfloat16_rn(x8[u])), oh[u], ol[u]);
-                        uint8_t* o8 = static_cast<uint8_t*>(sg.out) + (long long)(ti.row0 + c0 + j) * sg.ldo + f;
-                        *reinterpret_cast<uint2*>(o8) = *reinterpret_cast<const uint2*>(oh);
-                        *reinterpret_cast<uint2*>(o8 + sg.F) = *reinterpret_cast<const uint2*>(ol);
-                    } else {
-                        __align__(16) __nv_bfloat16 o[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(x8[u]);
-                        *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
-                            *reinterpret_cast<const uint4*>(o);
-                    }
+                    for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(x8[u]);
+                    *reinterpret_cast<uint4*>(out + (long long)(ti.row0 + c0 + j) * sg.ldo + f) =
+                        *reinterpret_cast<const uint4*>(o);
                 }
             }
         } else if (sg.epi == SUB_ROUTER) {
@@ -330,7 +373,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
             // SITU: 16 tokens x 8 groups of 8 features, gate rows 0..63, up rows 64..127
             const int j = et >> 3, fg = et & 7;
             const int f = f_base + fg * 8;
-            if (j < tok_left && f < sg.F) {
+            const bool ok = j < tok_left && f < sg.F;
+            // E4M3 output: every lane takes part in the block-scale exchange
+            // (four consecutive lanes hold one 32-feature block)
+            if (ok || sg.out_e4m3) {
                 const float inv_b1 = 1.0f / p.beta1, inv_b2 = 1.0f / p.beta2;
                 const float* row = st + j * kStRow;
                 const float4 g0 = *reinterpret_cast<const float4*>(row + fg * 8);
@@ -342,21 +388,17 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
                 float a[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) a[u] = situ_glu_hw(g8[u], u8[u], p.beta1, inv_b1, p.beta2, inv_b2);
-                const long long off = (long long)(ti.row0 + c0 + j) * sg.ldo + f;
+                const long long r = (long long)(ti.row0 + c0 + j) * sg.ldo;
                 if (sg.out_e4m3) {
-                    // the bf16 activation as an E4M3 pair: hi plane, then lo plane F bytes on
-                    __align__(8) uint8_t oh[8];
-                    __align__(8) uint8_t ol[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) e4m3_pair(__bfloat162float(__float2bfloat16_rn(a[u])), oh[u], ol[u]);
-                    uint8_t* o8 = static_cast<uint8_t*>(sg.out) + off;
-                    *reinterpret_cast<uint2*>(o8) = *reinterpret_cast<const uint2*>(oh);
-                    *reinterpret_cast<uint2*>(o8 + sg.F) = *reinterpret_cast<const uint2*>(ol);
+                    for (int u = 0; u < 8; ++u) a[u] = __bfloat162float(__float2bfloat16_rn(a[u]));
+                    const uint8_t sc = mx_block_scale(a);
+                    if (ok) store_e4m3_block(static_cast<uint8_t*>(sg.out) + r, sg.F, f, a, sc);
                 } else {
                     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(a[u]);
-                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sg.out) + off) =
+                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(sg.out) + r + f) =
                         *reinterpret_cast<const uint4*>(o);
                 }
             }
@@ -429,11 +471,14 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     // SMEM, so one N = 2n MMA is much cheaper than two N = n ones.)
     static_assert(!MXS || 2 * BN <= 256, "stacked token planes need N = 2 BN <= 256");
     constexpr int kAccCols = MXS ? 2 * BN : BN;   // TMEM columns per accumulator
-    // TMEM columns: two accumulators; block-scaled adds the token scales
-    // (8 columns of 2^0) and a 4-column weight-scale slot per stage.
-    constexpr int kSfbCol = 2 * kAccCols, kSfaCol = 2 * kAccCols + 8;
+    // TMEM columns: two accumulators; block-scaled adds, per stage, an
+    // 8-column token-scale slot (N = 2 BN <= 256 rows) and a 4-column
+    // weight-scale slot.
+    constexpr int kSfbCol = 2 * kAccCols, kSfaCol = 2 * kAccCols + 8 * S;
     constexpr uint32_t kCols = MXS ? pow2_cols(kSfaCol + 4 * S) : pow2_cols(2 * BN);
     static_assert(!MXS || kSfaCol + 4 * S <= 512, "TMEM columns");
+    constexpr int kTokScBytes = MXS ? BN * 16 : 0;   // token scales of one scale group (16 per row)
+    constexpr bool kScaleAhead = MXS && BN >= 64;     // scale groups issued one group ahead
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // S stages, each a 16 KB weight tile and a BN-row token tile that share
@@ -445,7 +490,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     uint8_t* b_ring = smem + S * kATileBytes;
     uint8_t* p_ring = b_ring + S * kBBytes;
     uint8_t* sc_ring = p_ring + (MX ? S * kPackBytes : 0);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sc_ring + (MX || MXS ? 2 * kScaleBytes : 0));
+    uint8_t* tsc_ring = sc_ring + (MX || MXS ? 2 * kScaleBytes : 0);   // block-scaled: 2 token-scale slots
+    uint64_t* full = reinterpret_cast<uint64_t*>(tsc_ring + 2 * kTokScBytes);
     uint64_t* empty = full + S;
     uint64_t* fullP = empty + S;                       // MX: packed block landed
     uint64_t* fullS = fullP + (MX ? S : 0);            // MX, MXS: scale group landed
@@ -453,6 +499,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     uint64_t* accf = emptyS + (MX || MXS ? 2 : 0);
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
+    // words after the barriers: [0] TMEM base, [1] abort flag, [2] the
+    // epilogue's per-tile verdict, [4, 5] the MMA issuer's per-tile go/stop
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* go_flag = reinterpret_cast<volatile int*>(tmem_slot + 4);   // [2]: per-tile MMA go/stop
@@ -510,18 +558,27 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         const bool is_a = warp == kProdAWarp || warp == kProdA1Warp;
         const int pair = (warp == kProdAWarp || warp == kProdBWarp) ? 0 : 1;
         uint64_t* fullx = (MX && is_a) ? fullP : full;
-        uint64_t* emptyx = empty;
         uint32_t issued = 0, last_par = 0;
         uint32_t sc_issued = 0, sc_par = 0;
         int gidx = 0;
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
+            // The walker runs one tile ahead: the next tile's bookkeeping loads
+            // are issued while this tile's K blocks go out (and block-scaled
+            // kernels issue the next tile's first scale group from it).
             TileWalker<BN> tw;
             tw.start(p);
-            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x, tw.next(p)) {
-                TileInfo ti;
-                tw.get(p, tile, n_tiles_dense, ti);
+            TileInfo tn;
+            if ((int)blockIdx.x < n_tiles) tw.get(p, blockIdx.x, n_tiles_dense, tn);
+            int gstart = 0;   // block-scaled: scale groups begun by this thread
+            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+                const TileInfo ti = tn;
+                const bool has_next = tile + (int)gridDim.x < n_tiles;
+                if (has_next) {
+                    tw.next(p);
+                    tw.get(p, tile + gridDim.x, n_tiles_dense, tn);
+                }
                 const SubGemm& sg = p.sub[ti.sub];
                 const int n_eff = (ti.nrows + 15) & ~15;
                 for (int kb = 0; kb < p.nkb; ++kb) {
@@ -529,7 +586,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         if (++s == S) { s = 0; ph ^= 1u; }
                         continue;
                     }
-                    if (!tc::mbar_wait<kTestFirst>(&emptyx[s], ph ^ 1u, lim)) {
+                    if (!tc::mbar_wait<kTestFirst>(&empty[s], ph ^ 1u, lim)) {
                         set_status(p.status, QBMOE_ETIMEOUT);
                         *abort_flag = 1;
                         break;
@@ -541,7 +598,47 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         const bool situ = sg.epi == SUB_SITU;
                         const int y = ti.g * sg.F + ti.mt * (situ ? 64 : 128);
                         constexpr int sgrp = MX ? kScaleGroup : kScaleGroupS;
-                        if (kb % sgrp == 0) {
+                        if (MXS && kb % sgrp == 0) {
+                            // Weight and token scales of a group go out one group
+                            // ahead (two slots) on prefill-sized tiles, so that the
+                            // scale writers find a group's scales landed when its
+                            // first stage is due.  (Measured on GB300: 3% faster at
+                            // 112-row tiles, 5-7% slower at 16-row decode tiles,
+                            // which then issue each group with its first stage.)
+                            auto issue_scales = [&](const TileInfo& t, int kbg) -> bool {
+                                const SubGemm& gs = p.sub[t.sub];
+                                const bool gsitu = gs.epi == SUB_SITU;
+                                const int gy = t.g * gs.F + t.mt * (gsitu ? 64 : 128);
+                                const int slot = gidx & 1;
+                                if (!tc::mbar_wait<kTestFirst>(&emptyS[slot], ((gidx >> 1) & 1) ^ 1u, lim)) return false;
+                                uint8_t* SC = sc_ring + slot * kScaleBytes;
+                                tc::mbar_expect_tx(&fullS[slot], kScaleBytes + kTokScBytes);
+                                const int xs = (kbg / sgrp) * 16;
+                                if (gsitu) {
+                                    tc::tma_load_2d(SC, &p.sc0, &fullS[slot], xs, gy);
+                                    tc::tma_load_2d(SC + kScaleBytes / 2, &p.sc1, &fullS[slot], xs, gy);
+                                } else {
+                                    tc::tma_load_2d(SC, &p.sc0, &fullS[slot], xs, gy);
+                                }
+                                tc::tma_load_2d(tsc_ring + slot * kTokScBytes, &p.bsc, &fullS[slot], xs, t.row0);
+                                sc_issued |= 1u << slot;
+                                sc_par = (sc_par & ~(1u << slot)) | (((gidx >> 1) & 1u) << slot);
+                                ++gidx;
+                                return true;
+                            };
+                            bool iss = true;
+                            if (gidx == gstart) iss = issue_scales(ti, kb);   // the thread's first group
+                            if (kScaleAhead && iss && gidx == gstart + 1) {
+                                if (kb + sgrp < p.nkb) iss = issue_scales(ti, kb + sgrp);
+                                else if (has_next) iss = issue_scales(tn, 0);
+                            }
+                            ++gstart;
+                            if (!iss) {
+                                set_status(p.status, QBMOE_ETIMEOUT);
+                                *abort_flag = 1;
+                                break;
+                            }
+                        } else if (MX && kb % sgrp == 0) {
                             const int slot = gidx & 1;
                             if (!tc::mbar_wait<kTestFirst>(&emptyS[slot], ((gidx >> 1) & 1) ^ 1u, lim)) {
                                 set_status(p.status, QBMOE_ETIMEOUT);
@@ -689,51 +786,78 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         }
         __syncthreads();
     } else if (MXS && warp >= kSfFirstWarp && warp < kSfFirstWarp + kSfWarps) {
-        // ------------------------------------------------- weight scales -> TMEM
-        // Warp w writes TMEM lane quarter w % 4.  A stage's scale words (four
-        // E8M0 bytes per weight row, one per 32-wide K slice) go to its
-        // 4-column slot in the layout the block-scaled MMA reads for M = 128:
-        // in every lane quarter, lane i column j holds row i + 32 j.  The
-        // token scales are all 2^0 (the lo plane's 2^-4 is applied in the
-        // epilogue): 8 columns of 0x7F bytes, written once.
+        // ------------------------------------------------- scales -> TMEM
+        // Warp w writes TMEM lane quarter w % 4 (each quarter holds a full
+        // copy).  A stage's scale words (four E8M0 bytes per row, one per
+        // 32-wide K slice) go to its slots in the layout the block-scaled MMA
+        // reads: lane i column j holds row i + 32 j.  Weights: a 4-column slot
+        // for the M = 128 rows.  Tokens: an 8-column slot for the N = 2 n_eff
+        // stacked rows, lo row n_eff + r taking hi row r's scale.  A scale
+        // group (4 stages) holds 16 bytes per row, one word per stage, so each
+        // lane reads its rows' groups once as 16-byte vectors (4 weight rows,
+        // 8 stacked token rows) and releases the group's slot right away.
+        static_assert(!MXS || kScaleGroupS == 4, "one 16-byte vector per row and scale group");
         const int q = warp & 3;
         const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
-        constexpr uint32_t kSf1 = 0x7F7F7F7Fu;
-        tc::tmem_st4(tbase + lanes + kSfbCol, kSf1, kSf1, kSf1, kSf1);
-        tc::tmem_st4(tbase + lanes + kSfbCol + 4, kSf1, kSf1, kSf1, kSf1);
-        tc::tmem_wait_st();
         int s = 0, gidx = 0;
         uint32_t ph = 0;
+        TileWalker<BN> tw;   // one tile ahead, as in the producers
+        tw.start(p);
+        TileInfo tn;
+        if ((int)blockIdx.x < n_tiles) tw.get(p, blockIdx.x, n_tiles_dense, tn);
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const int n_eff = (tn.nrows + 15) & ~15;
+            if (tile + (int)gridDim.x < n_tiles) {
+                tw.next(p);
+                tw.get(p, tile + gridDim.x, n_tiles_dense, tn);
+            }
             bool ok = true;
-            for (int kb = 0; kb < p.nkb; ++kb) {
-                const int slot = gidx & 1;
-                int w = 1;
-                if (lane == 0) {
-                    if (kb % kScaleGroupS == 0) w = tc::mbar_wait<kTestFirst>(&fullS[slot], (gidx >> 1) & 1u, lim);
-                    // the slot is free once the MMAs of the stage's last use completed
-                    if (w) w = tc::mbar_wait<kTestFirst>(&empty[s], ph ^ 1u, lim);
-                    if (!w) {
-                        set_status(p.status, QBMOE_ETIMEOUT);
-                        *abort_flag = 1;
-                    }
-                }
-                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-                tc::tc_fence_after();
-                const uint8_t* SC = sc_ring + slot * kScaleBytes + (kb % kScaleGroupS) * 4;
-                uint32_t v[4];
+            for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += kScaleGroupS) {
+                uint4 wa[4], wt[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint32_t*>(SC + (lane + 32 * j) * 16);
-                tc::tmem_st4(tbase + lanes + kSfaCol + 4 * s, v[0], v[1], v[2], v[3]);
-                tc::tmem_wait_st();
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&full[s]);
-                if (kb % kScaleGroupS == kScaleGroupS - 1 || kb == p.nkb - 1) {
-                    if (lane == 0) tc::mbar_arrive(&emptyS[slot]);
-                    ++gidx;
+                for (int kq = 0; kq < kScaleGroupS; ++kq) {
+                    int w = 1;
+                    if (lane == 0) {
+                        if (kq == 0) w = tc::mbar_wait<kTestFirst>(&fullS[gidx & 1], (gidx >> 1) & 1u, lim);
+                        // the slots are free once the MMAs of the stage's last use completed
+                        if (w) w = tc::mbar_wait<kTestFirst>(&empty[s], ph ^ 1u, lim);
+                        if (!w) {
+                            set_status(p.status, QBMOE_ETIMEOUT);
+                            *abort_flag = 1;
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    if (kq == 0) {
+                        const int slot = gidx & 1;
+                        const uint8_t* SC = sc_ring + slot * kScaleBytes;
+                        const uint8_t* TS = tsc_ring + slot * kTokScBytes;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) wa[j] = *reinterpret_cast<const uint4*>(SC + (lane + 32 * j) * 16);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            // stacked row lane + 32 j: hi row n, lo row n - n_eff, or past the rows
+                            const int n = lane + 32 * j;
+                            const int r = n < n_eff ? n : n - n_eff;
+                            wt[j] = r < n_eff ? *reinterpret_cast<const uint4*>(TS + r * 16)
+                                              : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+                        }
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&emptyS[slot]);   // the group is in registers
+                        ++gidx;
+                    }
+                    tc::tmem_st4(tbase + lanes + kSfaCol + 4 * s, word_of(wa[0], kq), word_of(wa[1], kq),
+                                 word_of(wa[2], kq), word_of(wa[3], kq));
+                    tc::tmem_st4(tbase + lanes + kSfbCol + 8 * s, word_of(wt[0], kq), word_of(wt[1], kq),
+                                 word_of(wt[2], kq), word_of(wt[3], kq));
+                    tc::tmem_st4(tbase + lanes + kSfbCol + 8 * s + 4, word_of(wt[4], kq), word_of(wt[5], kq),
+                                 word_of(wt[6], kq), word_of(wt[7], kq));
+                    tc::tmem_wait_st();
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&full[s]);
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
-                if (++s == S) { s = 0; ph ^= 1u; }
             }
             const int stop = __shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0);
             if (!ok || stop) break;
@@ -774,21 +898,20 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             uint32_t id_k[4];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                id_k[kk] = MXS ? tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, kk, 0) : idesc;
+                id_k[kk] = MXS ? tc::idesc_mx_e2m1_e4m3_m128(2 * n_eff, kk, kk) : idesc;
             for (int kb = 0; kb < p.nkb; ++kb) {
                 tc::named_bar_sync(kHandoffBar, 64);   // stage sa has landed
                 if (lane == 0) {
                     tc::tc_fence_after();
                     const uint64_t ad = a_desc0 + (uint64_t)(sa * (kATileBytes >> 4));
                     const uint64_t bd = b_desc0 + (uint64_t)(sa * (kBBytes >> 4));
-                    const uint32_t sfa = tbase + kSfaCol + 4 * sa;
+                    const uint32_t sfa = tbase + kSfaCol + 4 * sa, sfb = tbase + kSfbCol + 8 * sa;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         if (MXS) {
                             // 32-wide K slice kk (byte kk of the weight scale words)
                             // against the stacked hi and lo rows
-                            tc::tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], sfa, tbase + kSfbCol,
-                                                (kb | kk) != 0);
+                            tc::tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], sfa, sfb, (kb | kk) != 0);
                         } else {
                             tc::tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], (kb | kk) != 0);
                         }
@@ -1202,7 +1325,7 @@ constexpr size_t smem_for() {
     constexpr int S = stages_of<BN, MODE>();
     constexpr bool MX = MODE == MODE_MX_DECODE, MXS = MODE == MODE_MX_SCALED;
     return 1024 + (size_t)S * (kATileBytes + (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
-           (MX || MXS ? 2 * kScaleBytes : 0) + 768 + kStBytes;
+           (MX || MXS ? 2 * kScaleBytes : 0) + (MXS ? 2 * BN * 16 : 0) + 768 + kStBytes;
 }
 
 }  // namespace
@@ -1292,10 +1415,17 @@ bool make_map_e4m3(TcPlan* P, CUtensorMap* m, const void* base, long long rows, 
     return r == CUDA_SUCCESS;
 }
 
+bool make_map_u8(TcPlan* P, CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_x,
+                 int box_rows);
+
+// E4M3 token rows of K activations (mx_row_bytes(K) bytes each): the hi and
+// lo planes as one [rows, 2K] map per tile height, and the block scales
+// [rows, K/32] (box {16, BN rows}).
 bool make_token_maps_e4m3(TcPlan* P, TcParams& prm, const void* x, long long rows, long long K, int BN) {
+    const long long ld = mx_row_bytes(K);
     for (int i = 0; i < kTokMaps && 16 * (i + 1) <= BN; ++i)
-        if (!make_map_e4m3(P, &prm.bx[i], x, rows, K, K, 16 * (i + 1))) return false;
-    return true;
+        if (!make_map_e4m3(P, &prm.bx[i], x, rows, 2 * K, ld, 16 * (i + 1))) return false;
+    return make_map_u8(P, &prm.bsc, static_cast<const uint8_t*>(x) + 2 * K, rows, K / 32, ld, 16, BN);
 }
 
 // Packed E2M1 weights [rows, K] (K codes per row, two per byte, row stride
@@ -1606,10 +1736,10 @@ int tc_prepare_xside(TcPlan* P, int T, const void* x, bool with_router, float* l
         g.epi = SUB_STORE; g.F = c.latent; g.m_tiles = m_tiles_of(c.latent, false, pair); g.m_begin = m;
         g.k_split = 1 << 30; g.out = h; g.ldo = c.latent;
         if (tc_mx_scaled(P)) {
-            // block-scaled experts read h as E4M3 pairs: converted here once
+            // block-scaled experts read h as E4M3 rows: converted here once
             // per token, then copied into expert order as plain bytes
             g.out_e4m3 = 1;
-            g.ldo = 2LL * c.latent;
+            g.ldo = mx_row_bytes(c.latent);
         }
         if (!make_map(P, &prm.a0[ns], P->w.w_down, c.latent, c.d, c.d, 128)) return QBMOE_ECUDA;
         prm.a1[ns] = prm.a0[ns];
@@ -1636,8 +1766,9 @@ static int prep_grouped(TcPlan* P, TcLaunch& L, bool pair, const void* act, long
                         const int* offsets, const int* tile_off, int BN, int mode) {
     TcParams& prm = L.prm;
     if (mode == MODE_MX_SCALED) {
-        // E4M3 pairs: rows of 2K bytes (hi plane, then lo plane)
-        if (!make_token_maps_e4m3(P, prm, act, routes, 2 * K, BN)) return QBMOE_ECUDA;
+        // E4M3 rows: hi plane, lo plane, block scales
+        if (K % 512 != 0) return QBMOE_EINVAL;   // whole scale groups: the scale writers take stage pairs
+        if (!make_token_maps_e4m3(P, prm, act, routes, K, BN)) return QBMOE_ECUDA;
         prm.nkb = (int)(K / kBKS);
     } else {
         if (!make_token_maps(P, prm, act, routes, K, K, pair ? 8 : 16, pair ? BN / 2 : BN)) return QBMOE_ECUDA;
@@ -1680,7 +1811,7 @@ int tc_prepare_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets,
         // [rows, K/32] (box 16 x 64); the output act is E4M3 for the down GEMM
         const long long K = c.latent;
         g.out_e4m3 = 1;
-        g.ldo = 2LL * c.expert_inter;   // act as E4M3 pairs: hi plane, then lo plane
+        g.ldo = mx_row_bytes(c.expert_inter);   // act as E4M3 rows for the down GEMM
         if (!make_map_e2m1(P, &prm.a0[0], P->w.w_gate, wrows, K, 64) ||
             !make_map_e2m1(P, &prm.a1[0], P->w.w_up, wrows, K, 64) ||
             !make_map_u8(P, &prm.sc0, P->w.s_gate, wrows, K / 32, K / 32, 16, 64) ||

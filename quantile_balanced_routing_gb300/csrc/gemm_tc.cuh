@@ -24,10 +24,15 @@ void tc_set_stall(TcPlan* p, int on);
 // a failure to prepare leaves nothing launched.
 enum { TC_XSIDE = 0, TC_GATE_UP = 1, TC_DOWN = 2, TC_UP_SHARED = 3, TC_STAGES = 4 };
 
+// A token row of K activations in E4M3 for the block-scaled MMA: K hi bytes,
+// K lo bytes, then K / 32 E8M0 block scales (K % 512 == 0 keeps every part
+// 16-byte aligned), the row padded to a multiple of 128 bytes so that every
+// 128-byte K block of a row is one aligned line.
+__host__ __device__ constexpr long long mx_row_bytes(long long K) { return (2 * K + K / 32 + 127) / 128 * 128; }
+
 // Router logits (optional; fp32 x W_r^T + o) + latent down-projection +
-// shared gate/up in one launch.  h is bf16 [T, latent], or E4M3 pairs (hi
-// plane, then lo plane: 2 x latent bytes a row) when the expert GEMMs run on
-// the block-scaled MMA.
+// shared gate/up in one launch.  h is bf16 [T, latent], or E4M3 rows of
+// mx_row_bytes(latent) when the expert GEMMs run on the block-scaled MMA.
 int tc_prepare_xside(TcPlan* p, int T, const void* x, bool with_router, float* logits, void* h, void* zcat,
                      long long ldz, int* status);
 // Whether the MXFP4 expert GEMMs run on the block-scaled MMA: their token

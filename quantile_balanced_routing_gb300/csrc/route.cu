@@ -179,6 +179,7 @@ QB_DEV void rank_rounds(const uint32_t (&key)[NPL], int k, int lane, unsigned lo
 // Common offset of raw coordinate biases b' (one warp): the pairwise-tree sum
 // of b' (zero-padded to a power of two P; each lane reduces P/32 contiguous
 // leaves, then the lanes combine by halving strides) divided by n.
+template <bool kFromL2 = false>
 QB_DEV float common_offset_warp(const float* __restrict__ raw, int n, int lane) {
     int P = 1;
     while (P < n) P <<= 1;
@@ -190,7 +191,7 @@ QB_DEV float common_offset_warp(const float* __restrict__ raw, int n, int lane) 
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int j = lane * L + i;
-            a[i] = (i < L && j < n) ? raw[j] : 0.0f;
+            a[i] = (i < L && j < n) ? (kFromL2 ? __ldcg(raw + j) : raw[j]) : 0.0f;
         }
 #pragma unroll
         for (int w = 32; w > 1; w >>= 1)
@@ -242,7 +243,7 @@ QB_DEV void stage_bias(const BiasArg& ba, int n, float* sb) {
 template <int NPL, bool kFromLogits>
 __global__ void __launch_bounds__(kTokPassWarps * 32, 4)
 k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __restrict__ scores, BiasArg ba,
-             float* __restrict__ margins) {
+             float* __restrict__ margins, unsigned* __restrict__ ticket) {
     extern __shared__ float tile[];   // [n][kTokPassTokens + 1]: scores, then margins
     __shared__ unsigned long long rank_buf[kTokPassWarps][32];
     __shared__ float sb[QBMOE_MAX_EXPERTS];
@@ -254,6 +255,7 @@ k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __res
     const int t = t0 + tl;
     pdl_wait();
     pdl_trigger();
+    if (ticket && blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;   // for the select that follows
     // the token's row is requested before the biases are staged
     const float* src = kFromLogits ? logits + (size_t)t * n : scores + (size_t)t * n;
     float x[NPL];
@@ -599,11 +601,36 @@ QB_DEV bool select_by_bins(int T, int r, const float* __restrict__ col, uint32_t
     return true;
 }
 
+// Thread 0 holds expert j's coordinate bias b': store it, and let the last
+// CTA of the launch to finish (ticket) subtract the common offset from all n
+// once, into fin, so that the kernels reading the biases next only copy them.
+QB_DEV void publish_bias(int j, float b, int n, float* __restrict__ raw, float* __restrict__ fin,
+                         unsigned* __restrict__ ticket) {
+    __shared__ int s_last;
+    __shared__ float s_off;
+    if (threadIdx.x == 0) {
+        raw[j] = b;
+        __threadfence();
+        s_last = atomicAdd(ticket, 1u) == (unsigned)(n - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x < 32) {
+        const float c = common_offset_warp<true>(raw, n, threadIdx.x);
+        if (threadIdx.x == 0) s_off = c;
+    }
+    __syncthreads();
+    for (int jj = threadIdx.x; jj < n; jj += blockDim.x) fin[jj] = __fsub_rn(__ldcg(raw + jj), s_off);
+    if (threadIdx.x == 0) *ticket = 0u;
+}
+
 // One CTA per expert: the fast path when it applies, else the general
 // radix select (coordinate_bias) over the column staged in shared memory.
 template <int KPT>
 __global__ void __launch_bounds__(kSelectThreads, KPT <= 16 ? 6 : 2)
-k_expert_select_reg(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw) {
+k_expert_select_reg(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw,
+                    float* __restrict__ bias_fin, unsigned* __restrict__ ticket) {
     extern __shared__ uint32_t keys[];   // [T] keys, then [min(T, kSelectCand)] candidates
     __shared__ SelectShared sh;
     const int j = blockIdx.x;
@@ -612,25 +639,24 @@ k_expert_select_reg(int T, int n, int k, const float* __restrict__ margins, floa
     const int r = target_load(T, n, k, j);
     const float* col = margins + (size_t)j * T;
     float b = 0.0f;
-    if (r >= 1 && r <= T - 1 && select_by_bins<KPT>(T, r, col, keys, keys + T, sh, b)) {
-        if (threadIdx.x == 0) bias_raw[j] = b;
-        return;
+    if (!(r >= 1 && r <= T - 1 && select_by_bins<KPT>(T, r, col, keys, keys + T, sh, b))) {
+        __syncthreads();
+        b = coordinate_bias<true>(T, r, col, keys, sh);
     }
-    __syncthreads();
-    b = coordinate_bias<true>(T, r, col, keys, sh);
-    if (threadIdx.x == 0) bias_raw[j] = b;
+    publish_bias(j, b, n, bias_raw, bias_fin, ticket);
 }
 
 template <bool kSmem>
 __global__ void __launch_bounds__(kSelectThreads)
-k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw) {
+k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* __restrict__ bias_raw,
+                float* __restrict__ bias_fin, unsigned* __restrict__ ticket) {
     extern __shared__ uint32_t keys[];   // [T] keys, then [min(T, kSelectCand)] candidates
     __shared__ SelectShared sh;
     const int j = blockIdx.x;
     pdl_wait();
     pdl_trigger();
     const float b = coordinate_bias<kSmem>(T, target_load(T, n, k, j), margins + (size_t)j * T, keys, sh);
-    if (threadIdx.x == 0) bias_raw[j] = b;
+    publish_bias(j, b, n, bias_raw, bias_fin, ticket);
 }
 
 
@@ -950,12 +976,12 @@ struct TokenPassAttr {
 template <int NPL>
 struct TokenPassLaunch {
     static int run(int T, int n, int k, const float* logits, float* scores, BiasArg ba, float* margins,
-                   cudaStream_t st) {
+                   unsigned* ticket, cudaStream_t st) {
         const size_t smem = (size_t)n * (kTokPassTokens + 1) * sizeof(float);
         auto kern = logits ? k_token_pass<NPL, true> : k_token_pass<NPL, false>;
         const int grid = (T + kTokPassTokens - 1) / kTokPassTokens;
         return qbh::launch_pdl(kern, dim3(grid), dim3(kTokPassWarps * 32), smem, st, T, n, k, logits, scores, ba,
-                               margins);
+                               margins, ticket);
     }
 };
 
@@ -972,26 +998,28 @@ struct TopkLaunch {
 
 size_t select_smem_bytes(int T) { return (size_t)(T + std::min(T, kSelectCand)) * sizeof(uint32_t); }
 
-int launch_select(int T, int n, int k, const float* margins, float* bias_raw, cudaStream_t st) {
+int launch_select(int T, int n, int k, const float* margins, float* bias_raw, float* bias_fin, unsigned* ticket,
+                  cudaStream_t st) {
     if (T <= 16 * kSelectThreads) {
         const size_t smem = select_smem_bytes(T);
         if (T <= 4 * kSelectThreads)
             return qbh::launch_pdl(k_expert_select_reg<4>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
-                                   bias_raw);
+                                   bias_raw, bias_fin, ticket);
         return qbh::launch_pdl(k_expert_select_reg<16>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
-                               bias_raw);
+                               bias_raw, bias_fin, ticket);
     }
     if (T <= 64 * kSelectThreads) {
         const size_t smem = select_smem_bytes(T);
         return qbh::launch_pdl(k_expert_select_reg<64>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
-                               bias_raw);
+                               bias_raw, bias_fin, ticket);
     }
     if (T <= kSelectSmemMaxT) {
         const size_t smem = select_smem_bytes(T);
         return qbh::launch_pdl(k_expert_select<true>, dim3(n), dim3(kSelectThreads), smem, st, T, n, k, margins,
-                               bias_raw);
+                               bias_raw, bias_fin, ticket);
     }
-    return qbh::launch_pdl(k_expert_select<false>, dim3(n), dim3(kSelectThreads), 0, st, T, n, k, margins, bias_raw);
+    return qbh::launch_pdl(k_expert_select<false>, dim3(n), dim3(kSelectThreads), 0, st, T, n, k, margins, bias_raw,
+                           bias_fin, ticket);
 }
 
 }  // namespace
@@ -1199,11 +1227,15 @@ size_t route_ws_layout(int T, int n, int k, RouteBuffers* rb, void* base) {
     };
     const size_t o_m = take((size_t)n * T * sizeof(float));
     const size_t o_raw = take((size_t)n * sizeof(float));
+    const size_t o_fin = take((size_t)n * sizeof(float));
+    const size_t o_tick = take(sizeof(unsigned));
     const size_t o_cnt = take((size_t)nblk * n * sizeof(int));
     if (rb && base) {
         char* p = static_cast<char*>(base);
         rb->margins = reinterpret_cast<float*>(p + o_m);
         rb->bias_raw = reinterpret_cast<float*>(p + o_raw);
+        rb->bias_fin = reinterpret_cast<float*>(p + o_fin);
+        rb->ticket = reinterpret_cast<unsigned*>(p + o_tick);
         rb->blk_cnt = reinterpret_cast<int*>(p + o_cnt);
     }
     return off;
@@ -1230,11 +1262,12 @@ int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* logits, flo
     if (logits && sweeps == 0 && (rc = launch_scores(logits, scores, (long long)T * n, s, nl))) return rc;
     BiasArg ba{bias_in, nullptr, nullptr};
     for (int it = 0; it < sweeps; ++it) {
-        rc = dispatch_npl<TokenPassLaunch>(npl, T, n, k, it == 0 ? logits : nullptr, scores, ba, rb.margins, s);
+        rc = dispatch_npl<TokenPassLaunch>(npl, T, n, k, it == 0 ? logits : nullptr, scores, ba, rb.margins,
+                                           rb.ticket, s);
         if (rc) return rc;
-        rc = launch_select(T, n, k, rb.margins, rb.bias_raw, s);
+        rc = launch_select(T, n, k, rb.margins, rb.bias_raw, rb.bias_fin, rb.ticket, s);
         if (rc) return rc;
-        ba = BiasArg{nullptr, rb.bias_raw, nullptr};
+        ba = BiasArg{rb.bias_fin, nullptr, nullptr};
         if (nl) *nl += 2;
     }
     ba.out = bias_out;
@@ -1529,7 +1562,7 @@ extern "C" int moe_qb_shard_margins(int T_shard, int n, int k, const float* logi
     if (npl < 0) return QBMOE_EINVAL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return dispatch_npl<TokenPassLaunch>(npl, T_shard, n, k, logits, scores, BiasArg{bias_in, nullptr, nullptr},
-                                         static_cast<float*>(workspace), s);
+                                         static_cast<float*>(workspace), (unsigned*)nullptr, s);
 }
 
 extern "C" int moe_qb_shard_hist(int T_shard, int n, int pass, const void* state, const void* workspace,

@@ -81,13 +81,15 @@ def upload_and_run(shape, logits_in=None, layer=None, dev_inputs=None):
     return inp, res, lay
 
 
-def compare_fed(shape, tokens=None, qb_mode="jacobi"):
-    """Both sides route from the same fp32 logits (the oracle's router GEMM):
-    routing must be bit-exact; outputs within the format's tolerance."""
+def compare_fed(shape, tokens=None, qb_mode="jacobi", logits_shape=None):
+    """Both sides route from the same fp32 logits (the oracle's router GEMM,
+    on logits_shape's inputs if given, else on shape's): routing must be
+    bit-exact; outputs within the format's tolerance."""
     from qb_inputs.device import layer_for
     inp = QI.LayerInputs(shape)
     W = O.LayerWeights(inp)
-    logits = O.router_logits(W.dense("x"), W.dense("w_router"), W.dense("router_offset"))
+    Wl = W if logits_shape is None else O.LayerWeights(QI.LayerInputs(logits_shape))
+    logits = O.router_logits(Wl.dense("x"), Wl.dense("w_router"), Wl.dense("router_offset"))
     _, g, lay = upload_and_run(shape, logits_in=logits, layer=layer_for(shape, qb_mode=qb_mode))
     lay.close()
     o = O.layer_forward(inp, tokens=tokens, logits=logits, weights=W, mode=qb_mode)

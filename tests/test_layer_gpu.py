@@ -40,6 +40,18 @@ def test_layer_fed_logits(shape):
     compare_fed(shape)
 
 
+@pytest.mark.parametrize("shape", [TC_MXFP4_DECODE_LIKE, TC_MXFP4_PREFILL_LIKE, TC_MXFP4_ONE_TOKEN],
+                         ids=lambda s: s.name)
+def test_mxfp4_large_latent_activations(shape):
+    """Latent activations a thousand times larger (|h| in the thousands, far
+    past E4M3's largest finite value, 448) with gate/up weights a thousand
+    times smaller, so the experts' GLU inputs are as usual: the per-32 block
+    scales of the E4M3 token rows keep the block-scaled experts within the
+    MXFP4 tolerance.  Routing comes from the unscaled workload's logits."""
+    big = shape.with_(name=shape.name + "_h1000", h_scale=1000.0)
+    compare_fed(big, logits_shape=shape)
+
+
 def test_mxfp4_layers_run_on_tensor_cores():
     from qb_inputs.device import layer_for
     lay = layer_for(TC_MXFP4)
