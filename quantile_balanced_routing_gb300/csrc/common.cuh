@@ -127,11 +127,15 @@ struct RouteBuffers {
 };
 size_t route_ws_layout(int T, int n, int k, RouteBuffers* rb, void* base);
 int route_tokens_per_warp(int T);
-int launch_scores(const float* logits, float* scores, long long count, cudaStream_t s, int* nl);
+// zero (may be NULL): nzero int32 set to 0 by the same launch.
+int launch_scores(const float* logits, float* scores, long long count, cudaStream_t s, int* nl,
+                  int32_t* zero = nullptr, int nzero = 0);
 // logits may be NULL (scores already computed); bias_in may be NULL (zeros).
+// blk_cnt (may be NULL): the top-k's per-CTA expert counts, expert-major;
+// loads (may be NULL): zeroed, then the expert loads accumulated atomically.
 int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* logits, float* scores, const float* bias_in,
                        float* bias_out, int32_t* idx, float* w, int* blk_cnt, const RouteBuffers& rb,
-                       cudaStream_t s, int* nl);
+                       cudaStream_t s, int* nl, int32_t* loads = nullptr);
 int launch_loads_from_counts(int T, int n, int tpw, const int* blk_cnt, int32_t* loads, cudaStream_t s,
                              int* nl);
 

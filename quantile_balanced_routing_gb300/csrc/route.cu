@@ -40,7 +40,10 @@ constexpr int kSelectThreads = 256;
 constexpr int kSelectSmemMaxT = 48 * 1024;   // margins staged in SMEM up to this T
 constexpr int kSelectCand = 1024;            // candidate words after the first digit pass (6 CTAs per SM at T = 4096)
 
-__global__ void k_scores(const float* __restrict__ logits, float* __restrict__ scores, long long count) {
+__global__ void k_scores(const float* __restrict__ logits, float* __restrict__ scores, long long count,
+                         int32_t* __restrict__ zero, int nzero) {
+    if (zero && blockIdx.x == 0)
+        for (int j = threadIdx.x; j < nzero; j += blockDim.x) zero[j] = 0;   // for the top-k's load counts
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (; i < count; i += stride) scores[i] = score_of_logit(logits[i]);
@@ -243,7 +246,7 @@ QB_DEV void stage_bias(const BiasArg& ba, int n, float* sb) {
 template <int NPL, bool kFromLogits>
 __global__ void __launch_bounds__(kTokPassWarps * 32, 4)
 k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __restrict__ scores, BiasArg ba,
-             float* __restrict__ margins, unsigned* __restrict__ ticket) {
+             float* __restrict__ margins, unsigned* __restrict__ ticket, int32_t* __restrict__ loads_zero) {
     extern __shared__ float tile[];   // [n][kTokPassTokens + 1]: scores, then margins
     __shared__ unsigned long long rank_buf[kTokPassWarps][32];
     __shared__ float sb[QBMOE_MAX_EXPERTS];
@@ -256,6 +259,8 @@ k_token_pass(int T, int n, int k, const float* __restrict__ logits, float* __res
     pdl_wait();
     pdl_trigger();
     if (ticket && blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;   // for the select that follows
+    if (loads_zero && blockIdx.x == 0)                                   // for the top-k's load counts
+        for (int j = threadIdx.x; j < n; j += blockDim.x) loads_zero[j] = 0;
     // the token's row is requested before the biases are staged
     const float* src = kFromLogits ? logits + (size_t)t * n : scores + (size_t)t * n;
     float x[NPL];
@@ -663,22 +668,32 @@ k_expert_select(int T, int n, int k, const float* __restrict__ margins, float* _
 template <int NPL>
 __global__ void __launch_bounds__(kTopkWarps * 32, 3)
 k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, BiasArg ba, int32_t* __restrict__ idx,
-       float* __restrict__ w, int* __restrict__ blk_cnt) {
+       float* __restrict__ w, int* __restrict__ blk_cnt, int32_t* __restrict__ loads_acc, int early) {
     extern __shared__ int cnt[];   // [n]
     __shared__ unsigned long long rank_buf[kTopkWarps][32];
     __shared__ float sb[QBMOE_MAX_EXPERTS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int j = threadIdx.x; j < n; j += blockDim.x) cnt[j] = 0;
-    pdl_wait();
-    pdl_trigger();
     const int blk_tokens = kTopkWarps * tpw;
     const int t0 = blockIdx.x * blk_tokens + warp * tpw;
-    // the first token's row is requested before the biases are staged
+    // The first token's row is requested before the biases are staged.  With
+    // `early` set the scores were written two kernels back (by the QB token
+    // pass, which had finished before the preceding select kernel got past
+    // its own dependency wait and let this one start), so the row is read
+    // before this kernel's dependency wait.
     float x[NPL];
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
 #pragma unroll
     for (int c = 0; c < NPL; ++c) {
         const int j = lane + 32 * c;
         x[c] = (t0 < T && j < n) ? s[(size_t)t0 * n + j] : 0.0f;
+    }
+    if (early) {
+        pdl_wait();
+        pdl_trigger();
     }
     stage_bias(ba, n, sb);
     for (int q = 0; q < tpw; ++q) {
@@ -726,7 +741,12 @@ k_topk(int T, int n, int k, int tpw, const float* __restrict__ s, BiasArg ba, in
     }
     __syncthreads();
     // expert-major [n, nblk]: expert j's counts of all blocks are contiguous
-    for (int j = threadIdx.x; j < n; j += blockDim.x) blk_cnt[(size_t)j * gridDim.x + blockIdx.x] = cnt[j];
+    if (blk_cnt)
+        for (int j = threadIdx.x; j < n; j += blockDim.x) blk_cnt[(size_t)j * gridDim.x + blockIdx.x] = cnt[j];
+    // or the loads themselves (integer sums: the same in any order)
+    if (loads_acc)
+        for (int j = threadIdx.x; j < n; j += blockDim.x)
+            if (cnt[j]) atomicAdd(&loads_acc[j], cnt[j]);
 }
 
 // Per expert (one warp each): exclusive prefix over blocks of the expert's
@@ -976,23 +996,23 @@ struct TokenPassAttr {
 template <int NPL>
 struct TokenPassLaunch {
     static int run(int T, int n, int k, const float* logits, float* scores, BiasArg ba, float* margins,
-                   unsigned* ticket, cudaStream_t st) {
+                   unsigned* ticket, int32_t* loads_zero, cudaStream_t st) {
         const size_t smem = (size_t)n * (kTokPassTokens + 1) * sizeof(float);
         auto kern = logits ? k_token_pass<NPL, true> : k_token_pass<NPL, false>;
         const int grid = (T + kTokPassTokens - 1) / kTokPassTokens;
         return qbh::launch_pdl(kern, dim3(grid), dim3(kTokPassWarps * 32), smem, st, T, n, k, logits, scores, ba,
-                               margins, ticket);
+                               margins, ticket, loads_zero);
     }
 };
 
 template <int NPL>
 struct TopkLaunch {
     static int run(int T, int n, int k, int tpw, const float* s, BiasArg ba, int32_t* idx, float* w,
-                   int* blk_cnt, cudaStream_t st) {
+                   int* blk_cnt, int32_t* loads_acc, int early, cudaStream_t st) {
         const size_t smem = (size_t)n * sizeof(int);
         const int grid = (T + kTopkWarps * tpw - 1) / (kTopkWarps * tpw);
         return qbh::launch_pdl(k_topk<NPL>, dim3(grid), dim3(kTopkWarps * 32), smem, st, T, n, k, tpw, s, ba, idx, w,
-                               blk_cnt);
+                               blk_cnt, loads_acc, early);
     }
 };
 
@@ -1241,11 +1261,12 @@ size_t route_ws_layout(int T, int n, int k, RouteBuffers* rb, void* base) {
     return off;
 }
 
-int launch_scores(const float* logits, float* scores, long long count, cudaStream_t s, int* nl) {
+int launch_scores(const float* logits, float* scores, long long count, cudaStream_t s, int* nl, int32_t* zero,
+                  int nzero) {
     const int threads = 256;
     long long blocks = (count + threads - 1) / threads;
     blocks = std::min<long long>(blocks, 152LL * 16);
-    k_scores<<<(int)std::max<long long>(blocks, 1), threads, 0, s>>>(logits, scores, count);
+    k_scores<<<(int)std::max<long long>(blocks, 1), threads, 0, s>>>(logits, scores, count, zero, nzero);
     if (nl) ++*nl;
     return cuda_err(cudaGetLastError());
 }
@@ -1255,15 +1276,17 @@ int launch_scores(const float* logits, float* scores, long long count, cudaStrea
 // token pass when there is a sweep).
 int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* logits, float* scores, const float* bias_in,
                        float* bias_out, int32_t* idx, float* w, int* blk_cnt, const RouteBuffers& rb,
-                       cudaStream_t s, int* nl) {
+                       cudaStream_t s, int* nl, int32_t* loads) {
     const int npl = npl_for(n);
     if (npl < 0) return QBMOE_EINVAL;
     int rc;
-    if (logits && sweeps == 0 && (rc = launch_scores(logits, scores, (long long)T * n, s, nl))) return rc;
+    if (logits && sweeps == 0 && (rc = launch_scores(logits, scores, (long long)T * n, s, nl, loads, n))) return rc;
+    if (loads && sweeps == 0 && !logits && cudaMemsetAsync(loads, 0, (size_t)n * sizeof(int32_t), s) != cudaSuccess)
+        return QBMOE_ECUDA;
     BiasArg ba{bias_in, nullptr, nullptr};
     for (int it = 0; it < sweeps; ++it) {
         rc = dispatch_npl<TokenPassLaunch>(npl, T, n, k, it == 0 ? logits : nullptr, scores, ba, rb.margins,
-                                           rb.ticket, s);
+                                           rb.ticket, loads, s);
         if (rc) return rc;
         rc = launch_select(T, n, k, rb.margins, rb.bias_raw, rb.bias_fin, rb.ticket, s);
         if (rc) return rc;
@@ -1272,7 +1295,7 @@ int launch_qb_and_topk(int T, int n, int k, int sweeps, const float* logits, flo
     }
     ba.out = bias_out;
     const int tpw = route_tokens_per_warp(T);
-    rc = dispatch_npl<TopkLaunch>(npl, T, n, k, tpw, scores, ba, idx, w, blk_cnt, s);
+    rc = dispatch_npl<TopkLaunch>(npl, T, n, k, tpw, scores, ba, idx, w, blk_cnt, loads, sweeps > 0 ? 1 : 0, s);
     if (nl) ++*nl;
     return rc;
 }
@@ -1333,9 +1356,10 @@ extern "C" int moe_route_qb(int T, int n, int k, int qb_sweeps, const float* log
     qbh::RouteBuffers rb;
     qbh::route_ws_layout(T, n, k, &rb, workspace);
     int nl = 0;
-    rc = qbh::launch_qb_and_topk(T, n, k, qb_sweeps, logits, scores, bias_in, bias_out, topk_idx, topk_w,
-                                 rb.blk_cnt, rb, s, &nl);
-    if (!rc) rc = qbh::launch_loads_from_counts(T, n, qbh::route_tokens_per_warp(T), rb.blk_cnt, loads, s, &nl);
+    // the loads come from the top-k's per-CTA counts, added atomically (no
+    // per-block prefix is needed without a dispatch)
+    rc = qbh::launch_qb_and_topk(T, n, k, qb_sweeps, logits, scores, bias_in, bias_out, topk_idx, topk_w, nullptr,
+                                 rb, s, &nl, loads);
     g_route_launches = nl;
     return rc;
 }
@@ -1562,7 +1586,7 @@ extern "C" int moe_qb_shard_margins(int T_shard, int n, int k, const float* logi
     if (npl < 0) return QBMOE_EINVAL;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return dispatch_npl<TokenPassLaunch>(npl, T_shard, n, k, logits, scores, BiasArg{bias_in, nullptr, nullptr},
-                                         static_cast<float*>(workspace), (unsigned*)nullptr, s);
+                                         static_cast<float*>(workspace), (unsigned*)nullptr, (int32_t*)nullptr, s);
 }
 
 extern "C" int moe_qb_shard_hist(int T_shard, int n, int pass, const void* state, const void* workspace,
