@@ -68,7 +68,8 @@ def kernel_source_sha256():
 
 def recorded_traffic(kernel, workload):
     """Per-launch DRAM bytes of `kernel` on `workload` from an ncu summary under
-    profiles/, if it was taken with the current kernel source; else None."""
+    profiles/ (a `traffic: <kernel> <workload> <bytes>` line), if the summary
+    was taken with the current kernel source; else None."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -76,16 +77,17 @@ def recorded_traffic(kernel, workload):
     for name in sorted(os.listdir(pdir)):
         if not name.endswith(".md"):
             continue
-        kv = {}
+        file_sha, found = None, None
         with open(os.path.join(pdir, name)) as f:
             for line in f:
-                if ":" in line and line.split(":", 1)[0].strip() in (
-                        "traffic_bytes_full_launch", "kernel", "workload", "kernel_source_sha256"):
-                    k, v = line.split(":", 1)
-                    kv[k.strip()] = v.strip()
-        if (kv.get("kernel") == kernel and kv.get("workload") == workload
-                and kv.get("kernel_source_sha256") == sha and "traffic_bytes_full_launch" in kv):
-            return int(kv["traffic_bytes_full_launch"])
+                if line.startswith("kernel_source_sha256:"):
+                    file_sha = line.split(":", 1)[1].strip()
+                elif line.startswith("traffic:"):
+                    parts = line.split(":", 1)[1].split()
+                    if len(parts) == 3 and parts[0] == kernel and parts[1] == workload:
+                        found = int(parts[2])
+        if found is not None and file_sha == sha:
+            return found
     return None
 
 
