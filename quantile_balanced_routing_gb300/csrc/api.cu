@@ -471,10 +471,12 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     const int tile_rows = use_tc ? qbh::tc_token_tile(c->tc, T) : qbh::kSimtBM;
     const size_t routes = (size_t)T * k;
     const int max_tiles = (int)((routes + tile_rows - 1) / tile_rows) + n;
+    bool gathered = false;   // expert gate/up gathers h rows by route: no expert-ordered copy
     if (use_tc) {
         if ((rc = qbh::tc_prepare_xside(c->tc, T, x, logits_in == nullptr, c->logits, c->h, c->zcat, ldz,
                                         c->status)) ||
-            (rc = qbh::tc_prepare_gate_up(c->tc, T, c->h_perm, c->offsets, c->tile_off_simt, c->act, c->status)) ||
+            (rc = qbh::tc_prepare_gate_up(c->tc, T, c->h_perm, c->offsets, c->tile_off_simt, c->act, c->status,
+                                          c->h, c->perm, &gathered)) ||
             (rc = qbh::tc_prepare_down(c->tc, T, c->act, c->offsets, c->tile_off_simt, c->e, c->status)) ||
             (rc = qbh::tc_prepare_up_shared(c->tc, T, c->zcat, ldz, out, c->status)))
             return rc;
@@ -515,7 +517,8 @@ extern "C" int moe_latent_forward(qbmoe_ctx* c, int T, const void* x, const floa
     if (use_tc) {
         // h rows are bf16, or E4M3 rows with block scales for block-scaled experts
         const int h_row = qbh::tc_mx_scaled(c->tc) ? (int)qbh::mx_row_bytes(L) : 2 * L;
-        if ((rc = qbh::launch_scatter_rows(c->h, h_row, c->route_pos, T, k, c->h_perm, s, &nl))) return rc;
+        if (!gathered && (rc = qbh::launch_scatter_rows(c->h, h_row, c->route_pos, T, k, c->h_perm, s, &nl)))
+            return rc;
         clk.mark("expert_gate_up");
         if ((rc = qbh::tc_launch(c->tc, qbh::TC_GATE_UP, s, &nl))) return rc;
         clk.mark("expert_down");

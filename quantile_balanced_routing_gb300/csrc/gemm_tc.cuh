@@ -38,8 +38,12 @@ int tc_prepare_xside(TcPlan* p, int T, const void* x, bool with_router, float* l
 // Whether the MXFP4 expert GEMMs run on the block-scaled MMA: their token
 // inputs (h_perm, act) are then E4M3 bytes.
 bool tc_mx_scaled(const TcPlan* p);
+// Expert gate/up.  With h and perm given, bf16 launches on the one-CTA
+// kernel gather their token rows from h [T, latent] through perm (token of
+// each route position) and set *gathered; otherwise they read h_perm, the
+// rows already in expert order.
 int tc_prepare_gate_up(TcPlan* p, int T, const void* h_perm, const int* offsets, const int* tile_off, void* act,
-                       int* status);
+                       int* status, const void* h = nullptr, const int* perm = nullptr, bool* gathered = nullptr);
 int tc_prepare_down(TcPlan* p, int T, const void* act, const int* offsets, const int* tile_off, void* e,
                     int* status);
 int tc_prepare_up_shared(TcPlan* p, int T, const void* zcat, long long ldz, void* out, int* status);

@@ -79,6 +79,27 @@ def test_mxfp4_weights_need_32_byte_alignment():
     lay.close()
 
 
+@pytest.mark.parametrize("shape", [TC_DECODE_LIKE, TC_TWO_TOKENS, QI.DECODE], ids=lambda s: s.name)
+def test_gathered_token_rows_match_the_copied_ones(shape, monkeypatch):
+    """Decode-sized token tiles gather their rows from h by route (TMA
+    four-row gathers); QBMOE_NO_GATHER=1 makes the same launch read an
+    expert-ordered copy instead.  The same bytes reach shared memory, so the
+    outputs are identical."""
+    from qb_inputs.device import layer_for, upload
+    d = upload(QI.LayerInputs(shape), "cuda:0")
+    outs = []
+    for env in ("0", "1"):
+        monkeypatch.setenv("QBMOE_NO_GATHER", env)
+        lay = layer_for(shape)
+        lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
+        o = lay.forward(d["x"])
+        torch.cuda.synchronize()
+        assert lay.status() == 0
+        outs.append(o.clone())
+        lay.close()
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_bf16_layers_run_on_tensor_cores(monkeypatch):
     from qb_inputs.device import layer_for
     lay = layer_for(SMALL_BF16)
