@@ -426,6 +426,15 @@ def expert_gemm_roofline(shape, stages, pk, src, mx_peak=None):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "peak_note": "measured copy bandwidth"}
     roof["frac"] = achieved / peak
+    # both roofs, whichever binds: the bf16 (or block-scaled) tensor peak and
+    # the HBM copy bandwidth, each against the same two launches
+    if shape.wfmt == "mxfp4":
+        t_peak = pk["bf16_tflops"] * mx_peak[0] if mx_peak else 2.0 * pk["bf16_tflops"]
+        t_frac = 2.0 * f / (ms * 1e-3) / 1e12 / t_peak
+    else:
+        t_frac = f / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]
+    roof["tensor_frac"] = t_frac
+    roof["hbm_frac"] = b / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]
     tr = [recorded_traffic(nm, shape.name) for nm in names]
     roof.update({"traffic": sum(tr) / 2 if all(t is not None for t in tr) else None,
                  "kernel": "k_tc_gemm grouped (expert gate/up + expert down launches)",
