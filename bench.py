@@ -444,6 +444,45 @@ def expert_gemm_roofline(shape, stages, pk, src, mx_peak=None):
     return roof
 
 
+def pipelined_e2e(steps, stream, h2d, compute, d2h):
+    """End-to-end steps as a user's pipeline would run them: each step copies
+    its input from pinned host memory (h2d, on one copy stream), computes (on
+    `stream`) and copies its result back (d2h, on another copy stream), with
+    two buffer slots so that step i's copies overlap the neighbouring steps'
+    compute.  Every step's copies are inside the timed region; returns ms per
+    step from the first input copy to the last result copy."""
+    import torch
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    Ev = torch.cuda.Event
+    in_ready = [Ev() for _ in range(steps)]
+    done = [Ev() for _ in range(steps)]
+    out_done = [Ev() for _ in range(steps)]
+    e0, e1 = Ev(enable_timing=True), Ev(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(steps):
+        slot = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(done[i - 2])      # step i-2 has read this input slot
+            h2d(slot)
+            in_ready[i].record(s_in)
+        stream.wait_event(in_ready[i])
+        if i >= 2:
+            stream.wait_event(out_done[i - 2])    # step i-2's result has left this output slot
+        compute(slot)
+        done[i].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[i])
+            d2h(slot)
+            out_done[i].record(s_out)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / max(steps, 1)
+
+
 def run_ours(args, shape, world, rank, local):
     import torch
     from qb_inputs.device import layer_for, upload
@@ -486,25 +525,25 @@ def run_ours(args, shape, world, rank, local):
     stages = lay.stage_times()
     lay.set_timing(0)
 
-    # end to end: pinned host input -> device, forward, device -> host output
+    # end to end: pinned host input -> device, forward, device -> host output,
+    # double-buffered so that copies overlap the neighbouring steps' forwards
     x_host = x.cpu().pin_memory()
     out_host = torch.empty_like(x_host).pin_memory()
-    x_dev = torch.empty_like(x)
-    for _ in range(2):
-        x_dev.copy_(x_host, non_blocking=True)
-        lay.forward(x_dev, out=out)
-        out_host.copy_(out, non_blocking=True)
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    out_dev = [torch.empty_like(out) for _ in range(2)]
+
+    def h2d(slot):
+        x_dev[slot].copy_(x_host, non_blocking=True)
+
+    def fwd(slot):
+        lay.forward(x_dev[slot], out=out_dev[slot])
+
+    def d2h(slot):
+        out_host.copy_(out_dev[slot], non_blocking=True)
+
+    pipelined_e2e(2, stream, h2d, fwd, d2h)
     barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        lay.forward(x_dev, out=out)
-        out_host.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / max(args.steps, 1), world)
+    ms_e2e = max_over_ranks(pipelined_e2e(args.steps, stream, h2d, fwd, d2h), world)
     lay.close()
     mx_peak = None
     if shape.wfmt == "mxfp4" and rank == 0:
@@ -605,29 +644,35 @@ def run_route(args, shape, world, rank, local):
     ms = sum(a.elapsed_time(b) for a, b in ev) / max(args.steps, 1)
     value_job, ms_max = replica_throughput(T, ms, world)
 
-    # end to end: pinned host logits -> device, routing, device -> host indices and weights
+    # end to end: pinned host logits -> device, routing, device -> host indices
+    # and weights, double-buffered (two sets of routing buffers) so that the
+    # copies overlap the neighbouring steps' routing
     lg_host = logits.cpu().pin_memory()
     idx_host = torch.empty((T, k), dtype=torch.int32).pin_memory()
     w_host = torch.empty((T, k), dtype=torch.float32).pin_memory()
+    bufs = [dict(logits=torch.empty_like(logits), scores=torch.empty_like(scores), idx=torch.empty_like(idx),
+                 w=torch.empty_like(w), loads=torch.empty_like(loads), bias=torch.empty_like(bias),
+                 ws=torch.empty_like(ws)) for _ in range(2)]
 
-    def e2e_step():
-        logits.copy_(lg_host, non_blocking=True)
+    def h2d(slot):
+        bufs[slot]["logits"].copy_(lg_host, non_blocking=True)
+
+    def route(slot):
+        nonlocal logits, scores, idx, w, loads, bias, ws
+        keep = (logits, scores, idx, w, loads, bias, ws)
+        b = bufs[slot]
+        logits, scores, idx, w, loads, bias, ws = (b["logits"], b["scores"], b["idx"], b["w"], b["loads"],
+                                                   b["bias"], b["ws"])
         step()
-        idx_host.copy_(idx, non_blocking=True)
-        w_host.copy_(w, non_blocking=True)
+        logits, scores, idx, w, loads, bias, ws = keep
 
-    for _ in range(2):
-        e2e_step()
+    def d2h(slot):
+        idx_host.copy_(bufs[slot]["idx"], non_blocking=True)
+        w_host.copy_(bufs[slot]["w"], non_blocking=True)
+
+    pipelined_e2e(2, stream, h2d, route, d2h)
     barrier(world)
-    torch.cuda.synchronize()
-    ev_e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in ev_e:
-        flush.fill_(1)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_e) / max(args.steps, 1), world)
+    ms_e2e = max_over_ranks(pipelined_e2e(args.steps, stream, h2d, route, d2h), world)
     if rank != 0:
         return
     balance = route_balance(logits, k, loads, T, n) if not gs else None
