@@ -80,3 +80,31 @@ def test_zero_sweeps_is_the_frozen_router():
     o = O.moe_route_qb(logits, b, 4, qb_sweeps=0)
     for name, a, bb in zip(("scores", "bias", "idx", "w", "loads"), g[:5], o):
         assert _same(a, bb), name
+
+
+def test_repeated_calls_on_the_same_buffers():
+    """Calls that reuse one set of buffers route the logits the buffers hold
+    at each call, bit-exact like a fresh call."""
+    import quantile_balanced_routing_gb300 as Q
+    T, n, k, sweeps = 300, 24, 3, 2
+    lib = Q.load_library()
+    dev = torch.device("cuda", 0)
+    lg = torch.empty((T, n), dtype=torch.float32, device=dev)
+    outs = dict(scores=torch.empty((T, n), dtype=torch.float32, device=dev),
+                bias=torch.empty((n,), dtype=torch.float32, device=dev),
+                idx=torch.empty((T, k), dtype=torch.int32, device=dev),
+                w=torch.empty((T, k), dtype=torch.float32, device=dev),
+                loads=torch.empty((n,), dtype=torch.int32, device=dev))
+    done = torch.zeros((4,), dtype=torch.int32, device=dev)
+    ws = torch.empty((lib.qbmoe_route_gs_workspace_bytes(T, n, k),), dtype=torch.uint8, device=dev)
+    p = lambda t: t.data_ptr()
+    for seed in (11, 12, 13):
+        logits = _logits(T, n, seed=seed, ov=1.5)
+        lg.copy_(torch.from_numpy(logits))
+        rc = lib.moe_route_qb_gs(T, n, k, sweeps, 0, p(lg), None, p(outs["bias"]), p(outs["scores"]), p(outs["idx"]),
+                                 p(outs["w"]), p(outs["loads"]), p(done), p(ws), ws.numel(), None)
+        assert rc == 0
+        torch.cuda.synchronize()
+        o = O.moe_route_qb(logits, None, k, qb_sweeps=sweeps, mode="gauss_seidel")
+        for name, b in zip(("scores", "bias", "idx", "w", "loads"), o):
+            assert _same(outs[name].cpu().numpy(), b), (seed, name)
