@@ -61,7 +61,11 @@ constexpr int kConvWarps = 8;                          // MXFP4 converter warps 
 constexpr int kThreadsMx = (kConvFirstWarp + kConvWarps) * 32;  // 480
 constexpr int kSfWarps = 4;                            // block-scaled MXFP4: scale writers, one per TMEM lane quarter
 constexpr int kSfFirstWarp = kProdB1Warp + 1;          // 9
-constexpr int kThreadsMxS = (kSfFirstWarp + kSfWarps) * 32;     // 416
+// block-scaled MXFP4: a second epilogue group (one warp per lane quarter)
+// takes every other 16-token chunk of a tile (its stacked hi and lo
+// accumulators make the epilogue twice as long per token)
+constexpr int kEpi2FirstWarp = kSfFirstWarp + kSfWarps;      // 13
+constexpr int kThreadsMxS = (kEpi2FirstWarp + 4) * 32;       // 544
 constexpr int kThreadsBf16 = (kProdB1Warp + 1) * 32;   // 288
 constexpr int kBKS = 128;                      // block-scaled: K elements per stage (128 bytes of E4M3 per row)
 constexpr int kScaleGroupS = 4;                // block-scaled: stages per E8M0 scale load (16 scale bytes per row)
@@ -300,14 +304,17 @@ __device__ __forceinline__ void store_e4m3_block(uint8_t* row, int F, int f, con
 // lo_col > 0 (block-scaled, stacked token planes): the accumulator holds
 // W * hi in columns [0, n) and W * lo in [lo_col, lo_col + n); the result is
 // hi + lo * 2^-kLoShift.
+// grp / n_grp: this group's share of the chunks (chunk c of the tile goes to
+// group c % n_grp); bar: the group's named barrier; st: its staging buffer.
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo& ti, const SubGemm& sg, int f_base,
-                                              uint32_t tacc, int lo_col, int q, int lane, int et, float* st) {
+                                              uint32_t tacc, int lo_col, int q, int lane, int et, float* st,
+                                              int grp = 0, int n_grp = 1, int bar = 1) {
     const int n_eff = (ti.nrows + 15) & ~15;
     // Staging: st[j * kStRow + f] holds token j (of a 16-token chunk) of the
     // tile's feature row f.  Each thread writes its feature row's 16 tokens
     // (consecutive lanes, consecutive words: no bank conflict); the stores
     // then read a token's consecutive features as float4 vectors.
-    for (int c0 = 0; c0 < n_eff; c0 += 16) {
+    for (int c0 = 16 * grp; c0 < n_eff; c0 += 16 * n_grp) {
         float v[16];
         tc::tmem_ld16(tacc + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
         if (lo_col > 0) {
@@ -316,10 +323,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = fmaf(lo[j], 1.0f / float(1 << kLoShift), v[j]);
         }
-        tc::named_bar_sync(1, 128);   // previous chunk's readers are done
+        tc::named_bar_sync(bar, 128);   // previous chunk's readers are done
 #pragma unroll
         for (int j = 0; j < 16; ++j) st[j * kStRow + 32 * q + lane] = v[j];
-        tc::named_bar_sync(1, 128);
+        tc::named_bar_sync(bar, 128);
         const int tok_left = ti.nrows - c0;
         if (sg.epi == SUB_STORE) {
             // 16 tokens x 16 groups of 8 features: two items per thread
@@ -531,7 +538,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&accf[a], 1);
-            tc::mbar_init(&acce[a], 4);
+            tc::mbar_init(&acce[a], MXS ? 8 : 4);   // every epilogue warp arrives
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -1039,10 +1046,16 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;               // TMEM lane quarter of this warp
-        const int et = threadIdx.x - kEpiFirstWarp * 32;   // 0..127
+        // block-scaled: two groups of four warps (3-6, 13-16), each with its
+        // own barrier, verdict word and staging buffer
+        const int grp = MXS && warp >= kEpi2FirstWarp ? 1 : 0;
+        constexpr int kGroups = MXS ? 2 : 1;
+        const int bar = grp ? 3 : 1;
+        const int et = threadIdx.x - (grp ? kEpi2FirstWarp : kEpiFirstWarp) * 32;   // 0..127
+        float* stg = st + grp * (kStBytes / 4);
         int ab = 0;
         uint32_t aph = 0;
-        volatile int* ok_slot = abort_flag + 1;
+        volatile int* ok_slot = abort_flag + 1 + grp;
         TileWalker<BN> tw;
         tw.start(p);
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, tw.next(p)) {
@@ -1058,13 +1071,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 }
                 *ok_slot = ok ? 1 : 0;
             }
-            tc::named_bar_sync(1, 128);
+            tc::named_bar_sync(bar, 128);
             const bool ok = *ok_slot != 0;
-            tc::named_bar_sync(1, 128);
+            tc::named_bar_sync(bar, 128);
             if (!ok) break;
             tc::tc_fence_after();
             epilogue_tile(p, ti, sg, sg.epi == SUB_SITU ? ti.mt * 64 : ti.mt * 128, tbase + ab * kAccCols,
-                          MXS ? (ti.nrows + 15) & ~15 : 0, q, lane, et, st);
+                          MXS ? (ti.nrows + 15) & ~15 : 0, q, lane, et, stg, grp, kGroups, bar);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acce[ab]);
@@ -1383,7 +1396,7 @@ constexpr size_t smem_for() {
     constexpr int S = stages_of<BN, MODE>();
     constexpr bool MX = MODE == MODE_MX_DECODE, MXS = MODE == MODE_MX_SCALED;
     return 1024 + (size_t)S * (kATileBytes + (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
-           (MX || MXS ? 2 * kScaleBytes : 0) + (MXS ? 2 * BN * 16 : 0) + 768 + kStBytes;
+           (MX || MXS ? 2 * kScaleBytes : 0) + (MXS ? 2 * BN * 16 : 0) + 768 + (MXS ? 2 : 1) * kStBytes;
 }
 
 }  // namespace
