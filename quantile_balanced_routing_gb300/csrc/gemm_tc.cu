@@ -510,8 +510,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     uint64_t* accf = emptyS + (MX || MXS ? 2 : 0);
     uint64_t* acce = accf + 2;
     uint64_t* drain = acce + 2;
-    // words after the barriers: [0] TMEM base, [1] abort flag, [2] the
-    // epilogue's per-tile verdict, [4, 5] the MMA issuer's per-tile go/stop
+    // words after the barriers: [0] TMEM base, [1] abort flag, [2, 3] the
+    // epilogue groups' per-tile ok words, [4, 5] the MMA issuer's per-tile go/stop
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* go_flag = reinterpret_cast<volatile int*>(tmem_slot + 4);   // [2]: per-tile MMA go/stop
@@ -1047,7 +1047,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;               // TMEM lane quarter of this warp
         // block-scaled: two groups of four warps (3-6, 13-16), each with its
-        // own barrier, verdict word and staging buffer
+        // own barrier, ok word and staging buffer
         const int grp = MXS && warp >= kEpi2FirstWarp ? 1 : 0;
         constexpr int kGroups = MXS ? 2 : 1;
         const int bar = grp ? 3 : 1;
@@ -1062,7 +1062,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             TileInfo ti;
             tw.get(p, tile, n_tiles_dense, ti);
             const SubGemm& sg = p.sub[ti.sub];
-            // one thread waits; the verdict is shared so the 128 threads stay uniform
+            // one thread waits; its result is shared so the 128 threads stay uniform
             if (et == 0) {
                 const bool ok = tc::mbar_wait<kTestFirst>(&accf[ab], aph, lim);
                 if (!ok) {
