@@ -468,6 +468,13 @@ constexpr int threads_of() {
 constexpr int kHandoffBar = 2;   // named barrier of the MMA warp and its waiter (64 threads)
 constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
+// 128-K sub-tiles per stage: two for the block-scaled kernel on 16-row token
+// tiles, whose short MMAs (N = 32) leave the per-stage hand-off, commit and
+// barrier costs comparable to the MMAs themselves, so a stage carries eight
+// MMAs instead of four; one elsewhere.
+template <int BN, int MODE>
+constexpr int ksub_of() { return MODE == MODE_MX_SCALED && BN == 16 ? 2 : 1; }
+
 template <int BN, int S, int MODE>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_constant__ TcParams p) {
     constexpr bool MX = MODE == MODE_MX_DECODE;    // MXFP4 decoded to bf16 by converter warps
@@ -482,12 +489,17 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     // SMEM, so one N = 2n MMA is much cheaper than two N = n ones.)
     static_assert(!MXS || 2 * BN <= 256, "stacked token planes need N = 2 BN <= 256");
     constexpr int kAccCols = MXS ? 2 * BN : BN;   // TMEM columns per accumulator
-    // TMEM columns: two accumulators; block-scaled adds, per stage, an
-    // 8-column token-scale slot (N = 2 BN <= 256 rows) and a 4-column
-    // weight-scale slot.
-    constexpr int kSfbCol = 2 * kAccCols, kSfaCol = 2 * kAccCols + 8 * S;
-    constexpr uint32_t kCols = MXS ? pow2_cols(kSfaCol + 4 * S) : pow2_cols(2 * BN);
-    static_assert(!MXS || kSfaCol + 4 * S <= 512, "TMEM columns");
+    constexpr int kSub = ksub_of<BN, MODE>();     // 128-K sub-tiles per stage
+    constexpr int kAStage = kATileBytes * kSub;   // a stage's weight tiles
+    constexpr int kBStage = kBBytes * kSub;       // a stage's token tiles
+    static_assert(kScaleGroupS % kSub == 0, "whole stages per scale group");
+    constexpr int kGrpStages = kScaleGroupS / kSub;   // block-scaled: stages per scale group
+    // TMEM columns: two accumulators; block-scaled adds, per stage and 128-K
+    // sub-tile, an 8-column token-scale slot (N = 2 BN <= 256 rows) and a
+    // 4-column weight-scale slot.
+    constexpr int kSfbCol = 2 * kAccCols, kSfaCol = 2 * kAccCols + 8 * kSub * S;
+    constexpr uint32_t kCols = MXS ? pow2_cols(kSfaCol + 4 * kSub * S) : pow2_cols(2 * BN);
+    static_assert(!MXS || kSfaCol + 4 * kSub * S <= 512, "TMEM columns");
     constexpr int kTokScBytes = MXS ? BN * 16 : 0;   // token scales of one scale group (16 per row)
     constexpr bool kScaleAhead = MXS && BN >= 64;     // scale groups issued one group ahead
     extern __shared__ uint8_t smem_raw[];
@@ -498,8 +510,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     // MXFP4 weights add: a ring of packed E2M1 blocks (S x 4 KB) and two
     // scale slots (2 x 2 KB, 8 K blocks each).
     uint8_t* a_ring = smem;
-    uint8_t* b_ring = smem + S * kATileBytes;
-    uint8_t* p_ring = b_ring + S * kBBytes;
+    uint8_t* b_ring = smem + S * kAStage;
+    uint8_t* p_ring = b_ring + S * kBStage;
     uint8_t* sc_ring = p_ring + (MX ? S * kPackBytes : 0);
     uint8_t* tsc_ring = sc_ring + (MX || MXS ? 2 * kScaleBytes : 0);   // block-scaled: 2 token-scale slots
     uint64_t* full = reinterpret_cast<uint64_t*>(tsc_ring + 2 * kTokScBytes);
@@ -662,7 +674,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         // blocks also the E8M0 scales (16 bytes per row).
                         const bool situ = sg.epi == SUB_SITU;
                         const int y = ti.g * sg.F + ti.mt * (situ ? 64 : 128);
-                        constexpr int sgrp = MX ? kScaleGroup : kScaleGroupS;
+                        constexpr int sgrp = MX ? kScaleGroup : kGrpStages;   // stages per scale group
                         if (MXS && kb % sgrp == 0) {
                             // Weight and token scales of a group go out one group
                             // ahead (two slots) on prefill-sized tiles, so that the
@@ -735,13 +747,18 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         } else {
                             // 128 rows x 128 codes, each 16-code chunk landing as 8 bytes + 8 unused;
                             // the transaction counts the 8 KB of packed codes read
-                            uint8_t* A = a_ring + s * kATileBytes;
-                            tc::mbar_expect_tx(&full[s], kATileBytes / 2);
-                            if (situ) {
-                                tc::tma_load_2d(A, &p.a0[ti.sub], &full[s], kb * kBKS, y);
-                                tc::tma_load_2d(A + kATileBytes / 2, &p.a1[ti.sub], &full[s], kb * kBKS, y);
-                            } else {
-                                tc::tma_load_2d(A, &p.a0[ti.sub], &full[s], kb * kBKS, y);
+                            uint8_t* A = a_ring + s * kAStage;
+                            tc::mbar_expect_tx(&full[s], kSub * kATileBytes / 2);
+#pragma unroll
+                            for (int u = 0; u < kSub; ++u) {
+                                const int xk = (kb * kSub + u) * kBKS;
+                                uint8_t* Au = A + u * kATileBytes;
+                                if (situ) {
+                                    tc::tma_load_2d(Au, &p.a0[ti.sub], &full[s], xk, y);
+                                    tc::tma_load_2d(Au + kATileBytes / 2, &p.a1[ti.sub], &full[s], xk, y);
+                                } else {
+                                    tc::tma_load_2d(Au, &p.a0[ti.sub], &full[s], xk, y);
+                                }
                             }
                         }
                     } else if (is_a) {
@@ -759,13 +776,19 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                                 tc::tma_load_2d(A, &p.a1[ti.sub], &fullx[s], (kb - sg.k_split) * kBK, y);
                         }
                     } else {
-                        uint8_t* B = b_ring + s * kBBytes;
-                        tc::mbar_expect_tx(&fullx[s], (MXS ? 2 : 1) * n_eff * 128);
-                        // the n_eff token rows as one box (block-scaled: hi columns kb * 128, lo
-                        // columns K + kb * 128, the lo rows stacked under the hi rows)
+                        uint8_t* B = b_ring + s * kBStage;
+                        tc::mbar_expect_tx(&fullx[s], (MXS ? 2 : 1) * n_eff * 128 * kSub);
+                        // the n_eff token rows as one box per 128-K sub-tile (block-scaled:
+                        // hi columns k, lo columns K + k, the lo rows stacked under the hi rows)
                         const CUtensorMap* bmap = &p.bx[(n_eff >> 4) - 1];
-                        tc::tma_load_2d(B, bmap, &fullx[s], kb * kKS, ti.row0);
-                        if (MXS) tc::tma_load_2d(B + n_eff * 128, bmap, &fullx[s], (p.nkb + kb) * kKS, ti.row0);
+#pragma unroll
+                        for (int u = 0; u < kSub; ++u) {
+                            const int kk128 = kb * kSub + u;
+                            tc::tma_load_2d(B + u * kBBytes, bmap, &fullx[s], kk128 * kKS, ti.row0);
+                            if (MXS)
+                                tc::tma_load_2d(B + u * kBBytes + n_eff * 128, bmap, &fullx[s],
+                                                (p.nkb * kSub + kk128) * kKS, ti.row0);
+                        }
                     }
                     issued |= 1u << s;
                     last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -877,10 +900,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 tw.get(p, tile + gridDim.x, n_tiles_dense, tn);
             }
             bool ok = true;
-            for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += kScaleGroupS) {
+            for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += kGrpStages) {
                 uint4 wa[4], wt[8];
 #pragma unroll
-                for (int kq = 0; kq < kScaleGroupS; ++kq) {
+                for (int kq = 0; kq < kGrpStages; ++kq) {
                     int w = 1;
                     if (lane == 0) {
                         if (kq == 0) w = tc::mbar_wait<kTestFirst>(&fullS[gidx & 1], (gidx >> 1) & 1u, lim);
@@ -911,12 +934,18 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                         if (lane == 0) tc::mbar_arrive(&emptyS[slot]);   // the group is in registers
                         ++gidx;
                     }
-                    tc::tmem_st4(tbase + lanes + kSfaCol + 4 * s, word_of(wa[0], kq), word_of(wa[1], kq),
-                                 word_of(wa[2], kq), word_of(wa[3], kq));
-                    tc::tmem_st4(tbase + lanes + kSfbCol + 8 * s, word_of(wt[0], kq), word_of(wt[1], kq),
-                                 word_of(wt[2], kq), word_of(wt[3], kq));
-                    tc::tmem_st4(tbase + lanes + kSfbCol + 8 * s + 4, word_of(wt[4], kq), word_of(wt[5], kq),
-                                 word_of(wt[6], kq), word_of(wt[7], kq));
+#pragma unroll
+                    for (int u = 0; u < kSub; ++u) {
+                        const int wi = kq * kSub + u;   // the sub-tile's word of the group's 16 bytes
+                        const uint32_t ca = tbase + lanes + kSfaCol + 4 * (kSub * s + u);
+                        const uint32_t cb = tbase + lanes + kSfbCol + 8 * (kSub * s + u);
+                        tc::tmem_st4(ca, word_of(wa[0], wi), word_of(wa[1], wi), word_of(wa[2], wi),
+                                     word_of(wa[3], wi));
+                        tc::tmem_st4(cb, word_of(wt[0], wi), word_of(wt[1], wi), word_of(wt[2], wi),
+                                     word_of(wt[3], wi));
+                        tc::tmem_st4(cb + 4, word_of(wt[4], wi), word_of(wt[5], wi), word_of(wt[6], wi),
+                                     word_of(wt[7], wi));
+                    }
                     tc::tmem_wait_st();
                     tc::tc_fence_before();
                     __syncwarp();
@@ -968,15 +997,19 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 tc::named_bar_sync(kHandoffBar, 64);   // stage sa has landed
                 if (lane == 0) {
                     tc::tc_fence_after();
-                    const uint64_t ad = a_desc0 + (uint64_t)(sa * (kATileBytes >> 4));
-                    const uint64_t bd = b_desc0 + (uint64_t)(sa * (kBBytes >> 4));
-                    const uint32_t sfa = tbase + kSfaCol + 4 * sa, sfb = tbase + kSfbCol + 8 * sa;
+                    const uint64_t ad = a_desc0 + (uint64_t)(sa * (kAStage >> 4));
+                    const uint64_t bd = b_desc0 + (uint64_t)(sa * (kBStage >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
+                    for (int kk = 0; kk < 4 * kSub; ++kk) {
                         if (MXS) {
-                            // 32-wide K slice kk (byte kk of the weight scale words)
-                            // against the stacked hi and lo rows
-                            tc::tc_mma_mxf8f6f4(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], sfa, sfb, (kb | kk) != 0);
+                            // 128-K sub-tile u, 32-wide K slice kq (byte kq of the weight and
+                            // token scale words) against the stacked hi and lo rows
+                            const int u = kk >> 2, kq = kk & 3;
+                            const uint32_t sfa = tbase + kSfaCol + 4 * (kSub * sa + u);
+                            const uint32_t sfb = tbase + kSfbCol + 8 * (kSub * sa + u);
+                            tc::tc_mma_mxf8f6f4(d, ad + (uint64_t)(u * (kATileBytes >> 4)) + 2 * kq,
+                                                bd + (uint64_t)(u * (kBBytes >> 4)) + 2 * kq, id_k[kq], sfa, sfb,
+                                                (kb | kk) != 0);
                         } else {
                             tc::tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], (kb | kk) != 0);
                         }
@@ -1380,7 +1413,7 @@ template <> struct StagesMx<160> { static constexpr int S = 5; };
 // Block-scaled MXFP4: stages as for bf16 (a 16 KB E2M1 tile and a token tile
 // of BN x 128 E4M3 bytes) plus two 2 KB scale slots.
 template <int BN> struct StagesMxS;
-template <> struct StagesMxS<16> { static constexpr int S = 10; };
+template <> struct StagesMxS<16> { static constexpr int S = 5; };   // stages of two 128-K sub-tiles
 template <> struct StagesMxS<64> { static constexpr int S = 6; };
 template <> struct StagesMxS<112> { static constexpr int S = 4; };
 
@@ -1395,7 +1428,8 @@ template <int BN, int MODE>
 constexpr size_t smem_for() {
     constexpr int S = stages_of<BN, MODE>();
     constexpr bool MX = MODE == MODE_MX_DECODE, MXS = MODE == MODE_MX_SCALED;
-    return 1024 + (size_t)S * (kATileBytes + (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
+    constexpr int kSub = ksub_of<BN, MODE>();
+    return 1024 + (size_t)S * (kSub * kATileBytes + kSub * (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
            (MX || MXS ? 2 * kScaleBytes : 0) + (MXS ? 2 * BN * 16 : 0) + 768 + (MXS ? 2 : 1) * kStBytes;
 }
 
@@ -1845,7 +1879,7 @@ static int prep_grouped(TcPlan* P, TcLaunch& L, bool pair, const void* act, long
         // E4M3 rows: hi plane, lo plane, block scales
         if (K % 512 != 0) return QBMOE_EINVAL;   // whole scale groups: the scale writers take stage pairs
         if (!make_token_maps_e4m3(P, prm, act, routes, K, BN)) return QBMOE_ECUDA;
-        prm.nkb = (int)(K / kBKS);
+        prm.nkb = (int)(K / (kBKS * (BN == 16 ? 2 : 1)));   // stages of ksub_of<BN, MODE_MX_SCALED> sub-tiles
     } else {
         if (!make_token_maps(P, prm, act, routes, K, K, pair ? 8 : 16, pair ? BN / 2 : BN)) return QBMOE_ECUDA;
         prm.nkb = (int)((K + kBK - 1) / kBK);
