@@ -14,20 +14,27 @@
 // expert still issues full-height MMAs while streaming the weights.
 //
 // One persistent, warp-specialised kernel (one CTA per SM):
-//   warp 0      weight producer (one lane): TMA of A tiles into a
-//               STAGES-deep ring (and the E8M0 scales for MXFP4)
-//   warp 1      token producer (one lane): TMA of B tiles into the same stage
+//   warps 0, 7  weight producers (one lane each; warp 7 takes the odd K
+//               blocks): TMA of A tiles into a STAGES-deep ring (and the
+//               E8M0 scales for MXFP4)
+//   warps 1, 8  token producers (one lane each; or, on 16-row bf16 tiles,
+//               the whole warp gathering the tile's rows by route with
+//               tile::gather4)
 //   warp 2      TMEM owner and MMA issuer (one lane); one commit per stage
 //               frees it, a tile's last commit hands the accumulator over
 //   warps 3-6   epilogue: tcgen05.ld 32 lanes x 16 columns, stage through
 //               SMEM, epilogue math, 16-byte stores
-//   warps 7+    MXFP4 only: converter warps (decode E2M1 to bf16 in SMEM for
-//               the kind::f16 MMA) or scale writers (E8M0 scale words into
-//               TMEM for the block-scaled kind::mxf8f6f4 MMA)
+//   warps 7+    MXFP4 decode only (one producer pair): converter warps that
+//               decode E2M1 to bf16 in SMEM for the kind::f16 MMA
+//   warps 9-12  block-scaled only: scale writers (E8M0 weight and token
+//               scale words into TMEM); warps 13-16 a second epilogue group
+//   last warp   the MMA issuer's waiter: every mbarrier wait of the issuer,
+//               handed over through a named barrier
 // Modes: bf16 weights (kind::f16, 4 x K=16 MMAs per 64-wide K stage);
 // MXFP4 decoded to bf16; MXFP4 block-scaled (E2M1 unpacked by TMA, tokens
-// as exact E4M3 hi/lo pairs stacked in one N = 2n MMA, 4 x K=32 MMAs per
-// 128-wide K stage).
+// as exact E4M3 hi/lo pairs with per-32 E8M0 scales stacked in one N = 2n
+// MMA, 4 x K=32 MMAs per 128-wide K sub-tile, two sub-tiles per stage on
+// 16-row token tiles).
 // Two TMEM accumulators alternate so a tile's epilogue overlaps the next
 // tile's main loop.  Every mbarrier wait is bounded: on expiry the kernel
 // records QBMOE_ETIMEOUT, stops, drains its own TMA/MMA work (bounded) and
