@@ -482,7 +482,7 @@ constexpr uint32_t pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 template <int BN, int MODE>
 constexpr int ksub_of() { return MODE == MODE_MX_SCALED && BN == 16 ? 2 : 1; }
 
-template <int BN, int S, int MODE>
+template <int BN, int S, int MODE, int MP>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_constant__ TcParams p) {
     constexpr bool MX = MODE == MODE_MX_DECODE;    // MXFP4 decoded to bf16 by converter warps
     constexpr bool MXS = MODE == MODE_MX_SCALED;   // MXFP4 on the block-scaled MMA, E4M3 tokens
@@ -497,7 +497,14 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     static_assert(!MXS || 2 * BN <= 256, "stacked token planes need N = 2 BN <= 256");
     constexpr int kAccCols = MXS ? 2 * BN : BN;   // TMEM columns per accumulator
     constexpr int kSub = ksub_of<BN, MODE>();     // 128-K sub-tiles per stage
-    constexpr int kAStage = kATileBytes * kSub;   // a stage's weight tiles
+    // MP m-tiles per work unit (bf16): the unit's MP weight tiles share each
+    // stage's token tile, so the token rows cross shared memory once per MP
+    // MMAs.  Its MP accumulators come from a ring of kSlots TMEM slots (MP = 2:
+    // three, so the next unit can start once the epilogue has drained the
+    // first accumulator of this one).
+    static_assert(MP == 1 || (MODE == MODE_BF16 && 3 * BN <= 512), "paired m-tiles: bf16, three accumulators");
+    constexpr int kSlots = MP == 1 ? 2 : 3;
+    constexpr int kAStage = kATileBytes * kSub * MP;   // a stage's weight tiles
     constexpr int kBStage = kBBytes * kSub;       // a stage's token tiles
     static_assert(kScaleGroupS % kSub == 0, "whole stages per scale group");
     constexpr int kGrpStages = kScaleGroupS / kSub;   // block-scaled: stages per scale group
@@ -505,7 +512,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     // sub-tile, an 8-column token-scale slot (N = 2 BN <= 256 rows) and a
     // 4-column weight-scale slot.
     constexpr int kSfbCol = 2 * kAccCols, kSfaCol = 2 * kAccCols + 8 * kSub * S;
-    constexpr uint32_t kCols = MXS ? pow2_cols(kSfaCol + 4 * kSub * S) : pow2_cols(2 * BN);
+    constexpr uint32_t kCols = MXS ? pow2_cols(kSfaCol + 4 * kSub * S) : pow2_cols(kSlots * BN);
     static_assert(!MXS || kSfaCol + 4 * kSub * S <= 512, "TMEM columns");
     constexpr int kTokScBytes = MXS ? BN * 16 : 0;   // token scales of one scale group (16 per row)
     constexpr bool kScaleAhead = MXS && BN >= 64;     // scale groups issued one group ahead
@@ -527,8 +534,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
     uint64_t* fullS = fullP + (MX ? S : 0);            // MX, MXS: scale group landed
     uint64_t* emptyS = fullS + (MX || MXS ? 2 : 0);    // MX, MXS: scale group consumed
     uint64_t* accf = emptyS + (MX || MXS ? 2 : 0);
-    uint64_t* acce = accf + 2;
-    uint64_t* drain = acce + 2;
+    uint64_t* acce = accf + kSlots;
+    uint64_t* drain = acce + kSlots;
     // words after the barriers: [0] TMEM base, [1] abort flag, [2, 3] the
     // epilogue groups' per-tile ok words, [4, 5] the MMA issuer's per-tile go/stop
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -555,7 +562,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 tc::mbar_init(&emptyS[g], MX ? kConvWarps : kSfWarps);
             }
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kSlots; ++a) {
             tc::mbar_init(&accf[a], 1);
             tc::mbar_init(&acce[a], MXS ? 8 : 4);   // every epilogue warp arrives
         }
@@ -769,18 +776,23 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                             }
                         }
                     } else if (is_a) {
-                        uint8_t* A = a_ring + s * kATileBytes;
-                        tc::mbar_expect_tx(&fullx[s], kATileBytes);
-                        if (sg.epi == SUB_SITU) {
-                            const int y = ti.g * sg.F + ti.mt * 64;
-                            tc::tma_load_2d(A, &p.a0[ti.sub], &fullx[s], kb * kBK, y);
-                            tc::tma_load_2d(A + kATileBytes / 2, &p.a1[ti.sub], &fullx[s], kb * kBK, y);
-                        } else {
-                            const int y = ti.g * sg.F + ti.mt * 128;
-                            if (kb < sg.k_split)
+                        uint8_t* A0 = a_ring + s * kAStage;
+                        tc::mbar_expect_tx(&fullx[s], kAStage);
+#pragma unroll
+                        for (int hm = 0; hm < MP; ++hm) {   // the unit's m-tiles
+                            uint8_t* A = A0 + hm * kATileBytes;
+                            const int mt = ti.mt * MP + hm;
+                            if (sg.epi == SUB_SITU) {
+                                const int y = ti.g * sg.F + mt * 64;
                                 tc::tma_load_2d(A, &p.a0[ti.sub], &fullx[s], kb * kBK, y);
-                            else
-                                tc::tma_load_2d(A, &p.a1[ti.sub], &fullx[s], (kb - sg.k_split) * kBK, y);
+                                tc::tma_load_2d(A + kATileBytes / 2, &p.a1[ti.sub], &fullx[s], kb * kBK, y);
+                            } else {
+                                const int y = ti.g * sg.F + mt * 128;
+                                if (kb < sg.k_split)
+                                    tc::tma_load_2d(A, &p.a0[ti.sub], &fullx[s], kb * kBK, y);
+                                else
+                                    tc::tma_load_2d(A, &p.a1[ti.sub], &fullx[s], (kb - sg.k_split) * kBK, y);
+                            }
                         }
                     } else {
                         uint8_t* B = b_ring + s * kBStage;
@@ -976,7 +988,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         // through named barrier kHandoffBar; once per tile it also passes the
         // go/stop decision in go_flag.
         int sa = 0;
-        int ab = 0;
+        int z0 = 0;   // TMEM slot of the unit's first accumulator
         int h = 0;
         TileWalker<BN> tw;
         tw.start(p);
@@ -985,11 +997,14 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
             tw.get(p, tile, n_tiles_dense, ti);
             const uint32_t n_eff = (ti.nrows + 15) & ~15;
             const uint32_t idesc = tc::idesc_bf16_m128(n_eff);
-            tc::named_bar_sync(kHandoffBar, 64);   // accumulator ab is free (or stop)
+            tc::named_bar_sync(kHandoffBar, 64);   // the unit's accumulators are free (or stop)
             const bool go = go_flag[h & 1] != 0;
             ++h;
             if (!go) break;
-            const uint32_t d = tbase + ab * kAccCols;
+            uint32_t dm[MP];
+#pragma unroll
+            for (int hm = 0; hm < MP; ++hm) dm[hm] = tbase + ((z0 + hm) % kSlots) * kAccCols;
+            const uint32_t d = dm[0];
             // Descriptors step by plain adds: the start-address field holds
             // address / 16, so a 32-byte K step is +2 and a stage is
             // +stage_bytes / 16 (addresses stay below 256 KB, inside the
@@ -1018,7 +1033,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                                                 bd + (uint64_t)(u * (kBBytes >> 4)) + 2 * kq, id_k[kq], sfa, sfb,
                                                 (kb | kk) != 0);
                         } else {
-                            tc::tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_k[kk], (kb | kk) != 0);
+#pragma unroll
+                            for (int hm = 0; hm < MP; ++hm)
+                                tc::tc_mma_bf16(dm[hm], ad + (uint64_t)(hm * (kATileBytes >> 4)) + 2 * kk,
+                                                bd + 2 * kk, id_k[kk], (kb | kk) != 0);
                         }
                     }
                     tc::tc_commit(&empty[sa]);
@@ -1026,9 +1044,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 __syncwarp();
                 if (++sa == S) sa = 0;
             }
-            if (lane == 0 && !(p.stall_first_tile && tile == (int)blockIdx.x)) tc::tc_commit(&accf[ab]);
+            if (lane == 0 && !(p.stall_first_tile && tile == (int)blockIdx.x))
+#pragma unroll
+                for (int hm = 0; hm < MP; ++hm) tc::tc_commit(&accf[(z0 + hm) % kSlots]);
             __syncwarp();
-            ab ^= 1;
+            z0 = (z0 + MP) % kSlots;
         }
         // all MMAs issued by this thread complete before TMEM is freed
         if (lane == 0) {
@@ -1046,20 +1066,27 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         // undefined after an expiry), until the next tile boundary stops both.
         int sa = 0;
         uint32_t pha = 0;
-        int ab = 0;
-        uint32_t aph = 0;
+        int z0 = 0;
+        uint32_t eph = 0;    // per TMEM slot: parity of its releases so far
         int h = 0;
         bool dead = false;   // lane 0: stop waiting
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
             if (lane == 0) {
                 if (!dead && *abort_flag) dead = true;
-                if (!dead && !tc::mbar_wait<kTestFirst>(&acce[ab], aph ^ 1u, lim)) {
-                    set_status(p.status, QBMOE_ETIMEOUT);
-                    *abort_flag = 1;
-                    dead = true;
+#pragma unroll
+                for (int hm = 0; hm < MP; ++hm) {
+                    const int z = (z0 + hm) % kSlots;
+                    if (!dead && !tc::mbar_wait<kTestFirst>(&acce[z], ((eph >> z) & 1u) ^ 1u, lim)) {
+                        set_status(p.status, QBMOE_ETIMEOUT);
+                        *abort_flag = 1;
+                        dead = true;
+                    }
                 }
                 go_flag[h & 1] = dead ? 0 : 1;
             }
+#pragma unroll
+            for (int hm = 0; hm < MP; ++hm) eph ^= 1u << ((z0 + hm) % kSlots);
+            z0 = (z0 + MP) % kSlots;
             __syncwarp();
             tc::named_bar_sync(kHandoffBar, 64);
             const bool go = go_flag[h & 1] != 0;
@@ -1078,8 +1105,6 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
                 tc::named_bar_sync(kHandoffBar, 64);
                 if (++sa == S) { sa = 0; pha ^= 1u; }
             }
-            ab ^= 1;
-            if (ab == 0) aph ^= 1u;
         }
         __syncwarp();
         __syncthreads();
@@ -1093,36 +1118,40 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) k_tc_gemm(const __grid_
         const int bar = grp ? 3 : 1;
         const int et = threadIdx.x - (grp ? kEpi2FirstWarp : kEpiFirstWarp) * 32;   // 0..127
         float* stg = st + grp * (kStBytes / 4);
-        int ab = 0;
-        uint32_t aph = 0;
+        int z = 0;           // TMEM slot of the next accumulator
+        uint32_t fph = 0;    // per slot: parity of its hand-offs so far
+        bool ok = true;
         volatile int* ok_slot = abort_flag + 1 + grp;
         TileWalker<BN> tw;
         tw.start(p);
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, tw.next(p)) {
+        for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, tw.next(p)) {
             TileInfo ti;
             tw.get(p, tile, n_tiles_dense, ti);
             const SubGemm& sg = p.sub[ti.sub];
-            // one thread waits; its result is shared so the 128 threads stay uniform
-            if (et == 0) {
-                const bool ok = tc::mbar_wait<kTestFirst>(&accf[ab], aph, lim);
-                if (!ok) {
-                    set_status(p.status, QBMOE_ETIMEOUT);
-                    *abort_flag = 1;
+            for (int hm = 0; hm < MP; ++hm) {   // the unit's accumulators, in hand-off order
+                // one thread waits; its result is shared so the 128 threads stay uniform
+                if (et == 0) {
+                    const bool okw = tc::mbar_wait<kTestFirst>(&accf[z], (fph >> z) & 1u, lim);
+                    if (!okw) {
+                        set_status(p.status, QBMOE_ETIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    *ok_slot = okw ? 1 : 0;
                 }
-                *ok_slot = ok ? 1 : 0;
+                tc::named_bar_sync(bar, 128);
+                ok = *ok_slot != 0;
+                tc::named_bar_sync(bar, 128);
+                if (!ok) break;
+                tc::tc_fence_after();
+                const int mt = ti.mt * MP + hm;
+                epilogue_tile(p, ti, sg, sg.epi == SUB_SITU ? mt * 64 : mt * 128, tbase + z * kAccCols,
+                              MXS ? (ti.nrows + 15) & ~15 : 0, q, lane, et, stg, grp, kGroups, bar);
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&acce[z]);
+                fph ^= 1u << z;
+                if (++z == kSlots) z = 0;
             }
-            tc::named_bar_sync(bar, 128);
-            const bool ok = *ok_slot != 0;
-            tc::named_bar_sync(bar, 128);
-            if (!ok) break;
-            tc::tc_fence_after();
-            epilogue_tile(p, ti, sg, sg.epi == SUB_SITU ? ti.mt * 64 : ti.mt * 128, tbase + ab * kAccCols,
-                          MXS ? (ti.nrows + 15) & ~15 : 0, q, lane, et, stg, grp, kGroups, bar);
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&acce[ab]);
-            ab ^= 1;
-            if (ab == 0) aph ^= 1u;
         }
         __syncthreads();
     }
@@ -1424,19 +1453,27 @@ template <> struct StagesMxS<16> { static constexpr int S = 5; };   // stages of
 template <> struct StagesMxS<64> { static constexpr int S = 6; };
 template <> struct StagesMxS<112> { static constexpr int S = 4; };
 
+// Paired m-tiles (bf16, 160-row token tiles): two 16 KB weight tiles and one
+// token tile per stage.
+template <int BN> struct StagesMp2;
+template <> struct StagesMp2<160> { static constexpr int S = 4; };
+
 template <int BN, int MODE> struct StagesOf { static constexpr int S = Stages<BN>::S; };
 template <int BN> struct StagesOf<BN, MODE_MX_DECODE> { static constexpr int S = StagesMx<BN>::S; };
 template <int BN> struct StagesOf<BN, MODE_MX_SCALED> { static constexpr int S = StagesMxS<BN>::S; };
 
-template <int BN, int MODE>
-constexpr int stages_of() { return StagesOf<BN, MODE>::S; }
+template <int BN, int MODE, int MP = 1>
+constexpr int stages_of() {
+    if constexpr (MP == 2) return StagesMp2<BN>::S;
+    else return StagesOf<BN, MODE>::S;
+}
 
-template <int BN, int MODE>
+template <int BN, int MODE, int MP = 1>
 constexpr size_t smem_for() {
-    constexpr int S = stages_of<BN, MODE>();
+    constexpr int S = stages_of<BN, MODE, MP>();
     constexpr bool MX = MODE == MODE_MX_DECODE, MXS = MODE == MODE_MX_SCALED;
     constexpr int kSub = ksub_of<BN, MODE>();
-    return 1024 + (size_t)S * (kSub * kATileBytes + kSub * (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
+    return 1024 + (size_t)S * (MP * kSub * kATileBytes + kSub * (MXS ? 2 : 1) * BN * 128 + (MX ? kPackBytes : 0)) +
            (MX || MXS ? 2 * kScaleBytes : 0) + (MXS ? 2 * BN * 16 : 0) + 768 + (MXS ? 2 : 1) * kStBytes;
 }
 
@@ -1452,6 +1489,7 @@ struct TcLaunch {
     int BN = 0;
     bool pair = false;
     int mode = MODE_BF16;
+    int mp = 1;   // m-tiles per work unit (one-CTA bf16 kernel)
     bool grouped = false;
     long long tiles = 0;
     bool ready = false;
@@ -1469,6 +1507,7 @@ struct TcPlan {
     bool pair_grouped = false;   // grouped launches on the 2-SM kernel (QBMOE_ENABLE_2SM=1)
     bool mx_scaled = false;  // MXFP4 experts on the block-scaled MMA (else decoded to bf16 in SMEM)
     bool no_gather = false;  // bf16 expert gate/up reads an expert-ordered copy of h (QBMOE_NO_GATHER=1)
+    bool no_mpair = false;   // bf16 prefill gate/up on single m-tiles (QBMOE_NO_MPAIR=1)
     int pair_clusters[2] = {0, 0};   // co-resident clusters of the 160 / 256 variants
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     TcLaunch stage[TC_STAGES];       // the forward's launches, prepared before the first one
@@ -1574,11 +1613,11 @@ bool make_map_u8(TcPlan* P, CUtensorMap* m, const void* base, long long rows, lo
 
 // Dynamic shared memory limits are set once per device by
 // tc_init_attributes (before any launch of the library on that device).
-template <int BN, int MODE>
+template <int BN, int MODE, int MP = 1>
 int attr_bn() {
-    constexpr size_t smem = smem_for<BN, MODE>();
+    constexpr size_t smem = smem_for<BN, MODE, MP>();
     static_assert(smem <= 232448, "shared memory per CTA");
-    return cuda_err(cudaFuncSetAttribute(k_tc_gemm<BN, stages_of<BN, MODE>(), MODE>,
+    return cuda_err(cudaFuncSetAttribute(k_tc_gemm<BN, stages_of<BN, MODE, MP>(), MODE, MP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
 }
 
@@ -1590,11 +1629,11 @@ int attr_bn2() {
                                          (int)smem));
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, int MP = 1>
 int launch_bn(TcParams& prm, int grid, cudaStream_t s) {
-    constexpr size_t smem = smem_for<BN, MODE>();
-    constexpr int S = stages_of<BN, MODE>();
-    k_tc_gemm<BN, S, MODE><<<grid, threads_of<MODE>(), smem, s>>>(prm);
+    constexpr size_t smem = smem_for<BN, MODE, MP>();
+    constexpr int S = stages_of<BN, MODE, MP>();
+    k_tc_gemm<BN, S, MODE, MP><<<grid, threads_of<MODE>(), smem, s>>>(prm);
     return cuda_err(cudaGetLastError());
 }
 
@@ -1712,6 +1751,7 @@ int prep_dense(TcPlan* P, TcLaunch& L, int BN, bool pair, int T, const void* x, 
     L.BN = BN;
     L.pair = pair;
     L.mode = MODE_BF16;
+    L.mp = 1;
     L.grouped = false;
     L.tiles = (long long)prm.m_total * ((T + BN - 1) / BN);
     if (pair && BN != 256) return QBMOE_EINVAL;
@@ -1731,6 +1771,7 @@ int launch_prepared(TcPlan* P, TcLaunch& L, cudaStream_t s) {
     if (L.mode == MODE_MX_DECODE) return launch_mx_decode(L.BN, L.prm, P->num_sms, s);
     if (L.pair)
         return L.BN == 160 ? launch_bn2<160>(P, L.prm, 1 << 30, s) : launch_bn2<256>(P, L.prm, 1 << 30, s);
+    if (L.mp == 2) return L.BN == 160 ? launch_bn<160, MODE_BF16, 2>(L.prm, P->num_sms, s) : QBMOE_EINVAL;
     return launch_any(L.BN, L.prm, P->num_sms, s);
 }
 
@@ -1767,6 +1808,8 @@ TcPlan* tc_plan_create(const qbmoe_config& cfg) {
     // expert-ordered copy of h) unless QBMOE_NO_GATHER=1 asks for the copy.
     const char* env5 = getenv("QBMOE_NO_GATHER");
     P->no_gather = env5 && env5[0] == '1';
+    const char* env6 = getenv("QBMOE_NO_MPAIR");
+    P->no_mpair = env6 && env6[0] == '1';
     if (P->enabled && (pair_occupancy<160>(P->num_sms, &P->pair_clusters[0]) ||
                        pair_occupancy<256>(P->num_sms, &P->pair_clusters[1]))) {
         // the 2-SM kernel cannot be placed: run everything on the one-CTA kernel
@@ -1778,7 +1821,7 @@ TcPlan* tc_plan_create(const qbmoe_config& cfg) {
 int tc_init_attributes() {
     int rc;
     if ((rc = attr_bn<16, MODE_BF16>()) || (rc = attr_bn<64, MODE_BF16>()) || (rc = attr_bn<128, MODE_BF16>()) ||
-        (rc = attr_bn<160, MODE_BF16>()) || (rc = attr_bn<256, MODE_BF16>()) ||
+        (rc = attr_bn<160, MODE_BF16>()) || (rc = attr_bn<256, MODE_BF16>()) || (rc = attr_bn<160, MODE_BF16, 2>()) ||
         (rc = attr_bn<16, MODE_MX_DECODE>()) || (rc = attr_bn<64, MODE_MX_DECODE>()) ||
         (rc = attr_bn<160, MODE_MX_DECODE>()) || (rc = attr_bn<16, MODE_MX_SCALED>()) ||
         (rc = attr_bn<64, MODE_MX_SCALED>()) || (rc = attr_bn<112, MODE_MX_SCALED>()) ||
@@ -1899,6 +1942,7 @@ static int prep_grouped(TcPlan* P, TcLaunch& L, bool pair, const void* act, long
     L.BN = BN;
     L.pair = pair;
     L.mode = mode;
+    L.mp = 1;
     L.grouped = true;
     L.tiles = 0;
     if (pair && BN != 160 && BN != 256) return QBMOE_EINVAL;
@@ -1962,7 +2006,16 @@ int tc_prepare_gate_up(TcPlan* P, int T, const void* h_perm, const int* offsets,
         prm.gather_rows = perm;
         return QBMOE_OK;
     }
-    return prep_grouped(P, L, pair, h_perm, routes, c.latent, offsets, tile_off, BN, mode);
+    int rc = prep_grouped(P, L, pair, h_perm, routes, c.latent, offsets, tile_off, BN, mode);
+    if (rc) return rc;
+    // Prefill-sized bf16 tiles: pairs of m-tiles share each stage's token
+    // tile (units of two m-tiles; QBMOE_NO_MPAIR=1 keeps single m-tiles).
+    if (mode == MODE_BF16 && !pair && BN == 160 && g.m_tiles % 2 == 0 && !P->no_mpair) {
+        L.mp = 2;
+        g.m_tiles /= 2;
+        prm.m_total = g.m_tiles;
+    }
+    return QBMOE_OK;
 }
 
 int tc_prepare_down(TcPlan* P, int T, const void* act, const int* offsets, const int* tile_off, void* e,

@@ -100,6 +100,27 @@ def test_gathered_token_rows_match_the_copied_ones(shape, monkeypatch):
     assert torch.equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("shape", [TC_PREFILL_LIKE], ids=lambda s: s.name)
+def test_paired_m_tiles_match_single_ones(shape, monkeypatch):
+    """Prefill-sized bf16 token tiles run the expert gate/up in units of two
+    m-tiles that share each stage's token tile; QBMOE_NO_MPAIR=1 runs the
+    same launch one m-tile at a time.  Every output element sums the same
+    products in the same K order either way, so the outputs are identical."""
+    from qb_inputs.device import layer_for, upload
+    d = upload(QI.LayerInputs(shape), "cuda:0")
+    outs = []
+    for env in ("0", "1"):
+        monkeypatch.setenv("QBMOE_NO_MPAIR", env)
+        lay = layer_for(shape)
+        lay.set_weights(**{k: v for k, v in d.items() if k != "x"})
+        o = lay.forward(d["x"])
+        torch.cuda.synchronize()
+        assert lay.status() == 0
+        outs.append(o.clone())
+        lay.close()
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_bf16_layers_run_on_tensor_cores(monkeypatch):
     from qb_inputs.device import layer_for
     lay = layer_for(SMALL_BF16)
