@@ -308,6 +308,19 @@ __device__ __forceinline__ void store_e4m3_block(uint8_t* row, int F, int f, con
     if ((f & 31) == 0) row[2 * F + f / 32] = sc;
 }
 
+// Eight consecutive staged floats at row + 8 fg as two float4 loads.  The
+// threads of a quarter-warp (fg = 0..7 or 8..15) read their two halves in
+// alternating order (fg % 8 >= 4 takes the upper half first), so each of the
+// two loads covers all 32 banks once instead of half of them twice.
+__device__ __forceinline__ void ld_staged8(const float* row, int fg, float (&x8)[8]) {
+    const int sw = fg & 4;
+    const float4 p0 = *reinterpret_cast<const float4*>(row + fg * 8 + sw);
+    const float4 p1 = *reinterpret_cast<const float4*>(row + fg * 8 + (4 - sw));
+    const float4 a = sw ? p1 : p0, b = sw ? p0 : p1;
+    x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w;
+    x8[4] = b.x; x8[5] = b.y; x8[6] = b.z; x8[7] = b.w;
+}
+
 // lo_col > 0 (block-scaled, stacked token planes): the accumulator holds
 // W * hi in columns [0, n) and W * lo in [lo_col, lo_col + n); the result is
 // hi + lo * 2^-kLoShift.
@@ -348,18 +361,16 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
                     // E4M3 row: hi plane, lo plane, block scales.  Four consecutive
                     // lanes hold one token's 32-feature block (F % 32 == 0, so they
                     // agree on ok); rows past the tile's end are read but not stored.
-                    const float4 a = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8);
-                    const float4 b = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8 + 4);
-                    float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    float x8[8];
+                    ld_staged8(st + j * kStRow, fg, x8);
 #pragma unroll
                     for (int u = 0; u < 8; ++u) x8[u] = __bfloat162float(__float2bfloat16_rn(x8[u]));
                     const uint8_t sc = mx_block_scale(x8);
                     if (ok) store_e4m3_block(static_cast<uint8_t*>(sg.out) + (long long)(ti.row0 + c0 + j) * sg.ldo,
                                              sg.F, f, x8, sc);
                 } else if (ok) {
-                    const float4 a = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8);
-                    const float4 b = *reinterpret_cast<const float4*>(st + j * kStRow + fg * 8 + 4);
-                    const float x8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    float x8[8];
+                    ld_staged8(st + j * kStRow, fg, x8);
                     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) o[u] = __float2bfloat16_rn(x8[u]);
@@ -397,12 +408,9 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileInfo&
             if (ok || sg.out_e4m3) {
                 const float inv_b1 = 1.0f / p.beta1, inv_b2 = 1.0f / p.beta2;
                 const float* row = st + j * kStRow;
-                const float4 g0 = *reinterpret_cast<const float4*>(row + fg * 8);
-                const float4 g1 = *reinterpret_cast<const float4*>(row + fg * 8 + 4);
-                const float4 u0 = *reinterpret_cast<const float4*>(row + 64 + fg * 8);
-                const float4 u1 = *reinterpret_cast<const float4*>(row + 64 + fg * 8 + 4);
-                const float g8[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-                const float u8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                float g8[8], u8[8];
+                ld_staged8(row, fg, g8);
+                ld_staged8(row + 64, fg, u8);
                 float a[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) a[u] = situ_glu_hw(g8[u], u8[u], p.beta1, inv_b1, p.beta2, inv_b2);
