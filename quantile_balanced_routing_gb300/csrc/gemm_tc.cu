@@ -36,9 +36,11 @@
 // MMA, 4 x K=32 MMAs per 128-wide K sub-tile, two sub-tiles per stage on
 // 16-row token tiles).
 // Two TMEM accumulators alternate so a tile's epilogue overlaps the next
-// tile's main loop.  Every mbarrier wait is bounded: on expiry the kernel
-// records QBMOE_ETIMEOUT, stops, drains its own TMA/MMA work (bounded) and
-// frees TMEM.
+// tile's main loop.  The bf16 gate/up at 160-row token tiles runs units of
+// two m-tiles that share each stage's token tile, their accumulators taken
+// from a ring of three TMEM slots.  Every mbarrier wait is bounded: on
+// expiry the kernel records QBMOE_ETIMEOUT, stops, drains its own TMA/MMA
+// work (bounded) and frees TMEM.
 //
 // Epilogues per sub-GEMM: STORE (bf16), ROUTER (fp32 logit + offset)
 // and SITU (A tile = 64 gate rows over 64 up rows of the same features;
