@@ -223,9 +223,10 @@ int moe_qb_hist_bias(int n, const void* state, float* bias_out, qbmoe_stream_t s
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress) and sets the library's kernel attributes
- * there; make that first call before any stream capture.  All calls share the one array, so calls that may overlap on the
- * GPU (different streams, or different host threads on one device) race and
- * must be serialised by the caller.  Nothing needs to start at zero: every
+ * there; make that first call before any stream capture.  All calls share
+ * the one array, so calls that may overlap on the GPU (different streams, or
+ * different host threads on one device) race and must be serialised by the
+ * caller.  Nothing needs to start at zero: every
  * scratch region is written before it is read.
  */
 size_t qbmoe_route_noalloc_max_bytes(void);
